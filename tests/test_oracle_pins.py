@@ -1,0 +1,384 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+Each test below checks the oracle against something it does not compute itself: a library
+routine (numpy's float16), values worked by hand from the block formats (tests/golden/),
+bijections the formats imply, invariants of the q8_K pack, closed forms of special blocks,
+and brute force in f64.  A plausible slip in the oracle (a swapped scale/min, a wrong shift,
+an off-by-one sub-block, a dropped or sign-flipped min term) fails at least one of them.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from quantised_decode_mat_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---- f16 ----------------------------------------------------------------------------------------
+def test_f16_decode_matches_numpy_on_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([O.f16_to_f32(int(b)) for b in bits], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# ---- hand-worked blocks ---------------------------------------------------------------------------
+def _read_fixture(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def test_q4k_handworked_block():
+    blk = np.zeros(144, np.uint8)
+    want_w = {}
+    for tok in _read_fixture("q4k_handworked.txt"):
+        if tok[0] == "header":
+            blk[:16] = [int(t, 16) for t in tok[1:]]
+        elif tok[0] == "code":
+            blk[16 + int(tok[1])] = int(tok[2], 16)
+        elif tok[0] == "sc":
+            want_sc = [int(t) for t in tok[1:]]
+        elif tok[0] == "m":
+            want_m = [int(t) for t in tok[1:]]
+        elif tok[0] == "w":
+            want_w[int(tok[1])] = float(tok[2])
+    d, dmin, sc, m, q = O.q4k_fields(blk)
+    assert (d, dmin) == (1.0, 0.5)
+    assert list(sc) == want_sc
+    assert list(m) == want_m
+    w = O.dequant(O.FMT_Q4_K, blk)
+    for e, v in want_w.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+def test_q6k_handworked_block():
+    blk = np.zeros(210, np.uint8)
+    want_q, want_w = {}, {}
+    for tok in _read_fixture("q6k_handworked.txt"):
+        if tok[0] == "ql":
+            blk[int(tok[1])] = int(tok[2], 16)
+        elif tok[0] == "qh":
+            blk[128 + int(tok[1])] = int(tok[2], 16)
+        elif tok[0] == "scales":
+            blk[192:208] = [int(t, 16) for t in tok[1:]]
+        elif tok[0] == "d":
+            blk[208:210] = [int(t, 16) for t in tok[1:]]
+        elif tok[0] == "q":
+            want_q[int(tok[1])] = int(tok[2])
+        elif tok[0] == "w":
+            want_w[int(tok[1])] = float(tok[2])
+    d, sc, q = O.q6k_fields(blk)
+    assert d == 0.5
+    assert list(sc) == [-32, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 31]
+    for e, v in want_q.items():
+        assert q[e] == v, (e, q[e], v)
+    w = O.dequant(O.FMT_Q6_K, blk)
+    for e, v in want_w.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+# ---- bijections the formats imply -----------------------------------------------------------------
+def test_q4k_scale_bits_are_a_bijection_onto_sixteen_6bit_fields():
+    """The 12 scale bytes are 96 bits = 8 scales + 8 mins of 6 bits: every bit lands in exactly
+    one field, at exactly one bit position, and no two bits land in the same place."""
+    seen = set()
+    for bit in range(96):
+        blk = np.zeros(144, np.uint8)
+        blk[4 + bit // 8] = 1 << (bit % 8)
+        _, _, sc, m, _ = O.q4k_fields(blk)
+        fields = np.concatenate([sc, m])
+        nz = np.nonzero(fields)[0]
+        assert len(nz) == 1, (bit, fields)
+        val = int(fields[nz[0]])
+        assert val & (val - 1) == 0 and val < 64
+        seen.add((int(nz[0]), val.bit_length() - 1))
+    assert len(seen) == 96
+
+
+def _q4k_encode_scales(sc, m):
+    """Inverse of the packing: low 6 bits of sc0..3 and m0..3 in bytes 0..7; for j >= 4 the low
+    nibbles of sc_j / m_j share byte j+4 (scale low, min high) and the top two bits of sc_j / m_j
+    ride in bits 6-7 of bytes j-4 / j."""
+    s = np.zeros(12, np.uint8)
+    for j in range(4):
+        s[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        s[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+        s[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    return s
+
+
+def test_q4k_scale_min_round_trip_all_pairs():
+    rng = np.random.default_rng(7)
+    pairs = [(a, b) for a in range(64) for b in range(64)]
+    for j in range(8):
+        for a, b in pairs[:: 1 if j == 0 else 17]:
+            sc = rng.integers(0, 64, 8)
+            m = rng.integers(0, 64, 8)
+            sc[j], m[j] = a, b
+            blk = np.zeros(144, np.uint8)
+            blk[4:16] = _q4k_encode_scales(sc, m)
+            _, _, gsc, gm, _ = O.q4k_fields(blk)
+            assert list(gsc) == list(sc) and list(gm) == list(m)
+
+
+def test_q4k_code_nibbles_are_a_bijection_onto_elements():
+    owner = {}
+    for byte in range(128):
+        for nib in range(2):
+            blk = np.zeros(144, np.uint8)
+            blk[16 + byte] = 1 << (4 * nib)
+            _, _, _, _, q = O.q4k_fields(blk)
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and q[nz[0]] == 1
+            owner[(byte, nib)] = int(nz[0])
+    assert sorted(owner.values()) == list(range(256))
+    # consecutive bytes feed consecutive elements of one 32-element sub-block
+    for byte in range(127):
+        if byte % 32 != 31:
+            assert owner[(byte + 1, 0)] == owner[(byte, 0)] + 1
+            assert owner[(byte + 1, 0)] // 32 == owner[(byte, 0)] // 32
+
+
+def test_q6k_code_bits_are_a_bijection_onto_elements():
+    low_owner, high_owner = {}, {}
+    for byte in range(128):
+        for nib in range(2):
+            blk = np.zeros(210, np.uint8)
+            blk[byte] = 1 << (4 * nib)
+            _, _, q = O.q6k_fields(blk)
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and q[nz[0]] == 1
+            low_owner[(byte, nib)] = int(nz[0])
+    for byte in range(64):
+        for pair in range(4):
+            blk = np.zeros(210, np.uint8)
+            blk[128 + byte] = 1 << (2 * pair)
+            _, _, q = O.q6k_fields(blk)
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1 and q[nz[0]] == 16
+            high_owner[(byte, pair)] = int(nz[0])
+    assert sorted(low_owner.values()) == list(range(256))
+    assert sorted(high_owner.values()) == list(range(256))
+
+
+def test_q6k_scale_index_is_element_over_16():
+    for s in range(16):
+        blk = np.zeros(210, np.uint8)
+        blk[208:210] = [0x00, 0x3C]  # d = 1
+        blk[192 + s] = 1  # only scale s is 1; all codes 0 -> w = -32 exactly where e/16 == s
+        w = O.dequant(O.FMT_Q6_K, blk)
+        assert np.array_equal(np.nonzero(w)[0], np.arange(16 * s, 16 * s + 16))
+        assert np.all(w[16 * s: 16 * s + 16] == -32.0)
+
+
+# ---- q8_K invariants -------------------------------------------------------------------------------
+def _pack_cases():
+    rng = np.random.default_rng(11)
+    xs = [synth.activations(0, 3, 2048)]
+    xs.append((rng.standard_normal((2, 1024)) * 1e-3).astype(np.float32))
+    xs.append((rng.standard_normal((1, 512)) * 1e4).astype(np.float32))
+    spiky = rng.standard_normal((1, 768)).astype(np.float32)
+    spiky[0, 5] = 80.0
+    spiky[0, 300] = -40.0
+    xs.append(spiky)
+    return xs
+
+
+@pytest.mark.parametrize("x", _pack_cases())
+def test_q8k_invariants(x):
+    qs, d, bs = O.q8k_pack(x)
+    batch, K = x.shape
+    nb = K // 256
+    xb = x.reshape(batch, nb, 256).astype(np.float64)
+    qb = qs.reshape(batch, nb, 256).astype(np.int64)
+    # eight sums of 32 codes each
+    assert np.array_equal(bs.astype(np.int64), qb.reshape(batch, nb, 8, 32).sum(-1))
+    # codes in range, argmax maps to +-127 with the sign of x
+    assert qb.min() >= -127 and qb.max() <= 127
+    am = np.abs(xb).argmax(-1)
+    top = np.take_along_axis(qb, am[..., None], -1)[..., 0]
+    topx = np.take_along_axis(xb, am[..., None], -1)[..., 0]
+    assert np.array_equal(top, np.where(topx > 0, 127, -127))
+    # d = amax / 127 to f32 rounding, and reconstruction error at most half a step
+    amax = np.abs(xb).max(-1)
+    assert np.allclose(d.astype(np.float64), amax / 127.0, rtol=2 ** -23, atol=0)
+    err = np.abs(xb - d[..., None].astype(np.float64) * qb)
+    assert np.all(err <= d[..., None] * (0.5 + 2 ** -20))
+
+
+def test_q8k_zero_block_and_exact_multiples():
+    x = np.zeros((1, 512), np.float32)
+    c = 2.0 ** -5
+    k = np.arange(-127, 129, dtype=np.int64)[:256]
+    k[-1] = 127
+    x[0, 256:] = (k * c).astype(np.float32)
+    qs, d, bs = O.q8k_pack(x)
+    assert d[0, 0] == 0 and not qs[0, :256].any() and not bs[0, 0].any()
+    assert d[0, 1] == np.float32(c)  # amax = 127c, d = 127c/127 exactly for a power-of-two c
+    assert np.array_equal(qs[0, 256:].astype(np.int64), k)
+
+
+def test_q8k_rounds_half_to_even():
+    x = np.zeros((1, 256), np.float32)
+    x[0, 0] = 127.0  # amax = 127 -> iscale = 1 exactly, so codes are rint(x)
+    x[0, 1:7] = [2.5, 3.5, -2.5, -3.5, 0.5, 1.5]
+    qs, d, _ = O.q8k_pack(x)
+    assert d[0, 0] == 1.0
+    assert list(qs[0, :7]) == [127, 2, 4, -2, -4, 0, 2]
+
+
+# ---- integer dots: brute force and closed forms -----------------------------------------------------
+def test_subdots_brute_force_tiny():
+    x = synth.activations(5, 1, 512)
+    qs, _, _ = O.q8k_pack(x)
+    for fmt in (O.FMT_Q4_K, O.FMT_Q6_K):
+        W = synth.weights("q4k" if fmt == O.FMT_Q4_K else "q6k", 5, 3, 512)
+        for r in range(3):
+            dots = O.subdots(fmt, W[r], qs[0])
+            for b in range(2):
+                if fmt == O.FMT_Q4_K:
+                    _, _, _, _, q = O.q4k_fields(W[r, b])
+                    ref = [int(np.dot(q[32 * j:32 * j + 32], qs[0, 256 * b + 32 * j: 256 * b + 32 * j + 32].astype(np.int64)))
+                           for j in range(8)]
+                else:
+                    _, _, q = O.q6k_fields(W[r, b])
+                    ref = [int(np.dot(q[16 * s:16 * s + 16] - 32, qs[0, 256 * b + 16 * s: 256 * b + 16 * s + 16].astype(np.int64)))
+                           for s in range(16)]
+                assert list(dots[b]) == ref
+
+
+def _q4k_uniform_block(d_bits, dmin_bits, sc, m, code):
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = [d_bits & 255, d_bits >> 8]
+    blk[2:4] = [dmin_bits & 255, dmin_bits >> 8]
+    blk[4:16] = _q4k_encode_scales([sc] * 8, [m] * 8)
+    blk[16:] = code | (code << 4)
+    return blk
+
+
+def test_q4k_unit_scales_reduce_to_a_plain_code_dot():
+    """sc = 1, m = 0, every code c: y = sum_b dx_b * d * c * sum(q8 of block b)."""
+    x = synth.activations(9, 1, 1024)
+    qs, xd, bs = O.q8k_pack(x)
+    for c in (0, 1, 7, 15):
+        row = np.stack([_q4k_uniform_block(0x3C00, 0x3800, 1, 0, c)] * 4)[None]
+        y = O.qmatvec(O.FMT_Q4_K, row, qs, xd, bs)
+        ref = sum(float(xd[0, b]) * c * int(qs[0, 256 * b:256 * b + 256].astype(np.int64).sum()) for b in range(4))
+        assert np.isclose(y[0, 0], ref, rtol=1e-6, atol=1e-6)
+
+
+def test_q4k_zero_codes_reduce_to_minus_dmin_min_term():
+    """All codes zero: y = -sum_b dx_b * dmin_b * sum_j m_j * bsum_j (the bsums carry it)."""
+    x = synth.activations(3, 2, 2048)
+    qs, xd, bs = O.q8k_pack(x)
+    W = synth.q4k_weights(3, 5, 2048).copy()
+    W[:, :, 16:] = 0
+    y = O.qmatvec(O.FMT_Q4_K, W, qs, xd, bs)
+    for v in range(2):
+        for r in range(5):
+            ref = 0.0
+            for b in range(8):
+                _, dmin, _, m, _ = O.q4k_fields(W[r, b])
+                ref -= float(xd[v, b]) * dmin * int(np.dot(m, bs[v, b].astype(np.int64)))
+            assert np.isclose(y[v, r], ref, rtol=1e-5, atol=0)
+
+
+def test_q6k_special_blocks():
+    x = synth.activations(4, 1, 768)
+    qs, xd, bs = O.q8k_pack(x)
+    nb = 3
+    # every code 32 (ql nibbles 0, qh pairs 2): y = 0 exactly
+    blk = np.zeros(210, np.uint8)
+    blk[128:192] = 0xAA
+    blk[192:208] = 5
+    blk[208:210] = [0x00, 0x3C]
+    y = O.qmatvec(O.FMT_Q6_K, np.stack([blk] * nb)[None], qs, xd, bs)
+    assert y[0, 0] == 0.0
+    # unit scales, d = 1, every code a + 16h: y = sum_b dx_b * (a + 16h - 32) * sum(q8 of block b)
+    for a, h in ((0, 0), (15, 3), (7, 1)):
+        blk = np.zeros(210, np.uint8)
+        blk[0:128] = a | (a << 4)
+        blk[128:192] = h * 0x55
+        blk[192:208] = 1
+        blk[208:210] = [0x00, 0x3C]
+        y = O.qmatvec(O.FMT_Q6_K, np.stack([blk] * nb)[None], qs, xd, bs)
+        ref = sum(float(xd[0, b]) * (a + 16 * h - 32) * int(qs[0, 256 * b:256 * b + 256].astype(np.int64).sum())
+                  for b in range(nb))
+        assert np.isclose(y[0, 0], ref, rtol=1e-6, atol=1e-6)
+
+
+# ---- f32 epilogue against the f64 brute force and the closed-form bound ------------------------------
+@pytest.mark.parametrize("fmt,K,rows,batch", [(O.FMT_Q4_K, 2048, 16, 2), (O.FMT_Q6_K, 1792, 12, 3)])
+def test_epilogue_against_f64_brute_force(fmt, K, rows, batch):
+    name = "q4k" if fmt == O.FMT_Q4_K else "q6k"
+    W = synth.weights(name, 21, rows, K)
+    x = synth.activations(21, batch, K)
+    qs, xd, bs = O.q8k_pack(x)
+    y64 = O.qmatvec_f64(fmt, W, qs, xd)
+    for order in (O.ORDER_SEQUENTIAL, O.ORDER_GROUPS_OF_FOUR):
+        y = O.qmatvec(fmt, W, qs, xd, bs, order)
+        assert O.rel_err(y, y64).max() < 2e-3
+        assert O.rel_err(y, y64).max() < 1e-5  # much tighter in practice: f32 rounding only
+    # against raw x: |y64 - sum w x| <= sum |w| * dx / 2
+    nb = K // 256
+    for v in range(batch):
+        for r in range(rows):
+            w = np.concatenate([O.dequant(fmt, W[r, b]) for b in range(nb)])
+            exact = float(np.dot(w, x[v].astype(np.float64)))
+            bound = float(np.dot(np.abs(w), np.repeat(xd[v].astype(np.float64), 256))) * 0.5 * (1 + 2 ** -20)
+            assert abs(y64[v, r] - exact) <= bound + 1e-12
+
+
+def test_orders_differ_only_in_rounding():
+    W = synth.weights("q4k", 8, 64, 4096)
+    x = synth.activations(8, 1, 4096)
+    qs, xd, bs = O.q8k_pack(x)
+    y0 = O.qmatvec(O.FMT_Q4_K, W, qs, xd, bs, O.ORDER_SEQUENTIAL)
+    y1 = O.qmatvec(O.FMT_Q4_K, W, qs, xd, bs, O.ORDER_GROUPS_OF_FOUR)
+    # two f32 summation orders of n terms differ by at most 2 (n - 1) u sum|t| (u = 2^-24)
+    for r in range(64):
+        t = O.block_terms(O.FMT_Q4_K, W[r], qs[0], xd[0], bs[0]).astype(np.float64)
+        assert abs(float(y1[0, r]) - float(y0[0, r])) <= 2 * 15 * 2.0 ** -24 * np.abs(t).sum()
+    # the grouped order is the stated tree over the block terms
+    for r in range(4):
+        t = O.block_terms(O.FMT_Q4_K, W[r], qs[0], xd[0], bs[0]).astype(np.float32)
+        groups = [(t[4 * g] + t[4 * g + 1]) + (t[4 * g + 2] + t[4 * g + 3]) for g in range(4)]
+        acc = groups[0]
+        for G in groups[1:]:
+            acc = np.float32(acc + G)
+        assert acc == y1[0, r]
+
+
+def test_q6k_split_round_trip():
+    g = synth.q6k_weights(2, 6, 1792)
+    body, prefix = O.q6k_split(g, prefix_stride=8)
+    rebuilt = np.concatenate([body, prefix[:, :7].view(np.uint8).reshape(6, 7, 2)], axis=2)
+    assert np.array_equal(rebuilt, g)
+    assert not prefix[:, 7:].any()
+
+
+def test_golden_regression():
+    """Stored oracle outputs (written by tests/golden/make_golden.py, which calls only the oracle)."""
+    path = os.path.join(GOLDEN, "oracle_regression.txt")
+    from tests.golden.make_golden import compute
+    stored = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, hexs = line.split(":", 1)
+            stored[key.strip()] = hexs.split()
+    now = compute()
+    assert set(now) == set(stored)
+    for k in now:
+        assert now[k] == stored[k], k
