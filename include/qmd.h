@@ -1,0 +1,240 @@
+/*
+ * qmd.h -- C ABI of libqmd: decode-time Q4_K / Q6_K x q8_K matrix-vector products on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Language models on the device: the cajeta-llm kernels", §1 and §2.1-2.2):
+ * activations are quantised on the device to q8_K (256 values a block, one scale and eight
+ * sub-block sums); each output row is an integer dot product of the row's GGUF K-quant weight
+ * blocks against those bytes, with the per-sub-block scales and mins folded in through a
+ * rank-one epilogue; batched decode dots one pass over a weight row against up to 8
+ * activation columns.  At bind, a Q6_K weight is split into a scale prefix plus 208-byte
+ * bodies and a Q4_K slab is read in place as 32-bit words (§1).
+ *
+ * Conventions for every call
+ *  - All pointers to tensors are DEVICE pointers, owned by the caller, who also owns the
+ *    stream.  The library allocates no device or host memory, keeps no per-call state, and
+ *    never synchronises the stream (except qmd_get_device_error, which says so).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls
+ *    are asynchronous; buffers must stay live until the stream has passed the work.
+ *  - Arguments are validated on the host before anything is launched.  A call that returns
+ *    anything but QMD_OK has launched nothing and written nothing.  There is no fallback:
+ *    a refused call returns its named reason ("One kernel, any device", §1, the seven named
+ *    launch refusals; "Kernel SPI and the selection algorithm", "Why a kernel declines").
+ *  - Layouts are batch-major and row-major; K is the reduction length (columns of W), a
+ *    multiple of 256; nb = K / 256.
+ *  - Launch order: qmd_q8k_pack and qmd_qmatvec are launched as programmatic dependents of
+ *    the preceding kernel in the stream.  Before waiting for that kernel to finish they read
+ *    only the weight buffers (W, W_aux); everything else is read and written after it has
+ *    finished.  Weights therefore must not be written by the kernel launched immediately
+ *    before them in the same stream unless that kernel signals completion only by exiting
+ *    (every kernel not written for programmatic launch does; so do this library's bind calls).
+ */
+#ifndef QMD_H
+#define QMD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMD_QK 256        /* values per K-quant and q8_K block */
+#define QMD_MAX_BATCH 8   /* activation columns per weight pass */
+#define QMD_Q4K_BLOCK_BYTES 144
+#define QMD_Q6K_BLOCK_BYTES 210
+#define QMD_Q6K_BODY_BYTES 208
+
+typedef enum qmd_status {
+    QMD_OK = 0,
+    QMD_ERR_NULL = 1,                  /* a required pointer is NULL */
+    QMD_ERR_FORMAT = 2,                /* unknown weight format */
+    QMD_ERR_K_NOT_MULTIPLE_OF_256 = 3, /* K % 256 != 0 */
+    QMD_ERR_BATCH = 4,                 /* batch outside [1, QMD_MAX_BATCH] */
+    QMD_ERR_MISALIGNED = 5,            /* a pointer is not aligned as the call requires */
+    QMD_ERR_SHAPE = 6,                 /* rows < 1, K < 256, K above the call's limit, or a size overflow */
+    QMD_ERR_LAUNCH = 7,                /* the CUDA runtime refused the launch (see qmd_last_error_detail) */
+    QMD_ERR_DEVICE_TIMEOUT = 8,        /* a bounded wait inside a kernel gave up (qmd_get_device_error) */
+    QMD_ERR_DEVICE = 9                 /* no usable CUDA device, or it is not an sm_103 part */
+} qmd_status;
+
+/* Weight formats, named by their GGUF type ids. */
+typedef enum qmd_fmt {
+    QMD_Q4_K = 12,       /* canonical GGUF Q4_K blocks, used in place (viewed as 32-bit words) */
+    QMD_Q6_K_SPLIT = 14  /* GGUF Q6_K after qmd_bind_q6k: 208-byte bodies + f16 scale prefix */
+} qmd_fmt;
+
+/* A batch of q8_K-packed activation vectors, all device pointers, batch-major:
+ *   qs    int8  [batch][K]       the codes, x ~= d * q, q in [-127, 127]
+ *   d     f32   [batch][nb]      one scale per 256-value block
+ *   bsums int16 [batch][nb][8]   sum of the 32 codes of each sub-block                   */
+typedef struct qmd_q8k {
+    int8_t *qs;
+    float *d;
+    int16_t *bsums;
+} qmd_q8k;
+
+typedef struct qmd_q8k_const {
+    const int8_t *qs;
+    const float *d;
+    const int16_t *bsums;
+} qmd_q8k_const;
+
+/*
+ * qmd_q8k_pack -- quantise `batch` f32 vectors of length K to q8_K
+ * ("Language models on the device: the cajeta-llm kernels", §1: q8kPackKernel, 256 values a
+ * block, one scale and eight sub-block sums).
+ *
+ * Per 256-value block, all in f32: amax = max |x|; if amax == 0 then d = 0 and every code and
+ * sum is 0; otherwise q = clamp(round_to_nearest_even(x * (127 / amax)), -127, 127) (the
+ * quotient and the product each rounded to f32) and d = amax / 127; bsums[j] is the sum of
+ * codes 32j .. 32j+31.  In a block so small that 127/amax overflows to infinity, nonzero
+ * values get +-127 and zeros get 0 (their product 0 * inf is NaN, whose code is 0).
+ * Non-finite inputs are outside the contract (no fault, result unspecified).
+ *
+ *   x   f32 [batch][K], 16-byte aligned          (read)
+ *   xq  qs and bsums 16-byte aligned, d 4-byte    (written)
+ * Errors: NULL, K_NOT_MULTIPLE_OF_256, SHAPE (K < 256 or batch*K overflows), BATCH,
+ * MISALIGNED, DEVICE, LAUNCH.
+ */
+qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *stream);
+
+/*
+ * qmd_qmatvec -- y[v][r] = sum over the row's blocks of the rank-one epilogue of integer
+ * sub-block dots, for v < batch, r < rows
+ * ("Language models on the device: the cajeta-llm kernels", §1, §2.1 one row finished by a
+ * reduction; §2.2 the batched "Cols" form: one pass over a weight row serves all columns).
+ *
+ * Per 256-value block b of row r against vector v (exact int32 S and M, f32 elsewhere, each
+ * operation rounded on its own):
+ *   Q4_K:        S = sum_j sc_j * dot_j,  M = sum_j m_j * bsums[v][b][j]   (j = 0..7, 32 values)
+ *                term = d_x * ( f32(d) * (float)S - f32(dmin) * (float)M )
+ *   Q6_K_SPLIT:  S = sum_s sc_s * dot'_s, dot'_s over 16 values of (q - 32) * q8   (s = 0..15)
+ *                term = d_x * ( f32(d) * (float)S )
+ * and the row's terms are summed in f32 in this order: blocks in groups of four, each group
+ * (t0 + t1) + (t2 + t3) with absent blocks past the row's end counted as +0, then the group
+ * sums left to right.  y is overwritten, not accumulated.
+ *
+ *   fmt    QMD_Q4_K or QMD_Q6_K_SPLIT
+ *   W      Q4_K: GGUF blocks u8 [rows][nb][144] (16-byte aligned; read in place as u32 words)
+ *          Q6_K_SPLIT: bodies u8 [rows][nb][208] from qmd_bind_q6k (16-byte aligned)
+ *   W_aux  Q4_K: ignored (may be NULL).  Q6_K_SPLIT: the f16 scale prefix from qmd_bind_q6k,
+ *          [rows][qmd_q6k_prefix_stride(K)] (16-byte aligned)
+ *   xq     packed activations for `batch` vectors of length K (qs, bsums 16-byte aligned,
+ *          d 4-byte aligned; bsums may be NULL for Q6_K_SPLIT, which does not read them)
+ *   y      f32 [batch][rows], 4-byte aligned (written)
+ * Limits: 1 <= batch <= 8; K <= 32768 for batch <= 2, K <= 16384 for batch > 2.
+ * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, DEVICE, LAUNCH.
+ * Device-side bounded waits that give up set a flag read by qmd_get_device_error.
+ */
+qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
+                       int64_t rows, int64_t K, int batch, void *stream);
+
+/*
+ * qmd_q6k_prefix_stride -- entries (f16) per row of the Q6_K scale prefix: nb rounded up to
+ * a multiple of 8, so that every prefix row starts on a 16-byte boundary.  0 if K is not a
+ * positive multiple of 256.
+ */
+int64_t qmd_q6k_prefix_stride(int64_t K);
+
+/*
+ * qmd_q6k_split_bytes -- sizes of the two buffers qmd_bind_q6k writes:
+ *   body   rows * nb * 208 bytes,  prefix   rows * qmd_q6k_prefix_stride(K) * 2 bytes.
+ * ("Language models on the device: the cajeta-llm kernels", §1: scale prefix plus 208-byte
+ * bodies.)  Errors: NULL, K_NOT_MULTIPLE_OF_256, SHAPE.
+ */
+qmd_status qmd_q6k_split_bytes(int64_t rows, int64_t K, size_t *body_bytes, size_t *prefix_bytes);
+
+/*
+ * qmd_bind_q6k -- bind-time relayout of a canonical GGUF Q6_K slab ("Language models on the
+ * device: the cajeta-llm kernels", §1 and §2.6 split relayouts).  Each 210-byte block
+ * (ql 128 B, qh 64 B, 16 int8 scales, f16 d) becomes a 208-byte body holding the first 208
+ * bytes unchanged, and its f16 d goes to prefix[r][b]; prefix padding entries are zero.
+ * Run once at load ("Kernel SPI and the selection algorithm": relayout once at load, never
+ * per call).
+ *   gguf    u8 [rows][nb][210], 2-byte aligned (read)
+ *   body    u8 [rows][nb][208], 16-byte aligned (written)
+ *   prefix  f16 [rows][qmd_q6k_prefix_stride(K)], 16-byte aligned (written)
+ * The three buffers must not overlap.
+ * Errors: NULL, K_NOT_MULTIPLE_OF_256, SHAPE, MISALIGNED, DEVICE, LAUNCH.
+ */
+qmd_status qmd_bind_q6k(const void *gguf, void *body, void *prefix, int64_t rows, int64_t K,
+                        void *stream);
+
+/*
+ * qmd_bind_q4k -- the Q4_K bind is a view: the GGUF slab u8 [rows][nb][144] is read in place
+ * as u32 [rows][nb][36] ("Language models on the device: the cajeta-llm kernels", §1: a Q4_K
+ * slab is viewed as 32-bit words).  This call copies nothing; it checks that the slab can be
+ * so viewed (16-byte aligned, K a multiple of 256, size without overflow).
+ * Errors: NULL, K_NOT_MULTIPLE_OF_256, SHAPE, MISALIGNED.
+ */
+qmd_status qmd_bind_q4k(const void *gguf, int64_t rows, int64_t K);
+
+/* Name of a status code (static string). */
+const char *qmd_status_str(qmd_status s);
+
+/* Detail of the last QMD_ERR_LAUNCH / QMD_ERR_DEVICE on the calling thread (static or
+ * thread-local string; empty if none). */
+const char *qmd_last_error_detail(void);
+
+/*
+ * qmd_get_device_error -- synchronises `stream`, then reads and clears the current device's
+ * error word, which kernels set when a bounded wait (on an asynchronous copy) gives up instead
+ * of hanging.  Returns QMD_ERR_DEVICE_TIMEOUT if it was set, QMD_ERR_LAUNCH if the stream
+ * reported a CUDA error, else QMD_OK.  ("One kernel, any device", §1: a refused launch is
+ * returned with its reason, never dropped.)
+ */
+qmd_status qmd_get_device_error(void *stream);
+
+/*
+ * qmd_set_wait_limit_ns -- the time after which a bounded wait inside a kernel gives up
+ * (default 1e9 ns).  Process-wide; applies to launches made after the call.
+ */
+void qmd_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * qmd_qmatvec_launch_info -- the launch qmd_qmatvec would make for these sizes on the current
+ * device: grid (CTAs), threads per CTA, dynamic shared bytes, pipeline stages, rows per
+ * stage.  Any output pointer may be NULL.  Errors as qmd_qmatvec's shape checks.
+ */
+qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int batch, int *grid,
+                                   int *threads, int *smem_bytes, int *stages, int *rows_per_stage);
+
+/* ---- test-only entry points (same kernels, extra outputs) --------------------------------- */
+
+/*
+ * qmd_debug_qmatvec_dump -- qmd_qmatvec plus a record of its integer arithmetic, from the
+ * same kernel code with extra stores.
+ *   dots  int32 [batch][rows][nb][16]:
+ *         Q4_K: entry 4c + 2h + u is the dot of the 16 elements (half h of the 32) of
+ *               sub-block 2c + u; Q6_K_SPLIT: entry s is dot'_s of group s.
+ *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K) M; M = 0 for Q6_K_SPLIT.
+ * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm.
+ */
+qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,
+                                  float *y, int64_t rows, int64_t K, int batch, int32_t *dots,
+                                  int32_t *sm, void *stream);
+
+/*
+ * qmd_debug_wait_timeout -- launches one CTA that waits, with the given limit, on a
+ * shared-memory barrier that nothing completes; the wait gives up, sets the device error
+ * word and the kernel returns.  Used to test the bounded-wait path without hanging a GPU.
+ */
+qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * qmd_debug_set_plan -- override the mat-vec launch plan for launches made after the call:
+ * row groups per CTA, CTAs per multiprocessor, and a cap on pipeline stages (0 = the default
+ * for each).  Results do not depend on the plan; tests use this to drive the stage ring
+ * through many wrap-arounds on small inputs.  Process-wide.
+ */
+void qmd_debug_set_plan(int row_groups, int ctas_per_sm, int max_stages);
+
+/* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
+int qmd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMD_H */

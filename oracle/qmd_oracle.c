@@ -152,7 +152,8 @@ void oracle_q6k_dequant(const uint8_t *blk, double *w)
  * Per 256-value block: amax = max |x|; if amax == 0 everything is 0; otherwise
  * iscale = 127/amax (f32 division), q = clamp(rint(x * iscale), -127, 127) with the product
  * rounded to f32 first and rint to nearest-even, d = amax / 127 (f32 division), and
- * bsums[j] = sum of the 32 codes of sub-block j. */
+ * bsums[j] = sum of the 32 codes of sub-block j.  A product that is NaN (x = 0 in a block so
+ * small that 127/amax overflows to infinity) gives code 0. */
 void oracle_q8k_pack(const float *x, int64_t K, int8_t *qs, float *d, int16_t *bsums)
 {
     for (int64_t b = 0; b < K / QK; ++b) {
@@ -174,7 +175,8 @@ void oracle_q8k_pack(const float *x, int64_t K, int8_t *qs, float *d, int16_t *b
         float iscale = 127.0f / amax;
         for (int i = 0; i < QK; ++i) {
             float v = xb[i] * iscale;
-            float r = nearbyintf(v); /* default rounding mode: nearest, ties to even */
+            /* 127/amax overflows to +inf when amax < 127/FLT_MAX; then 0 * inf is NaN: code 0 */
+            float r = isnan(v) ? 0.0f : nearbyintf(v); /* nearest, ties to even */
             if (r > 127.0f)
                 r = 127.0f;
             if (r < -127.0f)

@@ -1,0 +1,404 @@
+// api.cu -- the C ABI of libqmd: argument validation, launch planning, the device error word.
+//
+// Every entry point validates its arguments on the host and returns a named status before
+// anything is launched ("One kernel, any device", §1: a refused launch carries one of seven
+// named reasons; "Kernel SPI and the selection algorithm", "Why a kernel declines": a K-quant
+// tensor whose last dimension is not a multiple of 256 is rejected).  There is no fallback
+// path: a refused call does nothing.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "qmv.cuh"
+
+namespace qmd {
+
+// One word per device, set by kernels whose bounded waits give up.  A file-scope device
+// variable: the library never allocates.
+static __device__ unsigned int g_error_word;
+
+static thread_local char g_detail[320];
+static std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+static std::atomic<int> g_force_rg{0}, g_force_cps{0}, g_force_stages{0};
+
+qmd_status fail(qmd_status st, const char *what, cudaError_t e)
+{
+    snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    (void)cudaGetLastError();  // clear a non-sticky launch error
+    return st;
+}
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+qmd_status current_device(DeviceInfo *out)
+{
+    static DeviceInfo cache[64];
+    static std::atomic<bool> have[64];
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(QMD_ERR_DEVICE, "cudaGetDevice", e);
+    if (dev < 0 || dev >= 64)
+        return QMD_ERR_DEVICE;
+    if (!have[dev].load(std::memory_order_acquire)) {
+        DeviceInfo d = {};
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return fail(QMD_ERR_DEVICE, "cudaDeviceGetAttribute", e);
+        if (d.cc_major != 10 || d.cc_minor != 3) {
+            snprintf(g_detail, sizeof g_detail, "device %d is sm_%d%d; libqmd is built for sm_103a only", dev,
+                     d.cc_major, d.cc_minor);
+            return QMD_ERR_DEVICE;
+        }
+        cache[dev] = d;
+        have[dev].store(true, std::memory_order_release);
+    }
+    *out = cache[dev];
+    return QMD_OK;
+}
+
+unsigned *device_error_word()
+{
+    static unsigned *addr[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) {
+            fail(QMD_ERR_DEVICE, "cudaGetSymbolAddress(error word)", e);
+            return nullptr;
+        }
+        addr[dev] = static_cast<unsigned *>(p);
+    }
+    return addr[dev];
+}
+
+qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
+{
+    const bool q6 = fmt == QMD_Q6_K_SPLIT;
+    const int max_threads = batch <= 2 ? 1024 : 512;  // the kernels' launch bounds
+    const int WR = (nb + 3) / 4;                       // warps per row: 4 blocks per warp
+    if (WR * 32 > max_threads)
+        return QMD_ERR_SHAPE;
+    const int PR = (8 / batch) > 0 ? 8 / batch : 1;  // must match Tiling<B>::PR
+    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (8 / PR > 0 ? 8 / PR : 1);
+    if (RG * WR * 32 > max_threads)
+        RG = max_threads / (WR * 32);
+    if (RG < 1)
+        RG = 1;
+    const int TR = RG * PR;
+    const int row_bytes = nb * (q6 ? 208 : 144);
+    const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
+    const int64_t sb64 = (int64_t)TR * (row_bytes + pre_bytes);
+    if (sb64 > dev.smem_optin)
+        return QMD_ERR_SHAPE;
+    const int stage_bytes = align_up((int)sb64, 128);
+    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / (RG * WR) > 0 ? 16 / (RG * WR) : 1);
+    for (;; --cps) {
+        if (cps < 1)
+            return QMD_ERR_SHAPE;
+        int budget = dev.smem_per_sm / cps - 1024;
+        if (budget > dev.smem_optin)
+            budget = dev.smem_optin;
+        int64_t grid = (int64_t)dev.sm_count * cps;
+        if (grid > rows)
+            grid = rows;
+        const int64_t rows_per_cta = (rows + grid - 1) / grid;
+        const int64_t chunks = (rows_per_cta + TR - 1) / TR;
+        const int fixed = qmv_smem_layout(0, stage_bytes, batch, nb, !q6, RG, WR).total + 8 * 8;
+        int64_t stages = (budget - fixed) / stage_bytes;
+        if (stages > 8)
+            stages = 8;
+        if (stages > chunks)
+            stages = chunks;
+        if (g_force_stages.load() > 0 && stages > g_force_stages.load())
+            stages = g_force_stages.load();
+        if (stages < 1)
+            continue;
+        pl->grid = (int)grid;
+        pl->threads = RG * WR * 32;
+        pl->stages = (int)stages;
+        pl->smem = qmv_smem_layout((int)stages, stage_bytes, batch, nb, !q6, RG, WR).total;
+        pl->rows_per_stage = TR;
+        pl->WR = WR;
+        pl->RG = RG;
+        pl->PR = PR;
+        pl->row_bytes = row_bytes;
+        pl->pre_bytes = pre_bytes;
+        pl->stage_bytes = stage_bytes;
+        return QMD_OK;
+    }
+}
+
+// Test-only: one CTA waits on a barrier nothing completes, gives up after limit_ns, flags it.
+__global__ void debug_wait_kernel(unsigned *err, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(b, 0, limit_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0)
+        atomicOr(err, ERRBIT_DEBUG_WAIT);
+}
+
+}  // namespace qmd
+
+using namespace qmd;
+
+namespace {
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmd_status check_k(int64_t K)
+{
+    if (K < QMD_QK)
+        return K > 0 && K % QMD_QK != 0 ? QMD_ERR_K_NOT_MULTIPLE_OF_256 : QMD_ERR_SHAPE;
+    if (K % QMD_QK != 0)
+        return QMD_ERR_K_NOT_MULTIPLE_OF_256;
+    if (K / QMD_QK > (1 << 20))
+        return QMD_ERR_SHAPE;
+    return QMD_OK;
+}
+
+qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
+                          int64_t rows, int64_t K, int batch, int32_t *dots, int32_t *sm, bool dump,
+                          void *stream)
+{
+    if (fmt != QMD_Q4_K && fmt != QMD_Q6_K_SPLIT)
+        return QMD_ERR_FORMAT;
+    const bool q6 = fmt == QMD_Q6_K_SPLIT;
+    if (!W || !xq.qs || !xq.d || !y || (q6 && !W_aux) || (!q6 && !xq.bsums) || (dump && (!dots || !sm)))
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return QMD_ERR_BATCH;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    const int nb = (int)(K / QMD_QK);
+    if (!aligned(W, 16) || (q6 && !aligned(W_aux, 16)) || !aligned(xq.qs, 16) ||
+        (!q6 && !aligned(xq.bsums, 16)) || !aligned(xq.d, 4) || !aligned(y, 4) ||
+        (dump && (!aligned(dots, 16) || !aligned(sm, 16))))
+        return QMD_ERR_MISALIGNED;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return st;
+    QmvPlan plan;
+    if ((st = qmv_plan(fmt, rows, nb, batch, dev, &plan)) != QMD_OK)
+        return st;
+    QmvArgs a;
+    a.fmt = fmt;
+    a.W = static_cast<const uint8_t *>(W);
+    a.Wpre = static_cast<const uint8_t *>(W_aux);
+    a.xqs = xq.qs;
+    a.xd = xq.d;
+    a.xbs = xq.bsums;
+    a.y = y;
+    a.rows = rows;
+    a.nb = nb;
+    a.batch = batch;
+    a.dbg_dots = dump ? dots : nullptr;
+    a.dbg_sm = dump ? sm : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return q6 ? launch_qmv_q6k(a, plan, s) : launch_qmv_q4k(a, plan, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *stream)
+{
+    if (!x || !xq.qs || !xq.d || !xq.bsums)
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return QMD_ERR_BATCH;
+    if (!aligned(x, 16) || !aligned(xq.qs, 16) || !aligned(xq.bsums, 16) || !aligned(xq.d, 4))
+        return QMD_ERR_MISALIGNED;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return st;
+    return launch_q8k_pack(x, xq.qs, xq.d, xq.bsums, (int64_t)batch * (K / QMD_QK),
+                           static_cast<cudaStream_t>(stream));
+}
+
+qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
+                       int64_t rows, int64_t K, int batch, void *stream)
+{
+    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, nullptr, nullptr, false, stream);
+}
+
+qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,
+                                  float *y, int64_t rows, int64_t K, int batch, int32_t *dots,
+                                  int32_t *sm, void *stream)
+{
+    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, dots, sm, true, stream);
+}
+
+int64_t qmd_q6k_prefix_stride(int64_t K)
+{
+    if (K <= 0 || K % QMD_QK != 0)
+        return 0;
+    return (K / QMD_QK + 7) / 8 * 8;
+}
+
+qmd_status qmd_q6k_split_bytes(int64_t rows, int64_t K, size_t *body_bytes, size_t *prefix_bytes)
+{
+    if (!body_bytes || !prefix_bytes)
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    const int64_t nb = K / QMD_QK;
+    *body_bytes = (size_t)(rows * nb * QMD_Q6K_BODY_BYTES);
+    *prefix_bytes = (size_t)(rows * qmd_q6k_prefix_stride(K) * 2);
+    return QMD_OK;
+}
+
+qmd_status qmd_bind_q6k(const void *gguf, void *body, void *prefix, int64_t rows, int64_t K, void *stream)
+{
+    if (!gguf || !body || !prefix)
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    if (!aligned(gguf, 2) || !aligned(body, 16) || !aligned(prefix, 16))
+        return QMD_ERR_MISALIGNED;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return st;
+    return launch_q6k_split(static_cast<const uint8_t *>(gguf), static_cast<uint8_t *>(body),
+                            static_cast<uint16_t *>(prefix), rows, (int)(K / QMD_QK),
+                            qmd_q6k_prefix_stride(K), static_cast<cudaStream_t>(stream));
+}
+
+qmd_status qmd_bind_q4k(const void *gguf, int64_t rows, int64_t K)
+{
+    if (!gguf)
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    if (!aligned(gguf, 16))
+        return QMD_ERR_MISALIGNED;
+    return QMD_OK;
+}
+
+const char *qmd_status_str(qmd_status s)
+{
+    switch (s) {
+    case QMD_OK: return "QMD_OK";
+    case QMD_ERR_NULL: return "QMD_ERR_NULL";
+    case QMD_ERR_FORMAT: return "QMD_ERR_FORMAT";
+    case QMD_ERR_K_NOT_MULTIPLE_OF_256: return "QMD_ERR_K_NOT_MULTIPLE_OF_256";
+    case QMD_ERR_BATCH: return "QMD_ERR_BATCH";
+    case QMD_ERR_MISALIGNED: return "QMD_ERR_MISALIGNED";
+    case QMD_ERR_SHAPE: return "QMD_ERR_SHAPE";
+    case QMD_ERR_LAUNCH: return "QMD_ERR_LAUNCH";
+    case QMD_ERR_DEVICE_TIMEOUT: return "QMD_ERR_DEVICE_TIMEOUT";
+    case QMD_ERR_DEVICE: return "QMD_ERR_DEVICE";
+    }
+    return "QMD_ERR_UNKNOWN";
+}
+
+const char *qmd_last_error_detail(void) { return g_detail; }
+
+qmd_status qmd_get_device_error(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return fail(QMD_ERR_LAUNCH, "stream", e);
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof v);
+    if (e != cudaSuccess)
+        return fail(QMD_ERR_LAUNCH, "read error word", e);
+    if (v != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero);
+        if (e != cudaSuccess)
+            return fail(QMD_ERR_LAUNCH, "clear error word", e);
+        snprintf(g_detail, sizeof g_detail, "device error word 0x%x", v);
+        return QMD_ERR_DEVICE_TIMEOUT;
+    }
+    return QMD_OK;
+}
+
+void qmd_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+
+void qmd_debug_set_plan(int row_groups, int ctas_per_sm, int max_stages)
+{
+    g_force_rg.store(row_groups > 0 ? row_groups : 0);
+    g_force_cps.store(ctas_per_sm > 0 ? ctas_per_sm : 0);
+    g_force_stages.store(max_stages > 0 ? max_stages : 0);
+}
+
+qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int batch, int *grid,
+                                   int *threads, int *smem_bytes, int *stages, int *rows_per_stage)
+{
+    if (fmt != QMD_Q4_K && fmt != QMD_Q6_K_SPLIT)
+        return QMD_ERR_FORMAT;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return QMD_ERR_BATCH;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return st;
+    QmvPlan p;
+    if ((st = qmv_plan(fmt, rows, (int)(K / QMD_QK), batch, dev, &p)) != QMD_OK)
+        return st;
+    if (grid) *grid = p.grid;
+    if (threads) *threads = p.threads;
+    if (smem_bytes) *smem_bytes = p.smem;
+    if (stages) *stages = p.stages;
+    if (rows_per_stage) *rows_per_stage = p.rows_per_stage;
+    return QMD_OK;
+}
+
+qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)
+{
+    DeviceInfo dev;
+    qmd_status st = current_device(&dev);
+    if (st != QMD_OK)
+        return st;
+    unsigned *err = device_error_word();
+    if (!err)
+        return QMD_ERR_DEVICE;
+    debug_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, (unsigned long long)limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(QMD_ERR_LAUNCH, "debug wait launch", e);
+    return QMD_OK;
+}
+
+int qmd_version(void) { return 100; }
+
+}  // extern "C"

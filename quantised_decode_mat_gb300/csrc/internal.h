@@ -1,0 +1,71 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qmd.h"
+
+namespace qmd {
+
+// Error bits in the device error word.
+enum : unsigned {
+    ERRBIT_QMV_WAIT = 1u,     // a mat-vec pipeline wait gave up
+    ERRBIT_DEBUG_WAIT = 2u,   // the test-only wait kernel gave up (as intended)
+    ERRBIT_DRAIN_WAIT = 4u,   // draining copies after a give-up also gave up
+};
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int smem_optin;   // max dynamic shared memory per block (opt-in)
+    int smem_per_sm;  // shared memory per multiprocessor
+    int cc_major, cc_minor;
+};
+
+// Device properties of the current device (cached); QMD_ERR_DEVICE if there is none.
+qmd_status current_device(DeviceInfo *out);
+
+// Address of the error word on the current device (set up once per device).
+unsigned *device_error_word();
+
+uint64_t wait_limit_ns();
+
+// Record a CUDA error for qmd_last_error_detail and map it to a status.
+qmd_status fail(qmd_status st, const char *what, cudaError_t e);
+
+// ---- mat-vec -------------------------------------------------------------------------------
+struct QmvArgs {
+    int fmt;  // QMD_Q4_K or QMD_Q6_K_SPLIT
+    const uint8_t *W;
+    const uint8_t *Wpre;
+    const int8_t *xqs;
+    const float *xd;
+    const int16_t *xbs;
+    float *y;
+    int64_t rows;
+    int nb;
+    int batch;
+    int32_t *dbg_dots;  // non-NULL selects the recording variant
+    int32_t *dbg_sm;
+};
+
+struct QmvPlan {
+    int grid, threads, smem, stages, rows_per_stage;
+    int WR, RG, PR;
+    int row_bytes, pre_bytes, stage_bytes;
+};
+
+// Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.
+qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *plan);
+
+qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
+qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
+
+// ---- pack, bind, debug ---------------------------------------------------------------------
+qmd_status launch_q8k_pack(const float *x, int8_t *qs, float *d, int16_t *bsums, int64_t nblocks,
+                           cudaStream_t s);
+qmd_status launch_q6k_split(const uint8_t *gguf, uint8_t *body, uint16_t *prefix, int64_t rows,
+                            int nb, int64_t prefix_stride, cudaStream_t s);
+
+}  // namespace qmd

@@ -1,0 +1,163 @@
+"""A decode step of quantised projections, run through the C ABI and replayable as a CUDA graph.
+
+Each projection is: q8_K pack of its f32 activation (qmd_q8k_pack), then the mat-vec of its
+weight against the packed bytes (qmd_qmatvec).  A 7B-shaped decode step is 32 layers of
+{q|k|v fused Q4_K 6144x4096, o Q4_K 4096x4096, gate|up fused Q4_K 28672x4096, down Q6_K
+4096x14336} ("Language models on the device: the cajeta-llm kernels", §1 fused q|k|v and §3.3
+fused gate|up launches).  Capturing the step's launches once and replaying them is the CUDA
+form of the pages' deferred streams ("One kernel, any device", §1; "The scheduler: what runs
+when, beside what", §3), which issue a whole decode step as one graph.
+
+All activations of the step live in one device buffer and all outputs in another, so an
+end-to-end step moves its inputs in with one host-to-device copy and its outputs out with one
+device-to-host copy.
+"""
+from __future__ import annotations
+
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import Q4_K, Q6_K_SPLIT, QMD_QK, Q8K, bind_q6k, q6k_prefix_stride, q8k_pack, qmatvec
+from . import synth
+
+
+@dataclass
+class Projection:
+    name: str
+    layer: int
+    fmt: int
+    rows: int
+    K: int
+    W: "object"            # device uint8: Q4_K blocks or Q6_K bodies
+    W_aux: "object"        # device Q6_K prefix or None
+    x: "object"            # device f32 [B, K] (view into DecodeStep.x_all)
+    xq: Q8K
+    y: "object"            # device f32 [B, rows] (view into DecodeStep.y_all)
+    weight_bytes: int
+
+    def act_bytes(self) -> int:
+        """q8_K bytes the mat-vec reads: codes + scale (+ the eight sums for Q4_K) per block."""
+        nb = self.K // QMD_QK
+        per = 256 + 4 + (16 if self.fmt == Q4_K else 0)
+        return self.xq.batch * nb * per
+
+    def matvec_bytes(self) -> int:
+        return self.weight_bytes + self.act_bytes() + self.xq.batch * self.rows * 4
+
+    def pack_bytes(self) -> int:
+        nb = self.K // QMD_QK
+        B = self.xq.batch
+        return B * self.K * 4 + B * (self.K + nb * 4 + nb * 16)
+
+
+@dataclass
+class DecodeStep:
+    batch: int
+    projs: list = field(default_factory=list)
+    x_all: "object" = None
+    y_all: "object" = None
+    host_weights: dict = field(default_factory=dict)  # (layer, name) -> canonical GGUF bytes, if kept
+
+    def run(self, stream=None) -> None:
+        for p in self.projs:
+            q8k_pack(p.x, p.xq, stream)
+            qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+
+    def run_matvecs(self, fmt: int | None = None, stream=None) -> int:
+        n = 0
+        for p in self.projs:
+            if fmt is None or p.fmt == fmt:
+                qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+                n += 1
+        return n
+
+    def run_packs(self, stream=None) -> int:
+        for p in self.projs:
+            q8k_pack(p.x, p.xq, stream)
+        return len(self.projs)
+
+    def capture(self, fn=None):
+        """Capture fn() (default: the whole step) into a CUDA graph on a side stream."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            (fn or self.run)()  # warm: first launches set kernel attributes outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            (fn or self.run)()
+        torch.cuda.synchronize()
+        return g
+
+    @property
+    def launches(self) -> int:
+        return 2 * len(self.projs)
+
+    def bytes(self) -> dict:
+        mv = sum(p.matvec_bytes() for p in self.projs)
+        pk = sum(p.pack_bytes() for p in self.projs)
+        w = sum(p.weight_bytes for p in self.projs)
+        return dict(matvec=mv, pack=pk, total=mv + pk, weights=w)
+
+
+def _gen_layer(layer: int, projections, batch: int, seed_fn):
+    out = []
+    for t, (name, fmt, rows, K) in enumerate(projections):
+        seed = seed_fn(layer)
+        W = synth.weights(fmt, seed, rows, K, layer, t)
+        x = synth.activations(seed, batch, K, layer, t)
+        out.append((name, fmt, rows, K, W, x))
+    return out
+
+
+def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STEP_PROJECTIONS,
+              device="cuda", seed_fn=synth.step_seed, keep_host_layers=(), threads: int = 8) -> DecodeStep:
+    """Generate the seeded weights and activations of a decode step and place them on the device.
+
+    keep_host_layers: layers whose canonical GGUF weight bytes stay in host memory (for the
+    oracle).  Q6_K weights are bound (split) on the device."""
+    import torch
+    dev = torch.device(device)
+    step = DecodeStep(batch=batch)
+    x_sizes = [batch * K for (_, _, _, K) in projections] * layers
+    y_sizes = [(batch * rows + 3) // 4 * 4 for (_, _, rows, _) in projections] * layers
+    step.x_all = torch.empty(sum(x_sizes), dtype=torch.float32, device=dev)
+    step.y_all = torch.empty(sum(y_sizes), dtype=torch.float32, device=dev)
+    xo = yo = 0
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        futs = [ex.submit(_gen_layer, l, projections, batch, seed_fn) for l in range(layers)]
+        for l, fut in enumerate(futs):
+            for (name, fmt, rows, K, Wh, xh) in fut.result():
+                nb = K // QMD_QK
+                x = step.x_all[xo: xo + batch * K].view(batch, K)
+                x.copy_(torch.from_numpy(xh))
+                xo += batch * K
+                y = step.y_all[yo: yo + batch * rows].view(batch, rows)
+                yo += (batch * rows + 3) // 4 * 4
+                if fmt == "q4k":
+                    W = torch.from_numpy(Wh.reshape(rows, -1)).to(dev)
+                    Wa = None
+                    wbytes = rows * nb * 144
+                    qfmt = Q4_K
+                else:
+                    g = torch.from_numpy(Wh.reshape(rows, -1)).to(dev)
+                    W, Wa = bind_q6k(g, rows, K)
+                    del g
+                    wbytes = rows * nb * 208 + rows * q6k_prefix_stride(K) * 2
+                    qfmt = Q6_K_SPLIT
+                if l in keep_host_layers:
+                    step.host_weights[(l, name)] = Wh
+                step.projs.append(Projection(name, l, qfmt, rows, K, W, Wa, x, Q8K.empty(batch, K, dev), y,
+                                             wbytes))
+    torch.cuda.synchronize(dev)
+    return step
+
+
+def host_activation(step: DecodeStep, p: Projection) -> np.ndarray:
+    """The activation a projection was given (regenerated on the host from its seed)."""
+    names = [n for (n, _, _, _) in synth.STEP_PROJECTIONS]
+    return synth.activations(synth.step_seed(p.layer), step.batch, p.K, p.layer, names.index(p.name))

@@ -35,11 +35,19 @@ T_Q4K, T_Q6K, T_ACT = 1, 2, 3
 _S_D, _S_DMIN, _S_SCALES, _S_QS, _S_QL, _S_QH, _S_U1, _S_U2 = range(8)
 
 
+_S30, _S27, _S31 = np.uint64(30), np.uint64(27), np.uint64(31)
+
+
 def _mix(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 output function (z ^= z >> 30; z *= M1; z ^= z >> 27; z *= M2; z ^= z >> 31)."""
+    z = np.array(z, dtype=np.uint64, copy=True)
     with np.errstate(over="ignore"):
-        z = (z ^ (z >> np.uint64(30))) * _M1
-        z = (z ^ (z >> np.uint64(27))) * _M2
-        return z ^ (z >> np.uint64(31))
+        z ^= np.right_shift(z, _S30)
+        np.multiply(z, _M1, out=z)
+        z ^= np.right_shift(z, _S27)
+        np.multiply(z, _M2, out=z)
+        z ^= np.right_shift(z, _S31)
+    return z
 
 
 def stream_key(*ids: int) -> np.uint64:
@@ -53,9 +61,11 @@ def stream_key(*ids: int) -> np.uint64:
 
 def u64(key: np.uint64, n: int, start: int = 0) -> np.ndarray:
     """Words start .. start+n-1 of the stream `key`."""
-    i = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    z = np.arange(start + 1, start + n + 1, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        return _mix(np.uint64(key) + i * GAMMA)
+        np.multiply(z, GAMMA, out=z)
+        np.add(z, np.uint64(key), out=z)
+    return _mix(z)
 
 
 def rand_bytes(key: np.uint64, n: int) -> np.ndarray:

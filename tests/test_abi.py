@@ -1,0 +1,155 @@
+"""The C ABI on the host (no GPU needed): the library builds and loads, exports every function
+include/qmd.h declares, and refuses bad arguments with named statuses before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantised_decode_mat_gb300 as q
+from quantised_decode_mat_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(qmd_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("qmd_q8k_pack", "qmd_qmatvec", "qmd_bind_q6k", "qmd_bind_q4k", "qmd_q6k_split_bytes",
+                     "qmd_status_str", "qmd_get_device_error"):
+        assert required in names
+
+
+def test_every_declared_function_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in qmd.h but not exported by libqmd.so"
+        ctypes.cast(getattr(L, name), ctypes.c_void_p)
+
+
+def test_status_strings(L):
+    for code, name in q.STATUS.items():
+        assert q.status_str(code) == name
+    assert q.status_str(99) == "QMD_ERR_UNKNOWN"
+
+
+def test_version(L):
+    assert q.version() >= 100
+
+
+def test_prefix_stride_and_split_bytes(L):
+    assert q.q6k_prefix_stride(256) == 8
+    assert q.q6k_prefix_stride(14336) == 56
+    assert q.q6k_prefix_stride(2048) == 8
+    assert q.q6k_prefix_stride(2304) == 16
+    assert q.q6k_prefix_stride(100) == 0
+    assert q.q6k_split_bytes(4096, 14336) == (4096 * 56 * 208, 4096 * 56 * 2)
+    with pytest.raises(q.QmdError, match="QMD_ERR_K_NOT_MULTIPLE_OF_256"):
+        q.q6k_split_bytes(4, 300)
+    with pytest.raises(q.QmdError, match="QMD_ERR_SHAPE"):
+        q.q6k_split_bytes(0, 256)
+
+
+A = 0x10000  # aligned fake device addresses: validation must fail before any of them is used
+
+
+def _xq(qs=A, d=A, bs=A):
+    return q.Q8KPtrs(qs, d, bs)
+
+
+def st_qmatvec(L, fmt=q.Q4_K, W=A, Wa=A, xq=None, y=A, rows=16, K=512, batch=1):
+    return L.qmd_qmatvec(fmt, W, Wa, xq or _xq(), y, rows, K, batch, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=13), 2),
+    (dict(W=None), 1),
+    (dict(y=None), 1),
+    (dict(xq=_xq(qs=None)), 1),
+    (dict(xq=_xq(d=None)), 1),
+    (dict(xq=_xq(bs=None)), 1),                     # Q4_K needs the sub-block sums
+    (dict(fmt=q.Q6_K_SPLIT, Wa=None), 1),           # Q6_K needs the scale prefix
+    (dict(K=300), 3),
+    (dict(K=128), 3),
+    (dict(K=0), 6),
+    (dict(K=-256), 6),
+    (dict(batch=0), 4),
+    (dict(batch=9), 4),
+    (dict(rows=0), 6),
+    (dict(W=A + 8), 5),
+    (dict(fmt=q.Q6_K_SPLIT, Wa=A + 4), 5),
+    (dict(xq=_xq(qs=A + 4)), 5),
+    (dict(xq=_xq(bs=A + 2)), 5),
+    (dict(xq=_xq(d=A + 2)), 5),
+    (dict(y=A + 2), 5),
+])
+def test_qmatvec_refusals(L, kw, status):
+    assert st_qmatvec(L, **kw) == status
+
+
+def test_qmatvec_q6k_does_not_need_bsums_but_needs_a_device(L):
+    # validation passes; with no GPU in this process the call is refused as QMD_ERR_DEVICE
+    # (or runs, on a GPU machine) -- it never falls back to anything on the CPU
+    st = st_qmatvec(L, fmt=q.Q6_K_SPLIT, xq=_xq(bs=None))
+    assert st in (0, 9, 7)
+    if st == 0:
+        pytest.skip("a GPU is present; the refusal path is covered by the GPU tests")
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(x=None), 1),
+    (dict(K=100), 3),
+    (dict(K=0), 6),
+    (dict(batch=0), 4),
+    (dict(batch=9), 4),
+    (dict(x=A + 4), 5),
+    (dict(qs=A + 8), 5),
+    (dict(bs=A + 2), 5),
+    (dict(d=A + 1), 5),
+])
+def test_pack_refusals(L, args, status):
+    x = args.get("x", A)
+    xq = _xq(qs=args.get("qs", A), d=args.get("d", A), bs=args.get("bs", A))
+    assert L.qmd_q8k_pack(x, xq, args.get("K", 512), args.get("batch", 1), None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(g=None), 1),
+    (dict(K=200), 3),
+    (dict(rows=0), 6),
+    (dict(g=A + 1), 5),
+    (dict(b=A + 8), 5),
+    (dict(p=A + 4), 5),
+])
+def test_bind_refusals(L, args, status):
+    st = L.qmd_bind_q6k(args.get("g", A), args.get("b", A), args.get("p", A), args.get("rows", 4),
+                        args.get("K", 512), None)
+    assert st == status
+
+
+def test_bind_q4k_is_a_checked_view(L):
+    assert L.qmd_bind_q4k(A, 4, 512) == 0
+    assert L.qmd_bind_q4k(A + 8, 4, 512) == 5
+    assert L.qmd_bind_q4k(None, 4, 512) == 1
+    assert L.qmd_bind_q4k(A, 4, 500) == 3
+
+
+def test_no_gpu_means_a_named_refusal_not_a_fallback(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    assert L.qmd_qmatvec_launch_info(q.Q4_K, 4096, 4096, 1, None, None, None, None, None) == 9
+    assert st_qmatvec(L) == 9
+    assert L.qmd_q8k_pack(A, _xq(), 512, 1, None) == 9

@@ -1,0 +1,297 @@
+"""GPU path vs the CPU oracle, through the C ABI (needs a GB300).
+
+Bars (from the method's statement): q8_K packs and per-sub-block int32 dots bit-exact; f32
+outputs within 1e-5 relative of the oracle's f32 epilogue in the same order (the kernel is
+built to match it bit for bit, which is also checked), and within 2e-3 of the f64 brute force.
+Relative error is per element, |d| / max(|ref|, 1e-3 * rms(ref over the output vector)).
+Output buffers are poisoned with NaN (0xFF bytes) and followed by guard words, so a row that
+is not written, or a write past the end, fails.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+import quantised_decode_mat_gb300 as q  # noqa: E402
+from quantised_decode_mat_gb300 import synth  # noqa: E402
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+TOL_SAME_ORDER = 1e-5
+TOL_F64 = 2e-3
+GUARD = 64
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from quantised_decode_mat_gb300 import build as qbuild
+    qbuild.build()
+    q.lib()
+    q.debug_set_plan(0, 0, 0)
+    yield
+    q.debug_set_plan(0, 0, 0)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def poisoned_y(batch, rows):
+    """f32 [batch, rows] filled with NaN bits, followed by GUARD guard words."""
+    buf = torch.full((batch * rows + GUARD,), -1, dtype=torch.int32, device=DEV)
+    buf[batch * rows:] = 0x5A5A5A5A
+    return buf, buf[: batch * rows].view(torch.float32).view(batch, rows)
+
+
+def guard_intact(buf, batch, rows):
+    return bool((buf[batch * rows:] == 0x5A5A5A5A).all())
+
+
+def gpu_pack(x):
+    xq = q.q8k_pack(dev(x))
+    torch.cuda.synchronize()
+    return xq
+
+
+def run_matvec(fmtname, Wg, xq, rows, K, batch):
+    """Upload canonical GGUF weights, bind (Q6_K), run the mat-vec into a poisoned buffer."""
+    buf, y = poisoned_y(batch, rows)
+    if fmtname == "q4k":
+        q.qmatvec(q.Q4_K, dev(Wg.reshape(rows, -1)), None, xq, y, rows)
+    else:
+        body, prefix = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+        q.qmatvec(q.Q6_K_SPLIT, body, prefix, xq, y, rows)
+    q.get_device_error()
+    assert guard_intact(buf, batch, rows), "write past the end of y"
+    return y.cpu().numpy()
+
+
+OFMT = {"q4k": O.FMT_Q4_K, "q6k": O.FMT_Q6_K}
+
+
+def check_against_oracle(fmtname, Wg, x, y, rows_idx=None, exact=True):
+    """y [B, R] from the GPU vs oracle on the same W (canonical) and x; rows_idx samples rows."""
+    oqs, od, obs = O.q8k_pack(x)
+    W = Wg if rows_idx is None else Wg[rows_idx]
+    yg = y if rows_idx is None else y[:, rows_idx]
+    ref = O.qmatvec(OFMT[fmtname], W, oqs, od, obs, O.ORDER_GROUPS_OF_FOUR)
+    assert np.isfinite(yg).all(), "unwritten (NaN) outputs"
+    err = O.rel_err(yg, ref)
+    assert err.max() <= TOL_SAME_ORDER, f"same-order rel err {err.max():.3g}"
+    if exact:
+        diff = np.count_nonzero(yg.view(np.uint32) != ref.view(np.uint32))
+        assert diff == 0, f"{diff} outputs differ in bits from the same-order oracle"
+    ref64 = O.qmatvec_f64(OFMT[fmtname], W, oqs, od)
+    assert O.rel_err(yg, ref64).max() <= TOL_F64
+
+
+# ---- q8_K pack --------------------------------------------------------------------------------------
+def _pack_inputs():
+    rng = np.random.default_rng(3)
+    cases = [("n01_b1_k4096", synth.activations(1, 1, 4096)),
+             ("n01_b8_k14336", synth.activations(2, 8, 14336)),
+             ("n01_b3_k256", synth.activations(3, 3, 256))]
+    x = synth.activations(4, 2, 1024)
+    x[0, 256:512] = 0.0                         # all-zero block
+    x[1, 0:256] = np.float32(1e-38)              # block whose 127/amax overflows to inf
+    x[1, 3] = 0.0
+    x[1, 512:768] = (np.arange(256) - 128).astype(np.float32) * np.float32(0.5)   # ties at .5 steps
+    x[1, 768] = 1e30
+    cases.append(("special", x))
+    big = (rng.standard_normal((2, 2048)) * 1e4).astype(np.float32)
+    cases.append(("large", big))
+    return cases
+
+
+@pytest.mark.parametrize("name,x", _pack_inputs(), ids=[c[0] for c in _pack_inputs()])
+def test_pack_bit_exact(name, x):
+    xq = gpu_pack(x)
+    oqs, od, obs = O.q8k_pack(x)
+    assert np.array_equal(xq.qs.cpu().numpy(), oqs)
+    assert np.array_equal(xq.d.cpu().numpy().view(np.uint32), od.view(np.uint32))
+    assert np.array_equal(xq.bsums.cpu().numpy(), obs)
+
+
+# ---- integer dots, S and M, bit-exact (recording variant of the same kernel) -----------------------
+@pytest.mark.parametrize("fmtname", ["q4k", "q6k"])
+@pytest.mark.parametrize("batch,rows,K", [(1, 37, 1024), (2, 19, 2304), (3, 11, 256), (5, 7, 3072), (8, 13, 4096)])
+def test_subblock_dots_exact(fmtname, batch, rows, K):
+    Wg = synth.weights(fmtname, 7, rows, K)
+    x = synth.activations(7, batch, K)
+    xq = gpu_pack(x)
+    Wd = dev(Wg.reshape(rows, -1))
+    if fmtname == "q4k":
+        y, dots, sm = q.debug_qmatvec_dump(q.Q4_K, Wd, None, xq)
+    else:
+        body, prefix = q.bind_q6k(Wd, rows, K)
+        y, dots, sm = q.debug_qmatvec_dump(q.Q6_K_SPLIT, body, prefix, xq, rows)
+    q.get_device_error()
+    dots = dots.cpu().numpy()
+    sm = sm.cpu().numpy()
+    oqs, od, obs = O.q8k_pack(x)
+    nb = K // 256
+    for v in range(batch):
+        for r in range(rows):
+            od_ = O.subdots(OFMT[fmtname], Wg[r], oqs[v])
+            if fmtname == "q4k":
+                got = dots[v, r].reshape(nb, 4, 2, 2)  # [blk, c, half, u]
+                got = got.sum(axis=2).reshape(nb, 8)    # sub-block 2c+u
+            else:
+                got = dots[v, r]
+            assert np.array_equal(got, od_), (v, r)
+            for b in range(nb):
+                if fmtname == "q4k":
+                    _, _, sc, m, _ = O.q4k_fields(Wg[r, b])
+                    S = int(np.dot(sc, od_[b]))
+                    M = int(np.dot(m, obs[v, b].astype(np.int64)))
+                else:
+                    _, sc, _ = O.q6k_fields(Wg[r, b])
+                    S, M = int(np.dot(sc, od_[b])), 0
+                assert (sm[v, r, b, 0], sm[v, r, b, 1]) == (S, M), (v, r, b)
+    check_against_oracle(fmtname, Wg, x, y.cpu().numpy())
+
+
+# ---- outputs: the five workloads and a sweep of ragged shapes -----------------------------------------
+@pytest.mark.parametrize("cfg", [0, 1, 2])
+def test_configs_full(cfg):
+    c = synth.CONFIGS[cfg]
+    for batch in c["batches"]:
+        Wg = synth.weights(c["fmt"], c["seed"], c["rows"], c["K"])
+        x = synth.activations(c["seed"], batch, c["K"])
+        y = run_matvec(c["fmt"], Wg, gpu_pack(x), c["rows"], c["K"], batch)
+        check_against_oracle(c["fmt"], Wg, x, y)
+
+
+def _sample_rows(rows, n, seed):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(rows, size=min(n, rows), replace=False).tolist())
+    pick |= {0, 1, rows - 2, rows - 1}
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+def test_config3_gate_up_sampled(batch):
+    c = synth.CONFIGS[3]
+    Wg = synth.weights(c["fmt"], c["seed"], c["rows"], c["K"])
+    x = synth.activations(c["seed"], batch, c["K"])
+    y = run_matvec(c["fmt"], Wg, gpu_pack(x), c["rows"], c["K"], batch)
+    assert np.isfinite(y).all()
+    # rows at every CTA boundary of the launch, plus a random sample
+    info = q.launch_info(q.Q4_K, c["rows"], c["K"], batch)
+    G = info["grid"]
+    bounds = {(c["rows"] * b) // G for b in range(G)} | {(c["rows"] * b) // G - 1 for b in range(1, G)}
+    idx = np.array(sorted(set(_sample_rows(c["rows"], 600, batch).tolist()) | bounds))
+    check_against_oracle(c["fmt"], Wg, x, y, rows_idx=idx)
+
+
+SWEEP = [
+    # fmt, rows, K, batch
+    ("q4k", 1, 256, 1), ("q4k", 3, 512, 2), ("q4k", 129, 768, 3), ("q4k", 1000, 1280, 1),
+    ("q4k", 333, 2048, 4), ("q4k", 77, 4352, 5), ("q4k", 250, 4096, 6), ("q4k", 61, 3840, 7),
+    ("q4k", 500, 4096, 8), ("q4k", 5, 16384, 8), ("q4k", 9, 32768, 1), ("q4k", 6, 32768, 2),
+    ("q6k", 1, 256, 1), ("q6k", 5, 512, 2), ("q6k", 130, 1792, 1), ("q6k", 257, 2304, 3),
+    ("q6k", 64, 3328, 4), ("q6k", 300, 14336, 1), ("q6k", 40, 14336, 2), ("q6k", 31, 14336, 4),
+    ("q6k", 17, 14336, 8), ("q6k", 4, 32768, 1), ("q6k", 9, 16384, 7),
+]
+
+
+@pytest.mark.parametrize("fmtname,rows,K,batch", SWEEP)
+def test_sweep_shapes(fmtname, rows, K, batch):
+    seed = rows * 7 + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    check_against_oracle(fmtname, Wg, x, y)
+
+
+@pytest.mark.parametrize("plan", [(1, 1, 1), (1, 2, 2), (2, 1, 3), (4, 1, 1), (1, 8, 2), (3, 2, 1)])
+@pytest.mark.parametrize("fmtname,rows,K,batch", [("q4k", 2000, 4096, 1), ("q4k", 700, 2048, 3),
+                                                  ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2)])
+def test_pipeline_plans(plan, fmtname, rows, K, batch):
+    """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits."""
+    q.debug_set_plan(*plan)
+    try:
+        Wg = synth.weights(fmtname, 5, rows, K)
+        x = synth.activations(5, batch, K)
+        y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    finally:
+        q.debug_set_plan(0, 0, 0)
+    check_against_oracle(fmtname, Wg, x, y)
+
+
+def test_degenerate_inputs():
+    rows, K = 64, 1024
+    # all-zero activations: every term is 0 * (...) = 0
+    Wg = synth.q4k_weights(1, rows, K)
+    x = np.zeros((2, K), np.float32)
+    y = run_matvec("q4k", Wg, gpu_pack(x), rows, K, 2)
+    assert np.all(y == 0.0)
+    # zero codes: only the -dmin * min term remains (checked against the oracle bit for bit)
+    Wz = Wg.copy()
+    Wz[:, :, 16:] = 0
+    x = synth.activations(2, 1, K)
+    y = run_matvec("q4k", Wz, gpu_pack(x), rows, K, 1)
+    check_against_oracle("q4k", Wz, x, y)
+    # Q6_K codes all 32 give exactly zero
+    W6 = synth.q6k_weights(1, rows, K).copy()
+    W6[:, :, 0:128] = 0
+    W6[:, :, 128:192] = 0xAA
+    y = run_matvec("q6k", W6, gpu_pack(x), rows, K, 1)
+    assert np.all(y == 0.0)
+
+
+def test_bind_q6k_matches_oracle_split():
+    rows, K = 33, 2304
+    g = synth.q6k_weights(9, rows, K)
+    body, prefix = q.bind_q6k(dev(g.reshape(rows, -1)), rows, K)
+    torch.cuda.synchronize()
+    ob, op = O.q6k_split(g, q.q6k_prefix_stride(K))
+    assert np.array_equal(body.cpu().numpy().reshape(ob.shape), ob)
+    assert np.array_equal(prefix.cpu().numpy().view(np.uint16), op)
+
+
+# ---- refusals launch nothing; bounded waits report instead of hanging ---------------------------------
+def test_refused_calls_write_nothing():
+    rows, K = 16, 512
+    Wg = synth.q4k_weights(1, rows, K)
+    xq = gpu_pack(synth.activations(1, 1, K))
+    Wd = dev(Wg.reshape(rows, -1))
+    buf, y = poisoned_y(1, rows)
+    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 500, 1, None)
+    assert st == 3
+    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr() + 8, None, xq.ptrs(), y.data_ptr(), rows, K, 1, None)
+    assert st == 5
+    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 65536, 1, None)
+    assert st == 6  # above the K limit
+    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 32768, 3, None)
+    assert st == 6  # K limit for batch > 2
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all() and guard_intact(buf, 1, rows)
+    q.get_device_error()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    q.debug_wait_timeout(2_000_000)  # 2 ms
+    with pytest.raises(q.QmdError, match="QMD_ERR_DEVICE_TIMEOUT"):
+        q.get_device_error()
+    q.get_device_error()  # cleared
+    # the context is still usable
+    rows, K = 8, 256
+    Wg = synth.q4k_weights(2, rows, K)
+    x = synth.activations(2, 1, K)
+    y = run_matvec("q4k", Wg, gpu_pack(x), rows, K, 1)
+    check_against_oracle("q4k", Wg, x, y)
+
+
+def test_launch_info_shapes():
+    i1 = q.launch_info(q.Q4_K, 4096, 4096, 1)
+    i2 = q.launch_info(q.Q6_K_SPLIT, 4096, 14336, 1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for i in (i1, i2):
+        assert i["grid"] >= sms and i["stages"] >= 1 and i["threads"] % 32 == 0
+        assert i["smem_bytes"] <= 232448

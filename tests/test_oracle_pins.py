@@ -228,6 +228,19 @@ def test_q8k_zero_block_and_exact_multiples():
     assert np.array_equal(qs[0, 256:].astype(np.int64), k)
 
 
+def test_q8k_block_below_overflow_threshold():
+    """amax = 1e-38 < 127/FLT_MAX: 127/amax is +inf in f32, so nonzero codes saturate to +-127 and a
+    zero (0 * inf = NaN) gets code 0; d = amax/127 is subnormal but exact division."""
+    x = np.zeros((1, 256), np.float32)
+    x[0, :] = np.float32(1e-38)
+    x[0, 1] = -np.float32(5e-39)
+    x[0, 2] = 0.0
+    qs, d, bs = O.q8k_pack(x)
+    assert qs[0, 0] == 127 and qs[0, 1] == -127 and qs[0, 2] == 0
+    assert d[0, 0] == np.float32(np.float32(1e-38) / np.float32(127.0))
+    assert bs[0, 0, 0] == 127 * 29 and list(bs[0, 0, 1:]) == [127 * 32] * 7
+
+
 def test_q8k_rounds_half_to_even():
     x = np.zeros((1, 256), np.float32)
     x[0, 0] = 127.0  # amax = 127 -> iscale = 1 exactly, so codes are rint(x)
