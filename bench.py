@@ -1,0 +1,395 @@
+"""Benchmark: one 7B-shaped decode step of quantised projections on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--batch B]
+
+A step is one pass of the whole hot path over one batch of synthetic input: for each of 32
+layers and each projection {q|k|v Q4_K 6144x4096, o Q4_K 4096x4096, gate|up Q4_K 28672x4096,
+down Q6_K 4096x14336}, the q8_K pack of that projection's activation and the mat-vec of its
+weight -- by default in one launch per projection (qmd_qmatvec_x, which packs inside the
+kernel), with --unfused as qmd_q8k_pack followed by qmd_qmatvec.  Each launch depends on the
+previous one in stream order, as in a real decode where a projection's input comes from the
+layer before.  The step's launches are captured once into a CUDA graph and replayed.  Weights
+(4.41 GB) exceed L2 many times over, so consecutive steps read them from HBM.
+
+Throughput is quoted on algorithmic bytes: every weight byte, the f32 activations read and the
+f32 outputs written, once per step (4.419 GB at batch 1).
+
+Printed (rank 0, one JSON line): the step's algorithmic bytes / time as GB/s (value), the
+same through host buffers (e2e: inputs copied in and outputs copied out every step), the
+dominant kernel's roofline, the oracle's throughput on the host cores (cpu_baseline), SM
+clocks sampled during the timed region, and launch counts.
+
+--impl reference times the CPU oracle on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica of the step (replicas only; the
+path needs no exchange); value is the bytes all ranks processed / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and rows/s for Q4_K/Q6_K×q8_K decode mat-vec"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SOURCES = ["quantised_decode_mat_gb300/csrc/qmv.cuh", "quantised_decode_mat_gb300/csrc/qmv_q4k.cu",
+                  "quantised_decode_mat_gb300/csrc/qmv_q6k.cu", "quantised_decode_mat_gb300/csrc/ptx.cuh",
+                  "quantised_decode_mat_gb300/csrc/pack.cu", "quantised_decode_mat_gb300/csrc/q8k.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    try:
+        vals = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                line = line.split("#", 1)[0].strip()
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("source_hash") != kernel_source_hash():
+            return None
+        v = vals.get(f"{kernel}_dram_bytes_per_launch")
+        return float(v) if v else None
+    except FileNotFoundError:
+        return None
+
+
+# ---- clocks sampled during the timed region ------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except FileNotFoundError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev_index: int):
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---- distributed helpers (timing only: replicas exchange no data) ---------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- the oracle on the host cores ------------------------------------------------------------------
+def oracle_step_sample(layers, batch: int, row_fraction: float = 1.0):
+    """Run the oracle (pack + mat-vec, its default sequential order) over the given layers of the
+    decode step; returns (seconds, algorithmic bytes, rows)."""
+    import oracle as O
+    from quantised_decode_mat_gb300 import synth
+    secs = 0.0
+    nbytes = 0
+    nrows = 0
+    for layer in layers:
+        for t, (name, fmt, rows, K) in enumerate(synth.STEP_PROJECTIONS):
+            r = max(1, int(rows * row_fraction))
+            W = synth.weights(fmt, synth.step_seed(layer), rows, K, layer, t)[:r]
+            x = synth.activations(synth.step_seed(layer), batch, K, layer, t)
+            ofmt = O.FMT_Q4_K if fmt == "q4k" else O.FMT_Q6_K
+            t0 = time.perf_counter()
+            qs, xd, bs = O.q8k_pack(x)
+            O.qmatvec(ofmt, W, qs, xd, bs)
+            secs += time.perf_counter() - t0
+            nb = K // 256
+            wb = r * nb * (144 if fmt == "q4k" else 210)
+            nbytes += wb + batch * K * 4 + batch * r * 4  # weights + f32 activations + f32 outputs
+            nrows += r
+    return secs, nbytes, nrows
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from quantised_decode_mat_gb300 import synth
+    import oracle
+    oracle.build()
+    layer_bytes = sum((rows * (K // 256) * (144 if f == "q4k" else 210)) for (_, f, rows, K) in synth.STEP_PROJECTIONS)
+    # bound the whole run to about two minutes at the oracle's ~0.15 GB/s
+    budget_bytes = 18e9
+    frac = min(1.0, budget_bytes / max(1, args.steps + args.warmup) / layer_bytes)
+    frac = max(frac, 1.0 / 4096)
+    for i in range(args.warmup):
+        oracle_step_sample([i % synth.STEP_LAYERS], args.batch, frac)
+    tot_s = tot_b = 0.0
+    for i in range(args.steps):
+        s, b, _ = oracle_step_sample([i % synth.STEP_LAYERS], args.batch, frac)
+        tot_s += s
+        tot_b += b
+    gbs = tot_b / tot_s / 1e9
+    sample = (f"per step: the first {frac:.4%} of every projection's rows of one layer (layer = step index mod 32) "
+              f"of the 32-layer step, batch {args.batch}; oracle pack + mat-vec, single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 dot / f32 epilogue",
+        "data": "synthetic", "config": workload_config(args),
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(args):
+    from quantised_decode_mat_gb300 import synth
+    return {"workload": f"decode_step_7b_q4k_q6k_32layers_b{args.batch}",
+            "launch": "pack+mat-vec as two kernels" if getattr(args, "unfused", False)
+            else "pack fused into the mat-vec (one kernel per projection)",
+            "layers": synth.STEP_LAYERS,
+            "projections": [f"{n}:{f}:{r}x{k}" for (n, f, r, k) in synth.STEP_PROJECTIONS],
+            "batch": args.batch,
+            "l2": "inputs larger than L2 (4.41 GB of weights streamed per step; no flush needed)",
+            "parallelism": "replicas" if args.gpus > 1 else "single"}
+
+
+# ---- our path ----------------------------------------------------------------------------------------
+def time_graph(torch, g, reps: int, stream) -> float:
+    """ms per replay of graph g, CUDA events on the replay stream."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local_rank)
+    if rank == 0:
+        from quantised_decode_mat_gb300 import build as qbuild
+        qbuild.build()
+    barrier(world)
+    import quantised_decode_mat_gb300 as q
+    from quantised_decode_mat_gb300 import step as qstep
+    q.lib()  # fails loudly if the CUDA library is missing
+
+    step = qstep.make_step(args.batch, device=f"cuda:{local_rank}", fused=not args.unfused)
+    nbytes = step.bytes()
+    stream = torch.cuda.current_stream()
+
+    g = step.capture()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(torch, local_rank))
+    barrier(world)
+    sampler.start()
+    ms = time_graph(torch, g, args.steps, stream)
+    clocks = sampler.stop()
+    barrier(world)
+    ms_max = max_over_ranks(ms, world)
+    q.get_device_error()
+
+    # the dominant kernel and the others, each timed as a graph of its launches in step order
+    nq4 = sum(1 for p in step.projs if p.fmt == q.Q4_K)
+    nq6 = len(step.projs) - nq4
+    reps = max(3, min(args.steps, 200))
+    g4 = step.capture(lambda: step.run_matvecs(q.Q4_K))
+    g6 = step.capture(lambda: step.run_matvecs(q.Q6_K_SPLIT))
+    gp = step.capture(step.run_packs)
+    for gg in (g4, g6, gp):
+        gg.replay()
+    ms4 = time_graph(torch, g4, reps, stream) / nq4
+    ms6 = time_graph(torch, g6, reps, stream) / nq6
+    msp = time_graph(torch, gp, reps, stream) / len(step.projs)
+    per = (lambda p: p.algorithmic_bytes()) if step.fused else (lambda p: p.matvec_bytes())
+    b4 = sum(per(p) for p in step.projs if p.fmt == q.Q4_K) / nq4
+    b6 = sum(per(p) for p in step.projs if p.fmt == q.Q6_K_SPLIT) / nq6
+    bp = nbytes["pack"] / len(step.projs)
+
+    # end to end: inputs from pinned host memory in, outputs to pinned host memory out, every step
+    x_host = torch.empty(step.x_all.shape, dtype=step.x_all.dtype, pin_memory=True)
+    y_host = torch.empty(step.y_all.shape, dtype=step.y_all.dtype, pin_memory=True)
+    x_host.copy_(step.x_all)
+
+    def e2e_step():
+        step.x_all.copy_(x_host, non_blocking=True)
+        step.run()
+        y_host.copy_(step.y_all, non_blocking=True)
+
+    ge = step.capture(e2e_step)
+    for _ in range(max(1, args.warmup)):
+        ge.replay()
+    barrier(world)
+    ms_e2e = max_over_ranks(time_graph(torch, ge, args.steps, stream), world)
+    q.get_device_error()
+
+    peak, peak_kind = measured_peak()
+    gbs = world * nbytes["algorithmic"] / (ms_max * 1e-3) / 1e9
+    rows_per_step = sum(p.rows for p in step.projs)
+    ach4 = b4 / (ms4 * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 dot / f32 epilogue", "data": "synthetic",
+        "config": workload_config(args),
+        "pct_of_peak": {"of_" + peak_kind: gbs / world / peak, "of_nominal_8TBps": gbs / world / NOMINAL_HBM_GBS},
+        "rows_per_s": world * rows_per_step / (ms_max * 1e-3),
+        "bytes_per_step": nbytes,
+        "roofline": {"bound": "hbm",
+                     "kernel": "qmv_kernel<Q4_K, batch %d, %s>" % (args.batch, "fused pack" if step.fused else "packed input"),
+                     "achieved": ach4, "peak": peak,
+                     "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic("qmv_q4k"),
+                     "algorithmic_bytes_per_launch": b4, "ms_per_launch": ms4},
+        "kernels": {
+            "qmv_q4k": {"launches_per_step": nq4, "us_per_launch": ms4 * 1e3, "gbs": ach4},
+            "qmv_q6k": {"launches_per_step": nq6, "us_per_launch": ms6 * 1e3, "gbs": b6 / (ms6 * 1e-3) / 1e9},
+            "q8k_pack": {"launches_per_step": 0 if step.fused else len(step.projs),
+                         "us_per_launch": msp * 1e3, "gbs": bp / (msp * 1e-3) / 1e9,
+                         "note": "stand-alone pack kernel, timed as a chain of its launches"},
+        },
+        "e2e": {"value": world * nbytes["algorithmic"] / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": step.x_all.numel() * 4, "d2h_bytes_per_step": step.y_all.numel() * 4,
+                "ms_per_step": ms_e2e},
+        "clocks": clocks,
+        "gpu_launches": step.launches * args.steps,
+    }
+    del g, g4, g6, gp, ge
+    if rank == 0 and args.cpu_layers > 0:
+        import oracle
+        oracle.build()
+        secs, ob, orows = oracle_step_sample(range(args.cpu_layers), args.batch)
+        line["cpu_baseline"] = {"value": ob / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"layers 0-{args.cpu_layers - 1} of 32, all four projections, batch "
+                                          f"{args.batch}: oracle q8_K pack + mat-vec, single thread, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--batch", type=int, default=1, choices=range(1, 9))
+    ap.add_argument("--unfused", action="store_true",
+                    help="run each projection as qmd_q8k_pack + qmd_qmatvec (two launches)")
+    ap.add_argument("--cpu-layers", type=int, default=8,
+                    help="layers of the step the oracle is timed on for cpu_baseline (0: skip)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -123,12 +123,30 @@ qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *
  *   xq     packed activations for `batch` vectors of length K (qs, bsums 16-byte aligned,
  *          d 4-byte aligned; bsums may be NULL for Q6_K_SPLIT, which does not read them)
  *   y      f32 [batch][rows], 4-byte aligned (written)
- * Limits: 1 <= batch <= 8; K <= 32768 for batch <= 2, K <= 16384 for batch > 2.
+ * Limits: 1 <= batch <= 8; K <= 32768 for batch <= 2 and K <= 16384 for batch > 2
+ * (QMD_ERR_SHAPE otherwise).
  * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, DEVICE, LAUNCH.
  * Device-side bounded waits that give up set a flag read by qmd_get_device_error.
  */
 qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                        int64_t rows, int64_t K, int batch, void *stream);
+
+/*
+ * qmd_qmatvec_x -- the q8_K pack and the mat-vec in one launch: y is exactly
+ * qmd_qmatvec(fmt, W, W_aux, qmd_q8k_pack(x), ...), with the same bits, but each CTA packs
+ * the f32 activations itself into shared memory instead of reading a packed copy, which
+ * removes a dependent launch from the stream ("Language models on the device: the cajeta-llm
+ * kernels", §1 q8kPackKernel and the decode mat-vecs, here fused).
+ *   x       f32 [batch][K], 16-byte aligned (read)
+ *   xq_out  optional: if its three pointers are non-NULL, the packed activations are also
+ *           written there (qs and bsums 16-byte aligned, d 4-byte aligned), the same bytes
+ *           qmd_q8k_pack writes; all three NULL writes nothing.
+ * Other arguments, limits and errors as qmd_qmatvec; in addition the batch's packed codes
+ * (batch x K bytes) must fit in shared memory beside the weight stages (QMD_ERR_SHAPE
+ * otherwise; every K <= 16384 at batch <= 4 and K <= 32768 at batch 1 fit).
+ */
+qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                         float *y, int64_t rows, int64_t K, int batch, void *stream);
 
 /*
  * qmd_q6k_prefix_stride -- entries (f16) per row of the Q6_K scale prefix: nb rounded up to
@@ -209,7 +227,8 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
  *         Q4_K: entry 4c + 2h + u is the dot of the 16 elements (half h of the 32) of
  *               sub-block 2c + u; Q6_K_SPLIT: entry s is dot'_s of group s.
  *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K) M; M = 0 for Q6_K_SPLIT.
- * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm.
+ * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm; this entry also
+ * refuses K > 16384 (QMD_ERR_SHAPE).
  */
 qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,
                                   float *y, int64_t rows, int64_t K, int batch, int32_t *dots,
@@ -224,11 +243,20 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream);
 
 /*
  * qmd_debug_set_plan -- override the mat-vec launch plan for launches made after the call:
- * row groups per CTA, CTAs per multiprocessor, and a cap on pipeline stages (0 = the default
- * for each).  Results do not depend on the plan; tests use this to drive the stage ring
- * through many wrap-arounds on small inputs.  Process-wide.
+ * row groups per CTA (each ceil(K/1024) warps; capped by the thread limit), rows per row group
+ * per stage (1, 2, 4 or 8; reduced until rows x batch <= 8), a cap on pipeline stages, and
+ * CTAs per multiprocessor (1..8); 0 keeps the default of each.  Results do not depend on the
+ * plan; tests use this to drive the stage ring through many wrap-arounds on small inputs.
+ * Process-wide.
  */
-void qmd_debug_set_plan(int row_groups, int ctas_per_sm, int max_stages);
+void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int ctas_per_sm);
+
+/*
+ * qmd_debug_set_launch_flags -- test-only launch options for later launches: bit 0 launches
+ * qmd_q8k_pack and qmd_qmatvec without programmatic dependent launch (plain stream order).
+ * Results are the same either way.  Process-wide.
+ */
+void qmd_debug_set_launch_flags(unsigned flags);
 
 /* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
 int qmd_version(void);

@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
         sigs = {
             "qmd_q8k_pack": ([vp, Q8KPtrs, i64, i32, vp], i32),
             "qmd_qmatvec": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
+            "qmd_qmatvec_x": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_q6k_prefix_stride": ([i64], i64),
             "qmd_q6k_split_bytes": ([i64, i64, sizep, sizep], i32),
             "qmd_bind_q6k": ([vp, vp, vp, i64, i64, vp], i32),
@@ -73,7 +74,8 @@ def lib() -> ctypes.CDLL:
             "qmd_qmatvec_launch_info": ([i32, i64, i64, i32, ip, ip, ip, ip, ip], i32),
             "qmd_debug_qmatvec_dump": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp, vp], i32),
             "qmd_debug_wait_timeout": ([u64, vp], i32),
-            "qmd_debug_set_plan": ([i32, i32, i32], None),
+            "qmd_debug_set_plan": ([i32, i32, i32, i32], None),
+            "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
             "qmd_version": ([], i32),
         }
         for name, (args, res) in sigs.items():
@@ -150,6 +152,21 @@ def qmatvec(fmt: int, W, W_aux, xq: Q8K, y=None, rows: int | None = None, stream
     return y
 
 
+def qmatvec_x(fmt: int, W, W_aux, x, y=None, rows: int | None = None, xq_out: Q8K | None = None,
+              stream=None):
+    """qmd_qmatvec_x: y f32 [batch, rows] = W (fmt) x q8k_pack(x), packing inside the kernel.
+    x: f32 [batch, K].  xq_out: optional Q8K that receives the packed activations."""
+    import torch
+    rows = W.shape[0] if rows is None else rows
+    batch, K = x.shape
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    out = xq_out.ptrs() if xq_out is not None else Q8KPtrs(None, None, None)
+    _check(lib().qmd_qmatvec_x(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
+                               _stream(stream)))
+    return y
+
+
 def q6k_prefix_stride(K: int) -> int:
     return int(lib().qmd_q6k_prefix_stride(K))
 
@@ -216,8 +233,12 @@ def debug_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(lib().qmd_debug_wait_timeout(int(limit_ns), _stream(stream)))
 
 
-def debug_set_plan(row_groups: int = 0, ctas_per_sm: int = 0, max_stages: int = 0) -> None:
-    lib().qmd_debug_set_plan(row_groups, ctas_per_sm, max_stages)
+def debug_set_plan(row_groups: int = 0, rows_per_stage: int = 0, max_stages: int = 0, ctas_per_sm: int = 0) -> None:
+    lib().qmd_debug_set_plan(row_groups, rows_per_stage, max_stages, ctas_per_sm)
+
+
+def debug_set_launch_flags(flags: int = 0) -> None:
+    lib().qmd_debug_set_launch_flags(int(flags))
 
 
 def version() -> int:

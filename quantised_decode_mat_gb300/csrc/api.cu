@@ -23,7 +23,7 @@ static __device__ unsigned int g_error_word;
 
 static thread_local char g_detail[320];
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};
-static std::atomic<int> g_force_rg{0}, g_force_cps{0}, g_force_stages{0};
+static std::atomic<int> g_force_rg{0}, g_force_rows{0}, g_force_stages{0}, g_force_cps{0};
 
 qmd_status fail(qmd_status st, const char *what, cudaError_t e)
 {
@@ -33,6 +33,9 @@ qmd_status fail(qmd_status st, const char *what, cudaError_t e)
 }
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+static std::atomic<unsigned> g_launch_flags{0};
+unsigned launch_flags() { return g_launch_flags.load(); }
 
 qmd_status current_device(DeviceInfo *out)
 {
@@ -83,30 +86,51 @@ unsigned *device_error_word()
     return addr[dev];
 }
 
-qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
+// Rows per row group per stage (PR x B <= 8).
+static int default_rows_per_stage(bool q6, int batch)
+{
+    if (batch == 1)
+        return 8;
+    if (batch == 2)
+        return q6 ? 2 : 4;
+    if (batch <= 4)
+        return 2;
+    return 1;
+}
+
+qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
 {
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
-    const int max_threads = batch <= 2 ? 1024 : 512;  // the kernels' launch bounds
+    const bool fused = mode == QMV_PACK;
+    const int max_threads = qmv_max_threads(batch, mode);  // the kernels' launch bounds
     const int WR = (nb + 3) / 4;                       // warps per row: 4 blocks per warp
     if (WR * 32 > max_threads)
         return QMD_ERR_SHAPE;
-    const int PR = (8 / batch) > 0 ? 8 / batch : 1;  // must match Tiling<B>::PR
-    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (8 / PR > 0 ? 8 / PR : 1);
+    int PR = g_force_rows.load() > 0 ? g_force_rows.load() : default_rows_per_stage(q6, batch);
+    while (PR > 1 && PR * batch > 8)
+        PR >>= 1;
+    // Row groups per CTA: the fused form at batch 1 takes 2 (half as many CTAs, so half the
+    // reads of the f32 activations that every CTA packs for itself); otherwise 1.
+    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (fused && batch == 1 ? 2 : 1);
     if (RG * WR * 32 > max_threads)
         RG = max_threads / (WR * 32);
-    if (RG < 1)
-        RG = 1;
     const int TR = RG * PR;
     const int row_bytes = nb * (q6 ? 208 : 144);
     const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
-    const int64_t sb64 = (int64_t)TR * (row_bytes + pre_bytes);
+    const int row_stride = row_bytes;  // rows of a stage are one contiguous copy
+    const int64_t sb64 = (int64_t)TR * row_stride + (int64_t)TR * pre_bytes;
     if (sb64 > dev.smem_optin)
         return QMD_ERR_SHAPE;
     const int stage_bytes = align_up((int)sb64, 128);
-    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / (RG * WR) > 0 ? 16 / (RG * WR) : 1);
-    for (;; --cps) {
-        if (cps < 1)
-            return QMD_ERR_SHAPE;
+    const int per_stage = stage_bytes + RG * WR * 8 * 4 + 16;  // ring + partials + counter + barrier
+    // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
+    // matter more than stage depth); capped at launch by the occupancy calculator.
+    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1);
+    if (cps > 8)
+        cps = 8;
+    if (fused && batch == 1 && g_force_cps.load() <= 0 && cps > 2)
+        cps = 2;
+    for (; cps >= 1; --cps) {
         int budget = dev.smem_per_sm / cps - 1024;
         if (budget > dev.smem_optin)
             budget = dev.smem_optin;
@@ -115,8 +139,8 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
             grid = rows;
         const int64_t rows_per_cta = (rows + grid - 1) / grid;
         const int64_t chunks = (rows_per_cta + TR - 1) / TR;
-        const int fixed = qmv_smem_layout(0, stage_bytes, batch, nb, !q6, RG, WR).total + 8 * 8;
-        int64_t stages = (budget - fixed) / stage_bytes;
+        const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused).total + 64;
+        int64_t stages = (budget - fixed) / per_stage;
         if (stages > 8)
             stages = 8;
         if (stages > chunks)
@@ -128,16 +152,17 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         pl->grid = (int)grid;
         pl->threads = RG * WR * 32;
         pl->stages = (int)stages;
-        pl->smem = qmv_smem_layout((int)stages, stage_bytes, batch, nb, !q6, RG, WR).total;
-        pl->rows_per_stage = TR;
+        pl->smem = qmv_smem_layout((int)stages, stage_bytes, RG, WR, batch, nb, q6, fused).total;
         pl->WR = WR;
         pl->RG = RG;
         pl->PR = PR;
         pl->row_bytes = row_bytes;
         pl->pre_bytes = pre_bytes;
         pl->stage_bytes = stage_bytes;
+        pl->row_stride = row_stride;
         return QMD_OK;
     }
+    return QMD_ERR_SHAPE;
 }
 
 // Test-only: one CTA waits on a barrier nothing completes, gives up after limit_ns, flags it.
@@ -176,12 +201,18 @@ qmd_status check_k(int64_t K)
 
 qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                           int64_t rows, int64_t K, int batch, int32_t *dots, int32_t *sm, bool dump,
-                          void *stream)
+                          const float *x, qmd_q8k xq_out, void *stream)
 {
     if (fmt != QMD_Q4_K && fmt != QMD_Q6_K_SPLIT)
         return QMD_ERR_FORMAT;
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
-    if (!W || !xq.qs || !xq.d || !y || (q6 && !W_aux) || (!q6 && !xq.bsums) || (dump && (!dots || !sm)))
+    const bool fused = x != nullptr;
+    const bool want_out = xq_out.qs || xq_out.d || xq_out.bsums;
+    if (!W || !y || (q6 && !W_aux) || (dump && (!dots || !sm)))
+        return QMD_ERR_NULL;
+    if (!fused && (!xq.qs || !xq.d || (!q6 && !xq.bsums)))
+        return QMD_ERR_NULL;
+    if (fused && want_out && (!xq_out.qs || !xq_out.d || !xq_out.bsums))
         return QMD_ERR_NULL;
     qmd_status st = check_k(K);
     if (st != QMD_OK)
@@ -191,15 +222,17 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
     if (rows < 1 || rows > (int64_t)1 << 31)
         return QMD_ERR_SHAPE;
     const int nb = (int)(K / QMD_QK);
-    if (!aligned(W, 16) || (q6 && !aligned(W_aux, 16)) || !aligned(xq.qs, 16) ||
-        (!q6 && !aligned(xq.bsums, 16)) || !aligned(xq.d, 4) || !aligned(y, 4) ||
+    if (!aligned(W, 16) || (q6 && !aligned(W_aux, 16)) || !aligned(y, 4) ||
+        (!fused && (!aligned(xq.qs, 16) || (!q6 && !aligned(xq.bsums, 16)) || !aligned(xq.d, 4))) ||
+        (fused && !aligned(x, 16)) ||
+        (fused && want_out && (!aligned(xq_out.qs, 16) || !aligned(xq_out.bsums, 16) || !aligned(xq_out.d, 4))) ||
         (dump && (!aligned(dots, 16) || !aligned(sm, 16))))
         return QMD_ERR_MISALIGNED;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != QMD_OK)
         return st;
     QmvPlan plan;
-    if ((st = qmv_plan(fmt, rows, nb, batch, dev, &plan)) != QMD_OK)
+    if ((st = qmv_plan(fmt, rows, nb, batch, dev, &plan, fused ? QMV_PACK : dump ? QMV_DUMP : QMV_PLAIN)) != QMD_OK)
         return st;
     QmvArgs a;
     a.fmt = fmt;
@@ -214,6 +247,10 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
     a.batch = batch;
     a.dbg_dots = dump ? dots : nullptr;
     a.dbg_sm = dump ? sm : nullptr;
+    a.x = x;
+    a.xq_qs_out = fused && want_out ? xq_out.qs : nullptr;
+    a.xq_d_out = fused && want_out ? xq_out.d : nullptr;
+    a.xq_bs_out = fused && want_out ? xq_out.bsums : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return q6 ? launch_qmv_q6k(a, plan, s) : launch_qmv_q4k(a, plan, s);
 }
@@ -243,14 +280,25 @@ qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *
 qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                        int64_t rows, int64_t K, int batch, void *stream)
 {
-    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, nullptr, nullptr, false, stream);
+    const qmd_q8k none = {nullptr, nullptr, nullptr};
+    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, nullptr, nullptr, false, nullptr, none, stream);
+}
+
+qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                         float *y, int64_t rows, int64_t K, int batch, void *stream)
+{
+    if (!x)
+        return QMD_ERR_NULL;
+    const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
+    return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream);
 }
 
 qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,
                                   float *y, int64_t rows, int64_t K, int batch, int32_t *dots,
                                   int32_t *sm, void *stream)
 {
-    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, dots, sm, true, stream);
+    const qmd_q8k none = {nullptr, nullptr, nullptr};
+    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, dots, sm, true, nullptr, none, stream);
 }
 
 int64_t qmd_q6k_prefix_stride(int64_t K)
@@ -350,11 +398,13 @@ qmd_status qmd_get_device_error(void *stream)
 
 void qmd_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
 
-void qmd_debug_set_plan(int row_groups, int ctas_per_sm, int max_stages)
+void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int ctas_per_sm)
 {
-    g_force_rg.store(row_groups > 0 ? row_groups : 0);
-    g_force_cps.store(ctas_per_sm > 0 ? ctas_per_sm : 0);
+    g_force_rg.store(row_groups > 0 && row_groups <= 32 ? row_groups : 0);
+    g_force_rows.store(rows_per_stage == 1 || rows_per_stage == 2 || rows_per_stage == 4 || rows_per_stage == 8
+                           ? rows_per_stage : 0);
     g_force_stages.store(max_stages > 0 ? max_stages : 0);
+    g_force_cps.store(ctas_per_sm > 0 && ctas_per_sm <= 8 ? ctas_per_sm : 0);
 }
 
 qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int batch, int *grid,
@@ -379,7 +429,7 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
     if (threads) *threads = p.threads;
     if (smem_bytes) *smem_bytes = p.smem;
     if (stages) *stages = p.stages;
-    if (rows_per_stage) *rows_per_stage = p.rows_per_stage;
+    if (rows_per_stage) *rows_per_stage = p.RG * p.PR;
     return QMD_OK;
 }
 
@@ -398,6 +448,8 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)
         return fail(QMD_ERR_LAUNCH, "debug wait launch", e);
     return QMD_OK;
 }
+
+void qmd_debug_set_launch_flags(unsigned flags) { g_launch_flags.store(flags); }
 
 int qmd_version(void) { return 100; }
 

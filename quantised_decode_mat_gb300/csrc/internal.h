@@ -31,6 +31,10 @@ unsigned *device_error_word();
 
 uint64_t wait_limit_ns();
 
+// Test-only launch flags (bit 0: launch without programmatic dependent launch).
+unsigned launch_flags();
+enum : unsigned { LAUNCH_NO_PDL = 1u };
+
 // Record a CUDA error for qmd_last_error_detail and map it to a status.
 qmd_status fail(qmd_status st, const char *what, cudaError_t e);
 
@@ -48,16 +52,22 @@ struct QmvArgs {
     int batch;
     int32_t *dbg_dots;  // non-NULL selects the recording variant
     int32_t *dbg_sm;
+    const float *x;      // non-NULL selects the fused form (packs x itself)
+    int8_t *xq_qs_out;   // fused form: optional copy of the packed activations
+    float *xq_d_out;
+    int16_t *xq_bs_out;
 };
 
 struct QmvPlan {
-    int grid, threads, smem, stages, rows_per_stage;
-    int WR, RG, PR;
-    int row_bytes, pre_bytes, stage_bytes;
+    int grid, threads, smem, stages;
+    int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
+    int row_bytes, pre_bytes, stage_bytes, row_stride;
 };
 
 // Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.
-qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *plan);
+// mode: 0 plain, 1 recording, 2 fused pack (the kernel variants)
+qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *plan,
+                    int mode = 0);
 
 qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);

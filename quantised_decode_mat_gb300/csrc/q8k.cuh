@@ -1,0 +1,56 @@
+// q8k.cuh -- the q8_K block quantiser shared by the stand-alone pack kernel and the fused
+// pack + mat-vec kernel, so that both produce the same bytes.
+//
+// "Language models on the device: the cajeta-llm kernels", §1: activations are quantised on
+// the device to q8_K, 256 values a block, one scale and eight sub-block sums.  Per block, all
+// in f32: amax = max |x|; iscale = 127 / amax (rounded once); code = clamp(round-to-nearest-
+// even(x * iscale), -127, 127) with the product rounded once; d = amax / 127; the sum of each
+// run of 32 codes.  If amax is 0 every output is 0.  If 127 / amax overflows to infinity, a
+// zero value's product is NaN and its code is 0.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmd {
+
+struct Q8Block {
+    uint2 codes;  // this lane's 8 codes, packed little-endian
+    int sum4;     // the lane's sub-block sum (valid in lanes 4j, for sub-block j)
+    float d;      // the block scale (valid in every lane)
+};
+
+// One warp quantises one 256-value block; lane l owns values 8l .. 8l+7 (v[0..8)).
+__device__ __forceinline__ Q8Block q8k_quantise_block(const float (&v)[8])
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+
+    const float iscale = amax == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax);
+    int q[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float pr = __fmul_rn(v[i], iscale);
+        int r = pr != pr ? 0 : __float2int_rn(pr);
+        r = min(127, max(-127, r));
+        q[i] = r;
+        sum += r;
+    }
+    Q8Block out;
+    out.codes.x = (q[0] & 255) | ((q[1] & 255) << 8) | ((q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
+    out.codes.y = (q[4] & 255) | ((q[5] & 255) << 8) | ((q[6] & 255) << 16) | ((uint32_t)(q[7] & 255) << 24);
+    // sub-block j = lanes 4j .. 4j+3
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    out.sum4 = sum;
+    out.d = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
+    return out;
+}
+
+}  // namespace qmd

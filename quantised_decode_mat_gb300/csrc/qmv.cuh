@@ -1,4 +1,5 @@
-// qmv.cuh -- the Q4_K / Q6_K x q8_K decode mat-vec kernel (templated on format and batch).
+// qmv.cuh -- the Q4_K / Q6_K x q8_K decode mat-vec kernel (templated on format, batch, rows
+// per stage).
 //
 // What it computes ("Language models on the device: the cajeta-llm kernels"):
 //   §1   integer dot products of weight codes against q8_K activation bytes, with the
@@ -7,28 +8,28 @@
 //   §2.1 a reduction over the row's blocks finishes each output row;
 //   §2.2 batched decode: one pass over a weight row is dotted against up to 8 vectors.
 //
-// How, on sm_103a (differs from the pages' wave-per-row design, which had one wave own a row
-// and each lane load its own words):
-//   * Persistent CTAs, each owning a contiguous range of rows.  A row range is one contiguous
-//     span of weight bytes, so it is streamed into a ring of shared-memory stages by 1-D bulk
-//     async copies (cp.async.bulk, one elected thread, mbarrier completion), evict-first in
-//     L2.  Nothing else is read from HBM in the main loop.
-//   * A CTA is RG row groups of WR warps; warp w of a group covers blocks 4w .. 4w+3 of a
-//     row and lane (g, k) = (lane/8, lane%8) one 16-byte slice k of block 4w+g.  A thread's
-//     slice is the same for every row, so its activation bytes (2 x 16 B per vector) are
-//     loaded once into registers and reused across all rows; per row a thread reads 16 B of
+// How, on sm_103a.  The pages' design has one wave own a row, each lane loading its own words
+// from global memory, with "prefetch twins" issuing the next block's loads early.  Here:
+//   * Persistent CTAs own contiguous row ranges.  A CTA's rows stream through a ring of
+//     shared-memory stages (each RG x PR whole rows) by 1-D bulk async copies (cp.async.bulk,
+//     mbarrier completion, L2 evict-first): kilobytes in flight per SM without registers.
+//   * A CTA is RG row groups of WR = ceil(nb / 4) warps.  Warp w of a group covers blocks
+//     4w .. 4w+3 of each of its PR rows; lane (g, k) = (lane / 8, lane % 8) takes 16-byte slice
+//     k of block 4w+g.  A thread's slice is the same for every row, so its activation bytes
+//     (2 x 16 B per vector) stay in registers for the whole kernel.  Per row it reads 16 B of
 //     codes (plus the block header) from shared memory, widens nibbles / 6-bit codes in
 //     registers and runs 8 dp4a per vector.
-//   * Integer partial sums S of a block (8 lanes) are combined exactly by an 8-lane
-//     reduce-scatter over PR rows x B vectors, so each lane ends with one (row, vector)
-//     block total and computes that block's f32 epilogue exactly as the oracle states it.
-//   * Block terms are summed in f32 by a declared tree: the four blocks of a warp as
-//     (t0 + t1) + (t2 + t3) (xor-shuffles 8, 16), then the warps' group sums left to right.
-//   * Programmatic dependent launch: the weight stream is started before waiting for the
-//     previous kernel in the stream (which produced the activations); everything that reads
-//     activations or writes y comes after the wait.
-//   * Every pipeline wait is bounded; on give-up the CTA sets the device error word, waits
-//     (bounded) for its own copies in flight, and exits.
+//   * The 8 lanes of a block combine their integers exactly by a reduce-scatter over the
+//     PR x B (row, vector) slots, so each lane holds one slot's block total and evaluates
+//     that block's f32 epilogue; the warp then sums its four blocks as (t0 + t1) + (t2 + t3).
+//   * No CTA-wide barrier in the main loop.  Each warp posts its per-row partials in shared
+//     memory and bumps the stage's arrival counter; the warp that arrives last adds the WR
+//     partials of each row left to right, writes y, and re-issues the stage's copy.  Warps
+//     never wait for one another, only for data.
+//   * Programmatic dependent launch: the first stages are requested before waiting for the
+//     previous kernel in the stream (which produces the activations).
+//   * Every barrier wait is bounded; on give-up a warp flags the device error word, waits
+//     (bounded) for the CTA's copies in flight, and exits.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -36,6 +37,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "q8k.cuh"
 
 namespace qmd {
 
@@ -47,68 +49,77 @@ struct QmvKParams {
     const int16_t *xbs;
     float *y;
     int64_t rows;
-    int nb, WR, RG, stages, row_bytes, pre_bytes, stage_bytes;
+    int nb, WR, RG, stages, row_bytes, pre_bytes, stage_bytes, row_stride;
     int32_t *dbg_dots;
     int32_t *dbg_sm;
+    const float *x;       // fused form: f32 activations [B][K], packed inside the kernel
+    int8_t *xq_qs_out;    // fused form, optional: the packed activations, written by CTA 0
+    float *xq_d_out;
+    int16_t *xq_bs_out;
     unsigned *err;
     unsigned long long wait_ns;
 };
 
-template <int B>
-struct Tiling {
-    static constexpr int PR = (8 / B) > 0 ? (8 / B) : 1;  // rows per row group per stage
-    static constexpr int P = PR * B;                      // (row, vector) totals per 8 lanes
-};
+// Kernel variants: plain; recording the integer arithmetic; packing f32 activations itself.
+enum QmvMode { QMV_PLAIN = 0, QMV_DUMP = 1, QMV_PACK = 2 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 struct SmemLayout {
-    int dx_off, bs_off, red_off, bar_off, total;
+    int red_off, cnt_off, bar_off, dx_off, bs_off, acts_off, total;
 };
 
-// Shared memory: [stages][stage_bytes] ring | dx f32 [B][nb] | bsums i16 [B][nb][8] (Q4_K)
-//                | red f32 [2][RG][WR][8] | mbarriers u64 [stages]
-__host__ __device__ inline SmemLayout qmv_smem_layout(int stages, int stage_bytes, int B, int nb,
-                                                      bool q4k, int RG, int WR)
+// Shared memory: ring [stages][stage_bytes] | red f32 [stages][RG][WR][8] | counters u32
+// [stages] | mbarriers u64 [stages] | dx f32 [B][nb] | Q4_K bsums i16 [B][nb][8] | fused form:
+// the packed codes i8 [B][K]
+__host__ __device__ inline SmemLayout qmv_smem_layout(int stages, int stage_bytes, int RG, int WR,
+                                                      int B, int nb, bool q6, bool pack = false)
 {
     SmemLayout L;
     int o = stages * stage_bytes;
+    L.red_off = o;
+    o += stages * RG * WR * 8 * 4;
+    L.cnt_off = o;
+    o = align_up(o + stages * 4, 8);
+    L.bar_off = o;
+    o += stages * 8;
     L.dx_off = o;
     o = align_up(o + B * nb * 4, 16);
     L.bs_off = o;
-    if (q4k)
+    if (!q6)
         o += B * nb * 16;
-    L.red_off = o;
-    o += 2 * RG * WR * 8 * 4;
-    o = align_up(o, 8);
-    L.bar_off = o;
-    o += stages * 8;
+    o = align_up(o, 16);
+    L.acts_off = o;
+    if (pack)
+        o += B * nb * 256;
     L.total = align_up(o, 16);
     return L;
 }
 
-// 8-lane reduce-scatter (lanes differing in bits 0..2): on return lane k holds the sum over
-// the 8 lanes of value index k.  Integer adds, so the order is immaterial.
-__device__ __forceinline__ int reduce_scatter8(int (&v)[8], int k)
+// Reduce-scatter over the 8 lanes of a block (lane bits 0..2): v[0..P) are this lane's partial
+// sums for P slots (P a power of two); on return the lane holds the 8-lane total of slot
+// k >> (3 - log2 P).  Integer adds, so the order is immaterial.
+template <int P>
+__device__ __forceinline__ int reduce_scatter(int (&v)[P], int k)
 {
+    constexpr int LP = P >= 8 ? 3 : P >= 4 ? 2 : P >= 2 ? 1 : 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = k & 4;
-        const int send = up ? v[i] : v[i + 4];
-        const int keep = up ? v[i + 4] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
+    for (int st = 0; st < LP; ++st) {
+        const int half = P >> (st + 1);
+        const int m = 4 >> st;
+        const bool up = k & m;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = k & 2;
-        const int send = up ? v[i] : v[i + 2];
-        const int keep = up ? v[i + 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        for (int i = 0; i < half; ++i) {
+            const int send = up ? v[i] : v[i + half];
+            const int keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
     }
-    const bool up = k & 1;
-    const int send = up ? v[0] : v[1];
-    const int keep = up ? v[1] : v[0];
-    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    int s = v[0];
+#pragma unroll
+    for (int st = LP; st < 3; ++st)
+        s += __shfl_xor_sync(0xffffffffu, s, 4 >> st);
+    return s;
 }
 
 __device__ __forceinline__ int dp4a_chain(const uint4 &w, const uint4 &a)
@@ -119,16 +130,54 @@ __device__ __forceinline__ int dp4a_chain(const uint4 &w, const uint4 &a)
     return __dp4a((int)w.w, (int)a.w, s);
 }
 
-template <bool Q6, int B, bool DUMP>
-__global__ void __launch_bounds__(B <= 2 ? 1024 : 512, 1) qmv_kernel(const QmvKParams p)
+// Four-way byte dot product with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 {
-    constexpr int PR = Tiling<B>::PR;
-    constexpr int P = Tiling<B>::P;
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Dot of the high nibbles of w (left in place, i.e. 16 x code) with a: 16 x the nibble dot.
+__device__ __forceinline__ int dp4a_chain_hi16(const uint4 &w, const uint4 &a)
+{
+    int s = dp4a_us(w.x & 0xF0F0F0F0u, a.x, 0);
+    s = dp4a_us(w.y & 0xF0F0F0F0u, a.y, s);
+    s = dp4a_us(w.z & 0xF0F0F0F0u, a.z, s);
+    return dp4a_us(w.w & 0xF0F0F0F0u, a.w, s);
+}
+
+__device__ __forceinline__ int dp4a_chain_lo(const uint4 &w, const uint4 &a)
+{
+    int s = __dp4a((int)(w.x & 0x0F0F0F0Fu), (int)a.x, 0);
+    s = __dp4a((int)(w.y & 0x0F0F0F0Fu), (int)a.y, s);
+    s = __dp4a((int)(w.z & 0x0F0F0F0Fu), (int)a.z, s);
+    return __dp4a((int)(w.w & 0x0F0F0F0Fu), (int)a.w, s);
+}
+
+// Threads a CTA may have: 1024 for one or two vectors (32 warps cover K = 32768), else 512.
+// The recording variant keeps the lower bound so that it never spills.
+__host__ __device__ constexpr int qmv_max_threads(int B, int mode)
+{
+    return (B <= 2 && mode != QMV_DUMP) ? 1024 : 512;
+}
+
+template <bool Q6, int B, int PR, int MODE>
+__global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const QmvKParams p)
+{
+    constexpr bool DUMP = MODE == QMV_DUMP;
+    constexpr bool PACK = MODE == QMV_PACK;
+    constexpr int P = PR * B;                                       // (row, vector) slots
+    static_assert(P >= 1 && P <= 8, "PR x B must be at most 8");
+    constexpr int PP = P > 4 ? 8 : P > 2 ? 4 : P > 1 ? 2 : 1;       // padded to a power of two
+    constexpr int LP = PP == 8 ? 3 : PP == 4 ? 2 : PP == 2 ? 1 : 0;
+    constexpr int DUP = 8 >> LP;  // lanes of a block holding the same slot
     constexpr int BLOCK_BYTES = Q6 ? 208 : 144;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int WR = p.WR, RG = p.RG, nb = p.nb;
+    const int NWT = WR * RG;  // warps in the CTA
     const int rg = warp / WR, wr = warp - rg * WR;
     const int g = lane >> 3, k = lane & 7;
     const int blk = 4 * wr + g;
@@ -137,42 +186,46 @@ __global__ void __launch_bounds__(B <= 2 ? 1024 : 512, 1) qmv_kernel(const QmvKP
     const int64_t r0 = p.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = p.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
     const int nch = (int)((r1 - r0 + TR - 1) / TR);
-    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, B, nb, !Q6, RG, WR);
+    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, RG, WR, B, nb, Q6, PACK);
+    float *s_red = reinterpret_cast<float *>(smem + L.red_off);
+    unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + L.cnt_off);
     const float *s_dx = reinterpret_cast<const float *>(smem + L.dx_off);
     const int16_t *s_bs = reinterpret_cast<const int16_t *>(smem + L.bs_off);
-    float *s_red = reinterpret_cast<float *>(smem + L.red_off);
     const uint32_t bar0 = smem_addr(smem + L.bar_off);
     const uint32_t ring0 = smem_addr(smem);
 
-    // Stream chunk c (rows r0 + c*TR ..) into stage c % stages.
+    // Stream chunk c (rows r0 + c*TR ..) into stage c % stages.  The chunk's rows are one
+    // contiguous span of W, copied by as few bulk copies as possible (each issue costs the
+    // issuing thread tens of nanoseconds), plus one copy of the rows' Q6_K prefix.
     auto issue = [&](int c) {
         const int st = c % p.stages;
         const int64_t rs = r0 + (int64_t)c * TR;
         const int nr = (int)min((int64_t)TR, r1 - rs);
         const uint32_t bar = bar0 + 8u * st;
-        const uint32_t body = (uint32_t)nr * (uint32_t)p.row_bytes;
-        const uint32_t pre = Q6 ? (uint32_t)nr * (uint32_t)p.pre_bytes : 0u;
+        const uint32_t body = (uint32_t)(nr * p.row_bytes);
+        const uint32_t pre = Q6 ? (uint32_t)(nr * p.pre_bytes) : 0u;
         mbar_arrive_expect_tx(bar, body + pre);
         const uint64_t pol = policy_evict_first();
+        const uint32_t dst = ring0 + (uint32_t)(st * p.stage_bytes);
         const uint8_t *src = p.W + rs * p.row_bytes;
-        const uint32_t dst = ring0 + (uint32_t)st * (uint32_t)p.stage_bytes;
-#pragma unroll 1
-        for (uint32_t off = 0; off < body; off += 16384u)
-            bulk_copy_g2s(dst + off, src + off, min(16384u, body - off), bar, pol);
+        for (uint32_t off = 0; off < body; off += 65536u)
+            bulk_copy_g2s(dst + off, src + off, min(65536u, body - off), bar, pol);
         if (Q6)
-            bulk_copy_g2s(dst + (uint32_t)TR * (uint32_t)p.row_bytes, p.Wpre + rs * p.pre_bytes, pre,
-                          bar, pol);
+            bulk_copy_g2s(dst + (uint32_t)(TR * p.row_stride), p.Wpre + rs * p.pre_bytes, pre, bar, pol);
     };
 
     if (tid == 0) {
-        for (int i = 0; i < p.stages; ++i)
+        for (int i = 0; i < p.stages; ++i) {
             mbar_init(bar0 + 8u * i, 1);
+            s_cnt[i] = 0;
+        }
         fence_barrier_init();
-        const int first = min(p.stages, nch);
-        for (int c = 0; c < first; ++c)
-            issue(c);
     }
     __syncthreads();
+    // the first stages, one per warp (issuing a bulk copy costs its thread tens of ns)
+    for (int c = warp; c < min(p.stages, nch); c += NWT)
+        if (lane == 0)
+            issue(c);
 
     pdl_launch_dependents();
     pdl_wait();  // activations come from earlier work in the stream
@@ -180,19 +233,60 @@ __global__ void __launch_bounds__(B <= 2 ? 1024 : 512, 1) qmv_kernel(const QmvKP
     // ---- this thread's activation slice, for all B vectors (fixed for every row) ----------
     const int64_t K = (int64_t)nb * 256;
     int off_lo;
-    if (Q6) {
-        const int hh = k >> 2, tl = (k >> 1) & 1, half = k & 1;
-        off_lo = 128 * hh + 32 * tl + 16 * half;  // elements of group 8hh + 2tl + half
-    } else {
-        off_lo = 64 * (k >> 1) + 16 * (k & 1);  // elements of sub-block 2c, half k&1
+    if (Q6)
+        off_lo = 128 * (k >> 2) + 32 * ((k >> 1) & 1) + 16 * (k & 1);  // group 8hh + 2tl + half
+    else
+        off_lo = 64 * (k >> 1) + 16 * (k & 1);  // sub-block 2c, half k&1
+    constexpr int HI = Q6 ? 64 : 32;            // the high-nibble run sits this far further on
+    if (PACK) {
+        // Fused form: quantise the B x nb activation blocks into shared memory, one warp per
+        // block, with the same arithmetic as the stand-alone pack kernel.
+        int8_t *acts = reinterpret_cast<int8_t *>(smem + L.acts_off);
+        float *dx = reinterpret_cast<float *>(smem + L.dx_off);
+        int16_t *bs = reinterpret_cast<int16_t *>(smem + L.bs_off);
+        const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
+        constexpr int QB = 4;  // blocks per warp whose loads are in flight together
+        for (int b0 = warp; b0 < B * nb; b0 += QB * NWT) {
+            float4 xa[QB], xb[QB];
+#pragma unroll
+            for (int u = 0; u < QB; ++u) {
+                const int b = b0 + u * NWT;
+                if (b < B * nb) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
+                    xa[u] = src[0];
+                    xb[u] = src[1];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QB; ++u) {
+                const int b = b0 + u * NWT;  // the same for every lane of the warp
+                if (b < B * nb) {
+                    const float v8[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                    const Q8Block r = q8k_quantise_block(v8);
+                    *reinterpret_cast<uint2 *>(acts + b * 256 + 8 * lane) = r.codes;
+                    if (!Q6 && (lane & 3) == 0)
+                        bs[b * 8 + (lane >> 2)] = (int16_t)r.sum4;
+                    if (lane == 0)
+                        dx[b] = r.d;
+                    if (out) {
+                        *reinterpret_cast<uint2 *>(p.xq_qs_out + (int64_t)b * 256 + 8 * lane) = r.codes;
+                        if ((lane & 3) == 0)
+                            p.xq_bs_out[b * 8 + (lane >> 2)] = (int16_t)r.sum4;
+                        if (lane == 0)
+                            p.xq_d_out[b] = r.d;
+                    }
+                }
+            }
+        }
+        __syncthreads();
     }
-    constexpr int HI = Q6 ? 64 : 32;  // the high-nibble elements sit this far further on
+    const int8_t *act_src = PACK ? reinterpret_cast<const int8_t *>(smem + L.acts_off) : p.xqs;
     uint4 alo[B], ahi[B];
     int xs_lo[B], xs_hi[B];
 #pragma unroll
     for (int v = 0; v < B; ++v) {
         if (blk_ok) {
-            const int8_t *base = p.xqs + v * K + 256 * blk + off_lo;
+            const int8_t *base = act_src + v * K + 256 * blk + off_lo;
             alo[v] = *reinterpret_cast<const uint4 *>(base);
             ahi[v] = *reinterpret_cast<const uint4 *>(base + HI);
         } else {
@@ -205,7 +299,7 @@ __global__ void __launch_bounds__(B <= 2 ? 1024 : 512, 1) qmv_kernel(const QmvKP
             xs_hi[v] = dp4a_chain(ones, ahi[v]);
         }
     }
-    {
+    if (!PACK) {
         float *dx = reinterpret_cast<float *>(smem + L.dx_off);
         for (int i = tid; i < B * nb; i += blockDim.x)
             dx[i] = p.xd[i];
@@ -218,167 +312,194 @@ __global__ void __launch_bounds__(B <= 2 ? 1024 : 512, 1) qmv_kernel(const QmvKP
     }
     __syncthreads();
 
+    // lane constants for reading a block's scales and codes
+    const bool hiw = (k >> 1) >= 2;  // Q4_K: sub-blocks 4..7 use the split 6-bit fields
+    const uint32_t sel_lo = Q6 ? (uint32_t)(0x4440 | (2 * ((k >> 1) & 1) + (k & 1)))
+                               : (uint32_t)(0x4440 | (((k >> 1) & 1) << 1));
+    const uint32_t sel_hi = sel_lo + 1;  // Q4_K: the next byte (sub-block 2c+1)
+    const int q6_qh_off = 128 + 32 * (k >> 2) + 16 * (k & 1);
+    const int q6_sc_off = 192 + 8 * (k >> 2);
+    const int q6_sl = 4 - 2 * ((k >> 1) & 1);  // low run: 2-bit field t=tl moved to bits 4..5
+    const int q6_sh = 2 * ((k >> 1) & 1);      // high run: field t=tl+2 moved to bits 4..5
+
+    const int slot = k >> (3 - LP);
+    const bool slot_ok = slot < P;
+    const int spr = slot_ok ? slot / B : PR, sv = slot_ok ? slot - (slot / B) * B : 0;
+    const int srow = rg * PR + spr;  // the slot's row within the stage
+
     const unsigned long long wait_ns = p.wait_ns;
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
         const int st = c % p.stages;
         const uint32_t parity = (uint32_t)(c / p.stages) & 1u;
-        const bool ok = mbar_wait_bounded(bar0 + 8u * st, parity, wait_ns);
-        const uint8_t *stage = smem + (size_t)st * p.stage_bytes;
-        const int64_t rs = r0 + (int64_t)c * TR;
-        const int nr = (int)min((int64_t)TR, r1 - rs);
-
-        // ---- integer slice dots, folded with the sub-block scales -------------------------
-        int S[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            S[i] = 0;
-#pragma unroll
-        for (int pr = 0; pr < PR; ++pr) {
-            const int i = rg * PR + pr;
-            if (blk_ok && i < nr) {
-                const uint8_t *bp = stage + i * p.row_bytes + blk * BLOCK_BYTES;
-                int sc_lo, sc_hi;
-                uint4 wlo, whi;  // codes of the low / high element runs, one byte each
-                if (!Q6) {
-                    const uint4 h = lds128(bp);
-                    const uint4 q = lds128(bp + 16 + 16 * k);
-                    const int c2 = k >> 1;
-                    const uint32_t scw = c2 < 2 ? (h.y & 0x3F3F3F3Fu)
-                                                : ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u));
-                    const int sh = (c2 & 1) << 4;
-                    sc_lo = (scw >> sh) & 0xff;
-                    sc_hi = (scw >> (sh + 8)) & 0xff;
-                    wlo = make_uint4(q.x & 0x0F0F0F0Fu, q.y & 0x0F0F0F0Fu, q.z & 0x0F0F0F0Fu,
-                                     q.w & 0x0F0F0F0Fu);
-                    whi = make_uint4((q.x >> 4) & 0x0F0F0F0Fu, (q.y >> 4) & 0x0F0F0F0Fu,
-                                     (q.z >> 4) & 0x0F0F0F0Fu, (q.w >> 4) & 0x0F0F0F0Fu);
-                } else {
-                    const int hh = k >> 2, tl = (k >> 1) & 1, half = k & 1;
-                    const uint4 ql = lds128(bp + 16 * k);
-                    const uint4 qh = lds128(bp + 128 + 32 * hh + 16 * half);
-                    const uint2 scw = *reinterpret_cast<const uint2 *>(bp + 192 + 8 * hh);
-                    const int sb = 8 * (2 * tl + half);
-                    sc_lo = (int)(int8_t)(scw.x >> sb);
-                    sc_hi = (int)(int8_t)(scw.y >> sb);
-                    const int slo = 2 * tl, shi = 2 * tl + 4;
-                    wlo = make_uint4((ql.x & 0x0F0F0F0Fu) | (((qh.x >> slo) & 0x03030303u) << 4),
-                                     (ql.y & 0x0F0F0F0Fu) | (((qh.y >> slo) & 0x03030303u) << 4),
-                                     (ql.z & 0x0F0F0F0Fu) | (((qh.z >> slo) & 0x03030303u) << 4),
-                                     (ql.w & 0x0F0F0F0Fu) | (((qh.w >> slo) & 0x03030303u) << 4));
-                    whi = make_uint4(((ql.x >> 4) & 0x0F0F0F0Fu) | (((qh.x >> shi) & 0x03030303u) << 4),
-                                     ((ql.y >> 4) & 0x0F0F0F0Fu) | (((qh.y >> shi) & 0x03030303u) << 4),
-                                     ((ql.z >> 4) & 0x0F0F0F0Fu) | (((qh.z >> shi) & 0x03030303u) << 4),
-                                     ((ql.w >> 4) & 0x0F0F0F0Fu) | (((qh.w >> shi) & 0x03030303u) << 4));
-                }
-#pragma unroll
-                for (int v = 0; v < B; ++v) {
-                    int dl = dp4a_chain(wlo, alo[v]);
-                    int dh = dp4a_chain(whi, ahi[v]);
-                    if (Q6) {
-                        dl -= 32 * xs_lo[v];
-                        dh -= 32 * xs_hi[v];
-                    }
-                    S[pr * B + v] = sc_lo * dl + sc_hi * dh;
-                    if (DUMP) {
-                        int32_t *dd = p.dbg_dots + ((v * p.rows + rs + i) * nb + blk) * 16;
-                        if (Q6) {
-                            const int s_lo = 8 * (k >> 2) + (k & 3);
-                            dd[s_lo] = dl;
-                            dd[s_lo + 4] = dh;
-                        } else {
-                            dd[2 * k] = dl;
-                            dd[2 * k + 1] = dh;
-                        }
-                    }
-                }
-            }
-        }
-
-        // ---- exact block totals, then this lane's block epilogue --------------------------
-        const int Sv = reduce_scatter8(S, k);
-        float t = 0.0f;
-        if (k < P) {
-            const int pr = k / B, v = k - pr * B;
-            const int i = rg * PR + pr;
-            if (blk_ok && i < nr) {
-                const uint8_t *bp = stage + i * p.row_bytes + blk * BLOCK_BYTES;
-                const float dx = s_dx[v * nb + blk];
-                const float fS = __int2float_rn(Sv);
-                int M = 0;
-                if (!Q6) {
-                    const uint4 h = lds128(bp);
-                    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
-                    const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-                    const uint32_t m0 = h.z & 0x3F3F3F3Fu;
-                    const uint32_t m1 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-                    const int4 bs = *reinterpret_cast<const int4 *>(s_bs + (v * nb + blk) * 8);
-                    M = __dp2a_lo(bs.x, (int)m0, 0);
-                    M = __dp2a_hi(bs.y, (int)m0, M);
-                    M = __dp2a_lo(bs.z, (int)m1, M);
-                    M = __dp2a_hi(bs.w, (int)m1, M);
-                    const float fM = __int2float_rn(M);
-                    t = __fmul_rn(dx, __fsub_rn(__fmul_rn(d, fS), __fmul_rn(dmin, fM)));
-                } else {
-                    const unsigned short dbits = *reinterpret_cast<const unsigned short *>(
-                        stage + TR * p.row_bytes + i * p.pre_bytes + 2 * blk);
-                    const float d = __half2float(__ushort_as_half(dbits));
-                    t = __fmul_rn(dx, __fmul_rn(d, fS));
-                }
-                if (DUMP) {
-                    int32_t *sm = p.dbg_sm + ((v * p.rows + rs + i) * nb + blk) * 2;
-                    sm[0] = Sv;
-                    sm[1] = M;
-                }
-            }
-        }
-        // blocks 4wr .. 4wr+3 of this warp: (t0 + t1) + (t2 + t3)
-        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 8));
-        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16));
-        const int buf = c & 1;
-        if (g == 0 && k < P)
-            s_red[((buf * RG + rg) * WR + wr) * 8 + k] = t;
-
-        if (__syncthreads_or(!ok)) {
-            // A copy did not land in time: flag it, wait (bounded) for this CTA's copies still
-            // in flight so none writes shared memory after exit, and leave.
-            if (tid == 0) {
+        if (!mbar_wait_bounded(bar0 + 8u * st, parity, wait_ns)) {
+            // A copy did not land in time: flag it, wait (bounded) for the copies that may
+            // still be in flight so that none writes shared memory after the CTA exits, leave.
+            if (lane == 0) {
                 atomicOr(p.err, ERRBIT_QMV_WAIT);
-                const int last = min(nch, c + p.stages);
-                for (int cc = c; cc < last; ++cc) {
+                for (int cc = c; cc < min(nch, c + p.stages); ++cc)
                     if (!mbar_wait_bounded(bar0 + 8u * (cc % p.stages), (uint32_t)(cc / p.stages) & 1u,
                                            wait_ns)) {
                         atomicOr(p.err, ERRBIT_DRAIN_WAIT);
                         break;
                     }
-                }
             }
+            __syncwarp();
             return;
         }
-        if (tid == 0 && c + p.stages < nch)
-            issue(c + p.stages);  // every thread is done with this stage
+        const uint8_t *stage = smem + (size_t)st * p.stage_bytes;
+        const int64_t rs = r0 + (int64_t)c * TR;
+        const int nr = (int)min((int64_t)TR, r1 - rs);
 
-        // ---- row totals: the warps' group sums, left to right ------------------------------
-        if (wr == 0 && g == 0 && k < P) {
-            const int pr = k / B, v = k - pr * B;
-            const int i = rg * PR + pr;
-            if (i < nr) {
-                const float *red = s_red + ((buf * RG + rg) * WR) * 8 + k;
-                float acc = red[0];
-                for (int w = 1; w < WR; ++w)
-                    acc = __fadd_rn(acc, red[w * 8]);
-                p.y[v * p.rows + rs + i] = acc;
+        // ---- integer slice dots, folded with the sub-block scales -------------------------
+        // Q4_K partials are carried as 16 x S (the high-nibble dots come out scaled by 16);
+        // Q6_K partials are S itself.
+        int S[PP];
+#pragma unroll
+        for (int i = 0; i < PP; ++i)
+            S[i] = 0;
+        auto row_dots = [&](int i, int pr) {
+            const uint8_t *bp = stage + i * p.row_stride + blk * BLOCK_BYTES;
+            if (!Q6) {
+                const uint4 h = lds128(bp);
+                const uint4 q = lds128(bp + 16 + 16 * k);
+                // this lane's sub-blocks' 6-bit scales (bytes of scw), then the two it needs
+                const uint32_t scw = hiw ? ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u))
+                                         : (h.y & 0x3F3F3F3Fu);
+                const int sc_lo = (int)__byte_perm(scw, 0u, sel_lo);
+                const int sc_hi = (int)__byte_perm(scw, 0u, sel_hi);
+#pragma unroll
+                for (int v = 0; v < B; ++v) {
+                    const int dl = dp4a_chain_lo(q, alo[v]);
+                    const int dh16 = dp4a_chain_hi16(q, ahi[v]);
+                    S[pr * B + v] = sc_lo * (dl << 4) + sc_hi * dh16;
+                    if (DUMP) {
+                        int32_t *dd = p.dbg_dots + ((v * p.rows + rs + i) * nb + blk) * 16;
+                        dd[2 * k] = dl;
+                        dd[2 * k + 1] = dh16 >> 4;
+                    }
+                }
+            } else {
+                const uint4 ql = lds128(bp + 16 * k);
+                const uint4 qh = lds128(bp + q6_qh_off);
+                const uint2 scw = *reinterpret_cast<const uint2 *>(bp + q6_sc_off);
+                const int sc_lo = (int)(int8_t)__byte_perm(scw.x, 0u, sel_lo);
+                const int sc_hi = (int)(int8_t)__byte_perm(scw.y, 0u, sel_lo);
+                uint4 wlo, whi;  // 6-bit codes of the low / high element runs, one per byte
+                wlo.x = (ql.x & 0x0F0F0F0Fu) | ((qh.x << q6_sl) & 0x30303030u);
+                wlo.y = (ql.y & 0x0F0F0F0Fu) | ((qh.y << q6_sl) & 0x30303030u);
+                wlo.z = (ql.z & 0x0F0F0F0Fu) | ((qh.z << q6_sl) & 0x30303030u);
+                wlo.w = (ql.w & 0x0F0F0F0Fu) | ((qh.w << q6_sl) & 0x30303030u);
+                whi.x = ((ql.x >> 4) & 0x0F0F0F0Fu) | ((qh.x >> q6_sh) & 0x30303030u);
+                whi.y = ((ql.y >> 4) & 0x0F0F0F0Fu) | ((qh.y >> q6_sh) & 0x30303030u);
+                whi.z = ((ql.z >> 4) & 0x0F0F0F0Fu) | ((qh.z >> q6_sh) & 0x30303030u);
+                whi.w = ((ql.w >> 4) & 0x0F0F0F0Fu) | ((qh.w >> q6_sh) & 0x30303030u);
+#pragma unroll
+                for (int v = 0; v < B; ++v) {
+                    const int dl = dp4a_chain(wlo, alo[v]) - 32 * xs_lo[v];
+                    const int dh = dp4a_chain(whi, ahi[v]) - 32 * xs_hi[v];
+                    S[pr * B + v] = sc_lo * dl + sc_hi * dh;
+                    if (DUMP) {
+                        int32_t *dd = p.dbg_dots + ((v * p.rows + rs + i) * nb + blk) * 16;
+                        const int s_lo = 8 * (k >> 2) + (k & 3);
+                        dd[s_lo] = dl;
+                        dd[s_lo + 4] = dh;
+                    }
+                }
+            }
+        };
+        if (blk_ok) {
+            if (nr == TR) {  // full chunk: no per-row predicates
+#pragma unroll
+                for (int pr = 0; pr < PR; ++pr)
+                    row_dots(rg * PR + pr, pr);
+            } else {
+#pragma unroll
+                for (int pr = 0; pr < PR; ++pr)
+                    if (rg * PR + pr < nr)
+                        row_dots(rg * PR + pr, pr);
+            }
+        }
+
+        // ---- exact block totals, then this lane's slot epilogue ----------------------------
+        const int Sv = reduce_scatter<PP>(S, k);
+        float t = 0.0f;
+        if (blk_ok && slot_ok && srow < nr) {
+            const uint8_t *bp = stage + srow * p.row_stride + blk * BLOCK_BYTES;
+            const float dx = s_dx[sv * nb + blk];
+            const int Sb = Q6 ? Sv : (Sv >> 4);  // exact: Q4_K carried 16 x S
+            const float fS = __int2float_rn(Sb);
+            int M = 0;
+            if (!Q6) {
+                const uint4 h = lds128(bp);
+                const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                const uint32_t m0 = h.z & 0x3F3F3F3Fu;
+                const uint32_t m1 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+                const int4 bs = *reinterpret_cast<const int4 *>(s_bs + (sv * nb + blk) * 8);
+                M = __dp2a_lo(bs.x, (int)m0, 0);
+                M = __dp2a_hi(bs.y, (int)m0, M);
+                M = __dp2a_lo(bs.z, (int)m1, M);
+                M = __dp2a_hi(bs.w, (int)m1, M);
+                const float fM = __int2float_rn(M);
+                t = __fmul_rn(dx, __fsub_rn(__fmul_rn(d, fS), __fmul_rn(dmin, fM)));
+            } else {
+                const unsigned short dbits = *reinterpret_cast<const unsigned short *>(
+                    stage + TR * p.row_stride + srow * p.pre_bytes + 2 * blk);
+                const float d = __half2float(__ushort_as_half(dbits));
+                t = __fmul_rn(dx, __fmul_rn(d, fS));
+            }
+            if (DUMP && (k & (DUP - 1)) == 0) {
+                int32_t *sm = p.dbg_sm + ((sv * p.rows + rs + srow) * nb + blk) * 2;
+                sm[0] = Sb;
+                sm[1] = M;
+            }
+        }
+        // blocks 4wr .. 4wr+3 of this warp: (t0 + t1) + (t2 + t3)
+        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 8));
+        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16));
+        float *red = s_red + (size_t)st * RG * WR * 8;
+        if (g == 0)
+            red[(rg * WR + wr) * 8 + k] = t;
+        __syncwarp();
+
+        // ---- arrive; the last warp of the stage finishes its rows and refills it -----------
+        unsigned last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&s_cnt[st], 1u) == (unsigned)(NWT - 1);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence_block();
+            // lane l finishes slot (l % 8) of row group l / 8, four row groups at a time
+            for (int rgb = 0; rgb < RG; rgb += 4) {
+                const int frg = rgb + (lane >> 3), fk = lane & 7;
+                const int fslot = fk >> (3 - LP);
+                const int frow = frg * PR + (fslot < P ? fslot / B : PR);
+                if (frg < RG && (fk & (DUP - 1)) == 0 && fslot < P && frow < nr) {
+                    const float *rr = red + (frg * WR) * 8 + fk;
+                    float acc = rr[0];
+                    for (int w = 1; w < WR; ++w)
+                        acc = __fadd_rn(acc, rr[w * 8]);
+                    p.y[(fslot - (fslot / B) * B) * p.rows + rs + frow] = acc;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                s_cnt[st] = 0;
+                if (c + p.stages < nch)
+                    issue(c + p.stages);  // every warp of the CTA is done with this stage
             }
         }
     }
 }
 
-template <bool Q6, int B, bool DUMP>
+template <bool Q6, int B, int PR, int MODE>
 qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
-    auto kern = qmv_kernel<Q6, B, DUMP>;
-    // opt in to the shared memory this launch needs (cached per device)
-    static int set_bytes[64] = {0};
+    auto kern = qmv_kernel<Q6, B, PR, MODE>;
+    static int set_bytes[64] = {0};  // dynamic shared memory opted in, per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64)
@@ -389,8 +510,28 @@ qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
             return fail(QMD_ERR_LAUNCH, "qmv smem attribute", e);
         set_bytes[dev] = plan.smem;
     }
+    // Persistent grid: no more CTAs than can be resident at once (rows are split by gridDim).
+    int grid = plan.grid;
+    {
+        // cached per device for the last (threads, shared bytes) this instance was asked for
+        static int c_threads[64] = {0}, c_smem[64] = {0}, c_max[64] = {0};
+        if (c_threads[dev] != plan.threads || c_smem[dev] != plan.smem) {
+            int per_sm = 0, sms = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, plan.threads, plan.smem);
+            if (e != cudaSuccess)
+                return fail(QMD_ERR_LAUNCH, "qmv occupancy", e);
+            if (per_sm < 1)
+                return QMD_ERR_SHAPE;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            c_max[dev] = per_sm * sms;
+            c_threads[dev] = plan.threads;
+            c_smem[dev] = plan.smem;
+        }
+        if (grid > c_max[dev])
+            grid = c_max[dev];
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
     cfg.dynamicSmemBytes = (size_t)plan.smem;
     cfg.stream = s;
@@ -398,11 +539,34 @@ qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = (launch_flags() & LAUNCH_NO_PDL) ? 0 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
     if (e != cudaSuccess)
         return fail(QMD_ERR_LAUNCH, "qmv launch", e);
     return QMD_OK;
+}
+
+// Rows per stage and row group (PR x B <= 8); the plan picks one.
+template <bool Q6, int B, int MODE>
+qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
+{
+    switch (plan.PR) {
+    case 1:
+        return launch_one<Q6, B, 1, MODE>(kp, plan, s);
+    case 2:
+        if constexpr (2 * B <= 8)
+            return launch_one<Q6, B, 2, MODE>(kp, plan, s);
+        break;
+    case 4:
+        if constexpr (4 * B <= 8)
+            return launch_one<Q6, B, 4, MODE>(kp, plan, s);
+        break;
+    case 8:
+        if constexpr (B == 1)
+            return launch_one<Q6, B, 8, MODE>(kp, plan, s);
+        break;
+    }
+    return QMD_ERR_SHAPE;
 }
 
 template <bool Q6>
@@ -423,16 +587,23 @@ qmd_status launch_qmv(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     kp.row_bytes = plan.row_bytes;
     kp.pre_bytes = plan.pre_bytes;
     kp.stage_bytes = plan.stage_bytes;
+    kp.row_stride = plan.row_stride;
     kp.dbg_dots = a.dbg_dots;
     kp.dbg_sm = a.dbg_sm;
+    kp.x = a.x;
+    kp.xq_qs_out = a.xq_qs_out;
+    kp.xq_d_out = a.xq_d_out;
+    kp.xq_bs_out = a.xq_bs_out;
     kp.err = device_error_word();
     kp.wait_ns = wait_limit_ns();
     if (kp.err == nullptr)
         return QMD_ERR_DEVICE;
-    const bool dump = a.dbg_dots != nullptr;
-#define QMD_CASE(BB)                                                                   \
-    case BB:                                                                           \
-        return dump ? launch_one<Q6, BB, true>(kp, plan, s) : launch_one<Q6, BB, false>(kp, plan, s);
+    const int mode = a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;
+#define QMD_CASE(BB)                                                                                 \
+    case BB:                                                                                         \
+        return mode == QMV_PACK   ? launch_rows<Q6, BB, QMV_PACK>(kp, plan, s)                       \
+               : mode == QMV_DUMP ? launch_rows<Q6, BB, QMV_DUMP>(kp, plan, s)                       \
+                                  : launch_rows<Q6, BB, QMV_PLAIN>(kp, plan, s);
     switch (a.batch) {
         QMD_CASE(1)
         QMD_CASE(2)

@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import Q4_K, Q6_K_SPLIT, QMD_QK, Q8K, bind_q6k, q6k_prefix_stride, q8k_pack, qmatvec
+from . import Q4_K, Q6_K_SPLIT, QMD_QK, Q8K, bind_q6k, q6k_prefix_stride, q8k_pack, qmatvec, qmatvec_x
 from . import synth
 
 
@@ -44,12 +44,20 @@ class Projection:
         return self.xq.batch * nb * per
 
     def matvec_bytes(self) -> int:
+        """Bytes the mat-vec kernel must read and write given packed activations."""
         return self.weight_bytes + self.act_bytes() + self.xq.batch * self.rows * 4
 
     def pack_bytes(self) -> int:
+        """Bytes the stand-alone pack kernel reads and writes."""
         nb = self.K // QMD_QK
         B = self.xq.batch
         return B * self.K * 4 + B * (self.K + nb * 4 + nb * 16)
+
+    def algorithmic_bytes(self) -> int:
+        """What the projection must move whatever the kernel split: its weights, its f32
+        activations and its f32 outputs (packed activations are an intermediate)."""
+        B = self.xq.batch
+        return self.weight_bytes + B * self.K * 4 + B * self.rows * 4
 
 
 @dataclass
@@ -59,17 +67,25 @@ class DecodeStep:
     x_all: "object" = None
     y_all: "object" = None
     host_weights: dict = field(default_factory=dict)  # (layer, name) -> canonical GGUF bytes, if kept
+    fused: bool = True  # one launch per projection (qmd_qmatvec_x) or pack + mat-vec
 
     def run(self, stream=None) -> None:
         for p in self.projs:
-            q8k_pack(p.x, p.xq, stream)
-            qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+            if self.fused:
+                qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
+            else:
+                q8k_pack(p.x, p.xq, stream)
+                qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
 
     def run_matvecs(self, fmt: int | None = None, stream=None) -> int:
+        """The step's mat-vec launches only (fused form: each packs its own activations)."""
         n = 0
         for p in self.projs:
             if fmt is None or p.fmt == fmt:
-                qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+                if self.fused:
+                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
+                else:
+                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
                 n += 1
         return n
 
@@ -95,13 +111,16 @@ class DecodeStep:
 
     @property
     def launches(self) -> int:
-        return 2 * len(self.projs)
+        return (1 if self.fused else 2) * len(self.projs)
 
     def bytes(self) -> dict:
+        """algorithmic: weights + f32 activations + f32 outputs of every projection (the
+        figure the throughput is quoted on); matvec/pack: what the two-kernel form moves."""
         mv = sum(p.matvec_bytes() for p in self.projs)
         pk = sum(p.pack_bytes() for p in self.projs)
         w = sum(p.weight_bytes for p in self.projs)
-        return dict(matvec=mv, pack=pk, total=mv + pk, weights=w)
+        alg = sum(p.algorithmic_bytes() for p in self.projs)
+        return dict(algorithmic=alg, matvec=mv, pack=pk, weights=w)
 
 
 def _gen_layer(layer: int, projections, batch: int, seed_fn):
@@ -115,14 +134,15 @@ def _gen_layer(layer: int, projections, batch: int, seed_fn):
 
 
 def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STEP_PROJECTIONS,
-              device="cuda", seed_fn=synth.step_seed, keep_host_layers=(), threads: int = 8) -> DecodeStep:
+              device="cuda", seed_fn=synth.step_seed, keep_host_layers=(), threads: int = 8,
+              fused: bool = True) -> DecodeStep:
     """Generate the seeded weights and activations of a decode step and place them on the device.
 
     keep_host_layers: layers whose canonical GGUF weight bytes stay in host memory (for the
     oracle).  Q6_K weights are bound (split) on the device."""
     import torch
     dev = torch.device(device)
-    step = DecodeStep(batch=batch)
+    step = DecodeStep(batch=batch, fused=fused)
     x_sizes = [batch * K for (_, _, _, K) in projections] * layers
     y_sizes = [(batch * rows + 3) // 4 * 4 for (_, _, rows, _) in projections] * layers
     step.x_all = torch.empty(sum(x_sizes), dtype=torch.float32, device=dev)

@@ -32,9 +32,9 @@ def _lib():
     from quantised_decode_mat_gb300 import build as qbuild
     qbuild.build()
     q.lib()
-    q.debug_set_plan(0, 0, 0)
+    q.debug_set_plan()
     yield
-    q.debug_set_plan(0, 0, 0)
+    q.debug_set_plan()
 
 
 def dev(a):
@@ -209,7 +209,9 @@ def test_sweep_shapes(fmtname, rows, K, batch):
     check_against_oracle(fmtname, Wg, x, y)
 
 
-@pytest.mark.parametrize("plan", [(1, 1, 1), (1, 2, 2), (2, 1, 3), (4, 1, 1), (1, 8, 2), (3, 2, 1)])
+# (row groups per CTA, rows per group per stage, max stages, CTAs per SM)
+@pytest.mark.parametrize("plan", [(1, 1, 1, 0), (2, 2, 2, 0), (1, 8, 1, 0), (3, 4, 2, 0), (4, 1, 3, 0),
+                                  (2, 2, 8, 2), (5, 1, 2, 3)])
 @pytest.mark.parametrize("fmtname,rows,K,batch", [("q4k", 2000, 4096, 1), ("q4k", 700, 2048, 3),
                                                   ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2)])
 def test_pipeline_plans(plan, fmtname, rows, K, batch):
@@ -220,7 +222,7 @@ def test_pipeline_plans(plan, fmtname, rows, K, batch):
         x = synth.activations(5, batch, K)
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
     finally:
-        q.debug_set_plan(0, 0, 0)
+        q.debug_set_plan()
     check_against_oracle(fmtname, Wg, x, y)
 
 
@@ -257,21 +259,22 @@ def test_bind_q6k_matches_oracle_split():
 
 # ---- refusals launch nothing; bounded waits report instead of hanging ---------------------------------
 def test_refused_calls_write_nothing():
-    rows, K = 16, 512
-    Wg = synth.q4k_weights(1, rows, K)
-    xq = gpu_pack(synth.activations(1, 1, K))
-    Wd = dev(Wg.reshape(rows, -1))
-    buf, y = poisoned_y(1, rows)
-    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 500, 1, None)
-    assert st == 3
-    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr() + 8, None, xq.ptrs(), y.data_ptr(), rows, K, 1, None)
-    assert st == 5
-    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 65536, 1, None)
-    assert st == 6  # above the K limit
-    st = q.lib().qmd_qmatvec(q.Q4_K, Wd.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 32768, 3, None)
-    assert st == 6  # K limit for batch > 2
+    """Every buffer here is large enough for the largest shape passed, so a call that the host
+    wrongly accepted could not read or write outside its buffers."""
+    rows, Kmax, Bmax = 16, 65536, 8
+    W = torch.zeros(rows * (Kmax // 256) * 144, dtype=torch.uint8, device=DEV)
+    xq = q.Q8K.empty(Bmax, Kmax, DEV)
+    buf, y = poisoned_y(Bmax, rows)
+    L = q.lib()
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 500, 1, None) == 3
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr() + 8, None, xq.ptrs(), y.data_ptr(), rows, 512, 1, None) == 5
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 512, 9, None) == 4
+    # above the K limits (32768 at batch <= 2, 16384 above)
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, Kmax, 1, None) == 6
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 32768, 3, None) == 6
+    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 256 << 21, 1, None) == 6
     torch.cuda.synchronize()
-    assert torch.isnan(y).all() and guard_intact(buf, 1, rows)
+    assert torch.isnan(y).all() and guard_intact(buf, Bmax, rows)
     q.get_device_error()
 
 
@@ -295,3 +298,48 @@ def test_launch_info_shapes():
     for i in (i1, i2):
         assert i["grid"] >= sms and i["stages"] >= 1 and i["threads"] % 32 == 0
         assert i["smem_bytes"] <= 232448
+
+
+# ---- fused pack + mat-vec: the same bits as the two-call path -----------------------------------------
+FUSED = [("q4k", 256, 2048, 1), ("q4k", 4096, 4096, 1), ("q6k", 4096, 14336, 1), ("q4k", 333, 2048, 4),
+         ("q4k", 77, 4352, 5), ("q6k", 64, 3328, 4), ("q6k", 17, 14336, 8), ("q4k", 9, 32768, 1),
+         ("q6k", 130, 1792, 3), ("q4k", 1000, 1280, 2)]
+
+
+@pytest.mark.parametrize("fmtname,rows,K,batch", FUSED)
+def test_fused_equals_pack_then_matvec(fmtname, rows, K, batch):
+    seed = 11 * rows + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xd = dev(x)
+    if fmtname == "q4k":
+        W, Wa, f = dev(Wg.reshape(rows, -1)), None, q.Q4_K
+    else:
+        W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+        f = q.Q6_K_SPLIT
+    xq = q.q8k_pack(xd)
+    y2 = q.qmatvec(f, W, Wa, xq, rows=rows)
+    buf, y1 = poisoned_y(batch, rows)
+    out = q.Q8K.empty(batch, K, DEV)
+    q.qmatvec_x(f, W, Wa, xd, y1, rows=rows, xq_out=out)
+    q.get_device_error()
+    assert guard_intact(buf, batch, rows)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert torch.equal(out.qs, xq.qs) and torch.equal(out.bsums, xq.bsums)
+    assert torch.equal(out.d.view(torch.int32), xq.d.view(torch.int32))
+    check_against_oracle(fmtname, Wg, x, y1.cpu().numpy())
+
+
+def test_fused_refusals():
+    rows, K = 8, 512
+    W = torch.zeros(rows * 2 * 144, dtype=torch.uint8, device=DEV)
+    x = torch.zeros((1, K), dtype=torch.float32, device=DEV)
+    buf, y = poisoned_y(1, rows)
+    L = q.lib()
+    none = q.Q8KPtrs(None, None, None)
+    assert L.qmd_qmatvec_x(q.Q4_K, W.data_ptr(), None, None, none, y.data_ptr(), rows, K, 1, None) == 1
+    assert L.qmd_qmatvec_x(q.Q4_K, W.data_ptr(), None, x.data_ptr() + 4, none, y.data_ptr(), rows, K, 1, None) == 5
+    part = q.Q8KPtrs(x.data_ptr(), None, None)
+    assert L.qmd_qmatvec_x(q.Q4_K, W.data_ptr(), None, x.data_ptr(), part, y.data_ptr(), rows, K, 1, None) == 1
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all() and guard_intact(buf, 1, rows)
