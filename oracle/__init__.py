@@ -27,6 +27,7 @@ QK = 256
 BLOCK_BYTES = {FMT_Q4_K: 144, FMT_Q6_K: 210}
 ORDER_SEQUENTIAL = 0
 ORDER_GROUPS_OF_FOUR = 1
+ORDER_RUNS_OF_SIXTEEN = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -268,8 +268,12 @@ void oracle_block_terms(int fmt, const uint8_t *row, const int8_t *qs, const flo
  * order 0: ascending blocks, left to right:  ((t0 + t1) + t2) + ...
  * order 1: blocks in groups of four, each group summed as (t0 + t1) + (t2 + t3) with an
  *          absent block (past the row's end) counted as +0.0f, then the group sums added
- *          left to right: ((G0 + G1) + G2) + ...   This is the order the GPU path declares
- *          for its reduction; the oracle states it independently.
+ *          left to right: ((G0 + G1) + G2) + ...
+ * order 2: as order 1 within runs of four groups (16 blocks): each run's group sums added
+ *          left to right, ((G0 + G1) + G2) + G3, absent groups past the row's end counted as
+ *          +0.0f; then the run sums added left to right: ((R0 + R1) + R2) + ...
+ *          This is the order the GPU path declares for its reduction (for rows of at most 16
+ *          blocks it equals order 1); the oracle states it independently.
  * W is canonical GGUF blocks [rows][K/256][144 or 210]; the packed vectors are batch-major:
  * qs [batch][K], xd [batch][K/256], bsums [batch][K/256][8]; y is [batch][rows].          */
 #define MAX_NB 4096
@@ -291,7 +295,7 @@ void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd
                 acc = terms[0];
                 for (int64_t b = 1; b < nb; ++b)
                     acc = acc + terms[b];
-            } else {
+            } else if (order == 1) {
                 acc = 0.0f;
                 for (int64_t g = 0; g < (nb + 3) / 4; ++g) {
                     float t[4];
@@ -299,6 +303,20 @@ void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd
                         t[i] = (4 * g + i < nb) ? terms[4 * g + i] : 0.0f;
                     float G = (t[0] + t[1]) + (t[2] + t[3]);
                     acc = (g == 0) ? G : acc + G;
+                }
+            } else {
+                acc = 0.0f;
+                for (int64_t run = 0; run < (nb + 15) / 16; ++run) {
+                    float Rs = 0.0f;
+                    for (int64_t gi = 0; gi < 4; ++gi) {
+                        const int64_t g = 4 * run + gi;
+                        float t[4];
+                        for (int i = 0; i < 4; ++i)
+                            t[i] = (4 * g + i < nb) ? terms[4 * g + i] : 0.0f;
+                        float G = (t[0] + t[1]) + (t[2] + t[3]);
+                        Rs = (gi == 0) ? G : Rs + G;
+                    }
+                    acc = (run == 0) ? Rs : acc + Rs;
                 }
             }
             y[v * rows + r] = acc;

@@ -372,6 +372,34 @@ def test_orders_differ_only_in_rounding():
         assert acc == y1[0, r]
 
 
+def test_runs_of_sixteen_order_is_the_stated_tree():
+    """Order 2: groups of four blocks, runs of four groups left to right (absent groups +0),
+    runs left to right; identical to order 1 for rows of at most 16 blocks."""
+    W = synth.weights("q6k", 6, 8, 14336)
+    x = synth.activations(6, 1, 14336)
+    qs, xd, bs = O.q8k_pack(x)
+    y2 = O.qmatvec(O.FMT_Q6_K, W, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN)
+    for r in range(8):
+        t = O.block_terms(O.FMT_Q6_K, W[r], qs[0], xd[0], bs[0]).astype(np.float32)
+        t = np.concatenate([t, np.zeros(64 - len(t), np.float32)])  # 56 blocks, padded to 4 runs
+        G = [np.float32((t[4 * g] + t[4 * g + 1]) + (t[4 * g + 2] + t[4 * g + 3])) for g in range(16)]
+        runs = []
+        for run in range(4):
+            acc = G[4 * run]
+            for g in range(1, 4):
+                acc = np.float32(acc + G[4 * run + g])
+            runs.append(acc)
+        total = runs[0]
+        for R in runs[1:]:
+            total = np.float32(total + R)
+        assert total == y2[0, r]
+    W4 = synth.weights("q4k", 6, 8, 4096)
+    x4 = synth.activations(6, 1, 4096)
+    qs4, xd4, bs4 = O.q8k_pack(x4)
+    assert np.array_equal(O.qmatvec(O.FMT_Q4_K, W4, qs4, xd4, bs4, O.ORDER_GROUPS_OF_FOUR).view(np.uint32),
+                          O.qmatvec(O.FMT_Q4_K, W4, qs4, xd4, bs4, O.ORDER_RUNS_OF_SIXTEEN).view(np.uint32))
+
+
 def test_q6k_split_round_trip():
     g = synth.q6k_weights(2, 6, 1792)
     body, prefix = O.q6k_split(g, prefix_stride=8)
