@@ -45,7 +45,7 @@ NOMINAL_HBM_GBS = 8000.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 KERNEL_SOURCES = ["quantised_decode_mat_gb300/csrc/qmv.cuh", "quantised_decode_mat_gb300/csrc/qmv_q4k.cu",
                   "quantised_decode_mat_gb300/csrc/qmv_q6k.cu", "quantised_decode_mat_gb300/csrc/ptx.cuh",
-                  "quantised_decode_mat_gb300/csrc/pack.cu", "quantised_decode_mat_gb300/csrc/q8k.cuh"]
+                  "quantised_decode_mat_gb300/csrc/pack.cu", "quantised_decode_mat_gb300/csrc/q8k.cuh",]
 
 
 def kernel_source_hash() -> str:

@@ -223,9 +223,9 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
 /*
  * qmd_debug_qmatvec_dump -- qmd_qmatvec plus a record of its integer arithmetic, from the
  * same kernel code with extra stores.
- *   dots  int32 [batch][rows][nb][16]:
- *         Q4_K: entry 4c + 2h + u is the dot of the 16 elements (half h of the 32) of
- *               sub-block 2c + u; Q6_K_SPLIT: entry s is dot'_s of group s.
+ *   dots  int32 [batch][rows][nb][16], zeroed by the caller:
+ *         Q4_K: entry j < 8 is dot_j of sub-block j (entries 8..15 stay 0);
+ *         Q6_K_SPLIT: entry s is dot'_s of group s.
  *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K) M; M = 0 for Q6_K_SPLIT.
  * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm; this entry also
  * refuses K > 16384 (QMD_ERR_SHAPE).
@@ -244,10 +244,10 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream);
 /*
  * qmd_debug_set_plan -- override the mat-vec launch plan for launches made after the call:
  * row groups per CTA (each ceil(K/1024) warps; capped by the thread limit), rows per row group
- * per stage (1, 2, 4 or 8; reduced until rows x batch <= 8), a cap on pipeline stages, and
- * CTAs per multiprocessor (1..8); 0 keeps the default of each.  Results do not depend on the
- * plan; tests use this to drive the stage ring through many wrap-arounds on small inputs.
- * Process-wide.
+ * per stage (rounded down to 1, 2, 4 or 8, then halved until rows x batch <= 8), a cap on
+ * pipeline stages, and CTAs per multiprocessor (1..8); 0 keeps the default of each.
+ * Results do not depend on the plan; tests use this to drive the stage ring through many
+ * wrap-arounds on small inputs.  Process-wide.
  */
 void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int ctas_per_sm);
 

@@ -89,47 +89,20 @@ unsigned *device_error_word()
 // Rows per row group per stage (PR x B <= 8).
 static int default_rows_per_stage(bool q6, int batch)
 {
+    (void)q6;
     if (batch == 1)
         return 8;
     if (batch == 2)
-        return q6 ? 2 : 4;
+        return 4;
     if (batch <= 4)
         return 2;
     return 1;
 }
 
-qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
+// Ring depth and CTAs per SM for a stage geometry; false if nothing fits.
+static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_bytes, int per_stage_extra,
+                       int fixed, int cps, QmvPlan *pl)
 {
-    const bool q6 = fmt == QMD_Q6_K_SPLIT;
-    const bool fused = mode == QMV_PACK;
-    const int max_threads = qmv_max_threads(batch, mode);  // the kernels' launch bounds
-    const int WR = (nb + 3) / 4;                       // warps per row: 4 blocks per warp
-    if (WR * 32 > max_threads)
-        return QMD_ERR_SHAPE;
-    int PR = g_force_rows.load() > 0 ? g_force_rows.load() : default_rows_per_stage(q6, batch);
-    while (PR > 1 && PR * batch > 8)
-        PR >>= 1;
-    // Row groups per CTA: the fused form at batch 1 takes 2 (half as many CTAs, so half the
-    // reads of the f32 activations that every CTA packs for itself); otherwise 1.
-    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (fused && batch == 1 ? 2 : 1);
-    if (RG * WR * 32 > max_threads)
-        RG = max_threads / (WR * 32);
-    const int TR = RG * PR;
-    const int row_bytes = nb * (q6 ? 208 : 144);
-    const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
-    const int row_stride = row_bytes;  // rows of a stage are one contiguous copy
-    const int64_t sb64 = (int64_t)TR * row_stride + (int64_t)TR * pre_bytes;
-    if (sb64 > dev.smem_optin)
-        return QMD_ERR_SHAPE;
-    const int stage_bytes = align_up((int)sb64, 128);
-    const int per_stage = stage_bytes + RG * WR * 8 * 4 + 16;  // ring + partials + counter + barrier
-    // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
-    // matter more than stage depth); capped at launch by the occupancy calculator.
-    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1);
-    if (cps > 8)
-        cps = 8;
-    if (fused && batch == 1 && g_force_cps.load() <= 0 && cps > 2)
-        cps = 2;
     for (; cps >= 1; --cps) {
         int budget = dev.smem_per_sm / cps - 1024;
         if (budget > dev.smem_optin)
@@ -139,8 +112,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
             grid = rows;
         const int64_t rows_per_cta = (rows + grid - 1) / grid;
         const int64_t chunks = (rows_per_cta + TR - 1) / TR;
-        const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused).total + 64;
-        int64_t stages = (budget - fixed) / per_stage;
+        int64_t stages = (budget - fixed) / (stage_bytes + per_stage_extra);
         if (stages > 8)
             stages = 8;
         if (stages > chunks)
@@ -150,19 +122,61 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         if (stages < 1)
             continue;
         pl->grid = (int)grid;
-        pl->threads = RG * WR * 32;
         pl->stages = (int)stages;
-        pl->smem = qmv_smem_layout((int)stages, stage_bytes, RG, WR, batch, nb, q6, fused).total;
-        pl->WR = WR;
-        pl->RG = RG;
-        pl->PR = PR;
-        pl->row_bytes = row_bytes;
-        pl->pre_bytes = pre_bytes;
-        pl->stage_bytes = stage_bytes;
-        pl->row_stride = row_stride;
-        return QMD_OK;
+        return true;
     }
-    return QMD_ERR_SHAPE;
+    return false;
+}
+
+qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
+{
+    const bool q6 = fmt == QMD_Q6_K_SPLIT;
+    const bool fused = mode == QMV_PACK;
+    const int row_bytes = nb * (q6 ? 208 : 144);
+    const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
+    pl->row_bytes = row_bytes;
+    pl->pre_bytes = pre_bytes;
+    pl->row_stride = row_bytes;
+    // A warp covers 4 blocks of a row, 8 lanes per block; a row takes ceil(nb / 4) warps.
+    const int max_threads = qmv_max_threads(batch, mode);  // the kernels' launch bounds
+    const int WR = (nb + 3) / 4;
+    if (WR * 32 > max_threads)
+        return QMD_ERR_SHAPE;
+    int PR = g_force_rows.load() > 0 ? g_force_rows.load() : default_rows_per_stage(q6, batch);
+    while (PR & (PR - 1))  // the slice kernel is built for 1, 2, 4 or 8 rows
+        PR &= PR - 1;
+    while (PR > 1 && PR * batch > 8)
+        PR >>= 1;
+    // Row groups per CTA: the fused form at batch 1 takes 2 (half as many CTAs, so half the
+    // reads of the f32 activations that every CTA packs for itself); otherwise 1.
+    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (fused && batch == 1 ? 2 : 1);
+    if (RG * WR * 32 > max_threads)
+        RG = max_threads / (WR * 32);
+    if (RG < 1)
+        RG = 1;
+    const int TR = RG * PR;
+    const int64_t sb64 = (int64_t)TR * (row_bytes + pre_bytes);
+    if (sb64 > dev.smem_optin)
+        return QMD_ERR_SHAPE;
+    const int stage_bytes = align_up((int)sb64, 128);
+    const int extra = RG * WR * 8 * 4 + 16;  // partials + counter + barrier per stage
+    // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
+    // matter more than stage depth); capped at launch by the occupancy calculator.
+    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1);
+    if (cps > 8)
+        cps = 8;
+    if (fused && batch == 1 && g_force_cps.load() <= 0 && cps > 2)
+        cps = 2;
+    const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused).total + 64;
+    if (!fit_stages(dev, rows, TR, stage_bytes, extra, fixed, cps, pl))
+        return QMD_ERR_SHAPE;
+    pl->threads = RG * WR * 32;
+    pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused).total;
+    pl->WR = WR;
+    pl->RG = RG;
+    pl->PR = PR;
+    pl->stage_bytes = stage_bytes;
+    return QMD_OK;
 }
 
 // Test-only: one CTA waits on a barrier nothing completes, gives up after limit_ns, flags it.
@@ -401,8 +415,7 @@ void qmd_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
 void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int ctas_per_sm)
 {
     g_force_rg.store(row_groups > 0 && row_groups <= 32 ? row_groups : 0);
-    g_force_rows.store(rows_per_stage == 1 || rows_per_stage == 2 || rows_per_stage == 4 || rows_per_stage == 8
-                           ? rows_per_stage : 0);
+    g_force_rows.store(rows_per_stage >= 1 && rows_per_stage <= 8 ? rows_per_stage : 0);
     g_force_stages.store(max_stages > 0 ? max_stages : 0);
     g_force_cps.store(ctas_per_sm > 0 && ctas_per_sm <= 8 ? ctas_per_sm : 0);
 }

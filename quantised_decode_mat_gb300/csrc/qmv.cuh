@@ -373,10 +373,10 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
                     const int dl = dp4a_chain_lo(q, alo[v]);
                     const int dh16 = dp4a_chain_hi16(q, ahi[v]);
                     S[pr * B + v] = sc_lo * (dl << 4) + sc_hi * dh16;
-                    if (DUMP) {
+                    if (DUMP) {  // sub-blocks 2c, 2c+1: this lane holds half of each
                         int32_t *dd = p.dbg_dots + ((v * p.rows + rs + i) * nb + blk) * 16;
-                        dd[2 * k] = dl;
-                        dd[2 * k + 1] = dh16 >> 4;
+                        atomicAdd(dd + 2 * (k >> 1), dl);
+                        atomicAdd(dd + 2 * (k >> 1) + 1, dh16 >> 4);
                     }
                 }
             } else {
@@ -472,16 +472,22 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence_block();
-            // lane l finishes slot (l % 8) of row group l / 8, four row groups at a time
+            // lane l finishes slot (l % 8) of row group l / 8, four row groups at a time.  The
+            // warps' group sums (one group of four blocks each) are added in runs of four
+            // groups, ((G0 + G1) + G2) + G3 with absent groups as +0, then the runs left to right.
             for (int rgb = 0; rgb < RG; rgb += 4) {
                 const int frg = rgb + (lane >> 3), fk = lane & 7;
                 const int fslot = fk >> (3 - LP);
                 const int frow = frg * PR + (fslot < P ? fslot / B : PR);
                 if (frg < RG && (fk & (DUP - 1)) == 0 && fslot < P && frow < nr) {
                     const float *rr = red + (frg * WR) * 8 + fk;
-                    float acc = rr[0];
-                    for (int w = 1; w < WR; ++w)
-                        acc = __fadd_rn(acc, rr[w * 8]);
+                    float acc = 0.0f;
+                    for (int w0 = 0; w0 < WR; w0 += 4) {
+                        float run = rr[w0 * 8];
+                        for (int w = w0 + 1; w < w0 + 4; ++w)
+                            run = __fadd_rn(run, w < WR ? rr[w * 8] : 0.0f);
+                        acc = w0 == 0 ? run : __fadd_rn(acc, run);
+                    }
                     p.y[(fslot - (fslot / B) * B) * p.rows + rs + frow] = acc;
                 }
             }
@@ -495,10 +501,13 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
     }
 }
 
-template <bool Q6, int B, int PR, int MODE>
-qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
+// Launch one kernel instance with the plan's shape: opt in to its shared memory, cap the grid
+// at what is resident at once (a persistent grid; rows are split by gridDim), and launch it as
+// a programmatic dependent of the previous kernel in the stream.
+template <auto Kern>
+qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
-    auto kern = qmv_kernel<Q6, B, PR, MODE>;
+    auto kern = Kern;
     static int set_bytes[64] = {0};  // dynamic shared memory opted in, per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -546,6 +555,12 @@ qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
     return QMD_OK;
 }
 
+template <bool Q6, int B, int PR, int MODE>
+qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
+{
+    return launch_kernel<qmv_kernel<Q6, B, PR, MODE>>(kp, plan, s);
+}
+
 // Rows per stage and row group (PR x B <= 8); the plan picks one.
 template <bool Q6, int B, int MODE>
 qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
@@ -569,10 +584,9 @@ qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s
     return QMD_ERR_SHAPE;
 }
 
-template <bool Q6>
-qmd_status launch_qmv(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
+// Kernel parameters from the call's arguments and the plan; mode is the kernel variant.
+inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams &kp, int &mode)
 {
-    QmvKParams kp;
     kp.W = a.W;
     kp.Wpre = a.Wpre;
     kp.xqs = a.xqs;
@@ -598,13 +612,19 @@ qmd_status launch_qmv(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     kp.wait_ns = wait_limit_ns();
     if (kp.err == nullptr)
         return QMD_ERR_DEVICE;
-    const int mode = a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;
+    mode = a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;
+    return QMD_OK;
+}
+
+template <bool Q6>
+qmd_status launch_qmv_slice(const QmvKParams &kp, const QmvPlan &plan, int batch, int mode, cudaStream_t s)
+{
 #define QMD_CASE(BB)                                                                                 \
     case BB:                                                                                         \
         return mode == QMV_PACK   ? launch_rows<Q6, BB, QMV_PACK>(kp, plan, s)                       \
                : mode == QMV_DUMP ? launch_rows<Q6, BB, QMV_DUMP>(kp, plan, s)                       \
                                   : launch_rows<Q6, BB, QMV_PLAIN>(kp, plan, s);
-    switch (a.batch) {
+    switch (batch) {
         QMD_CASE(1)
         QMD_CASE(2)
         QMD_CASE(3)

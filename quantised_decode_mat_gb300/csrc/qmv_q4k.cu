@@ -5,7 +5,12 @@ namespace qmd {
 
 qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
 {
-    return launch_qmv<false>(a, plan, s);
+    QmvKParams kp;
+    int mode = QMV_PLAIN;
+    const qmd_status st = make_params(a, plan, kp, mode);
+    if (st != QMD_OK)
+        return st;
+    return launch_qmv_slice<false>(kp, plan, a.batch, mode, s);
 }
 
 }  // namespace qmd
