@@ -234,13 +234,14 @@ def run_reference(args):
 
 def workload_config(args):
     from quantised_decode_mat_gb300 import synth
-    return {"workload": f"decode_step_7b_q4k_q6k_32layers_b{args.batch}",
+    layers = getattr(args, "layers", synth.STEP_LAYERS)
+    return {"workload": f"decode_step_7b_q4k_q6k_{layers}layers_b{args.batch}",
             "launch": "pack+mat-vec as two kernels" if getattr(args, "unfused", False)
             else "pack fused into the mat-vec (one kernel per projection)",
-            "layers": synth.STEP_LAYERS,
+            "layers": layers,
             "projections": [f"{n}:{f}:{r}x{k}" for (n, f, r, k) in synth.STEP_PROJECTIONS],
             "batch": args.batch,
-            "l2": "inputs larger than L2 (4.41 GB of weights streamed per step; no flush needed)",
+            "l2": f"inputs larger than L2 ({layers * 0.1378:.2f} GB of weights streamed per step; no flush needed)",
             "parallelism": "replicas" if args.gpus > 1 else "single"}
 
 
@@ -273,7 +274,7 @@ def run_ours(args):
     from quantised_decode_mat_gb300 import step as qstep
     q.lib()  # fails loudly if the CUDA library is missing
 
-    step = qstep.make_step(args.batch, device=f"cuda:{local_rank}", fused=not args.unfused)
+    step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=not args.unfused)
     nbytes = step.bytes()
     stream = torch.cuda.current_stream()
 
@@ -381,6 +382,9 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=1, choices=range(1, 9))
     ap.add_argument("--unfused", action="store_true",
                     help="run each projection as qmd_q8k_pack + qmd_qmatvec (two launches)")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="decoder layers in the step (32 for the 7B-shaped step; fewer only for profiling "
+                         "captures, which must stay small)")
     ap.add_argument("--cpu-layers", type=int, default=8,
                     help="layers of the step the oracle is timed on for cpu_baseline (0: skip)")
     args = ap.parse_args(argv)
