@@ -68,10 +68,13 @@ def lib():
             L.oracle_qmatvec.argtypes = [i32, p, p, p, p, i64, i64, i32, i32, p]
             L.oracle_qmatvec_f64.argtypes = [i32, p, p, p, i64, i64, i32, p]
             L.oracle_q6k_split.argtypes = [p, i64, i64, p, p, i64]
+            L.oracle_rmsnorm.argtypes = [p, p, p, ctypes.c_float, i64, p, p]
+            L.oracle_rmsnorm_q8k_pack.argtypes = [p, p, p, ctypes.c_float, i64, p, p, p, p, p]
             for name in ("oracle_q4k_fields", "oracle_q4k_dequant", "oracle_q6k_fields",
                          "oracle_q6k_dequant", "oracle_q8k_pack", "oracle_q4k_subdots",
                          "oracle_q6k_subdots", "oracle_block_terms", "oracle_qmatvec",
-                         "oracle_qmatvec_f64", "oracle_q6k_split"):
+                         "oracle_qmatvec_f64", "oracle_q6k_split", "oracle_rmsnorm",
+                         "oracle_rmsnorm_q8k_pack"):
                 getattr(L, name).restype = None
             _lib = L
     return _lib
@@ -207,6 +210,31 @@ def q6k_split(gguf: np.ndarray, prefix_stride: int):
     prefix = np.zeros((rows, prefix_stride), np.uint16)
     lib().oracle_q6k_split(_ptr(g), rows, nb * QK, _ptr(body), _ptr(prefix), prefix_stride)
     return body, prefix
+
+
+# ---- RMSNorm (+ residual) before the pack ------------------------------------------------------
+def rmsnorm(x: np.ndarray, r: np.ndarray | None, g: np.ndarray, eps: float):
+    """x, r f32 [batch, K] (r may be None), g f32 [K] -> (h, n) f32 [batch, K]: h = x + r, n the
+    RMS-normalised h times g, in the declared order (oracle_rmsnorm)."""
+    x = _c(np.atleast_2d(x), np.float32)
+    batch, K = x.shape
+    assert K % QK == 0
+    r = None if r is None else _c(np.atleast_2d(r), np.float32).reshape(batch, K)
+    g = _c(g, np.float32).reshape(K)
+    h = np.zeros((batch, K), np.float32)
+    n = np.zeros((batch, K), np.float32)
+    L = lib()
+    for v in range(batch):
+        L.oracle_rmsnorm(x[v].ctypes.data, None if r is None else r[v].ctypes.data, _ptr(g), eps, K,
+                         h[v].ctypes.data, n[v].ctypes.data)
+    return h, n
+
+
+def rmsnorm_q8k_pack(x: np.ndarray, r: np.ndarray | None, g: np.ndarray, eps: float):
+    """-> (h f32 [batch, K], qs, d, bsums) as q8k_pack of the RMS-normalised x + r."""
+    h, n = rmsnorm(x, r, g, eps)
+    qs, d, bs = q8k_pack(n)
+    return h, qs, d, bs
 
 
 def rel_err(y: np.ndarray, ref: np.ndarray, floor_frac: float = 1e-3) -> np.ndarray:

@@ -35,6 +35,9 @@
  *   - row sum over blocks in f32, in one of two declared orders (see oracle_qmatvec).
  * Non-finite activations are outside the contract.
  *
+ * RMSNorm with a residual add before the pack (oracle_rmsnorm): see its comment for the
+ * reading of the formula and the declared order of the sum of squares.
+ *
  * Parity pins (tests/test_oracle_pins.py): f16 decode against numpy's float16 over all 65536
  * bit patterns; Q4_K/Q6_K code maps are bijections onto the block's bits; q8_K invariants;
  * brute force in f64; closed-form special cases (unit scales, zero nibbles, q == 32).
@@ -364,4 +367,54 @@ void oracle_q6k_split(const uint8_t *gguf, int64_t rows, int64_t K, uint8_t *bod
             prefix[r * prefix_stride + b] = le16(src + 208);
         }
     }
+}
+
+/* ---- RMSNorm with an optional residual add, the step before the q8_K pack. -----------------
+ * "Language models on the device: the cajeta-llm kernels", §2.6 lists the normalisation and
+ * residual kernels (rmsnorm*, add*) beside the device q8_K quantiser; in a decode step they
+ * produce the activation that the quantiser packs.  The pages print no formula.  The reading
+ * taken here is the usual root-mean-square norm with a learned per-element gain g:
+ *     h_i = x_i + r_i               (r absent: h = x; h is the new residual stream)
+ *     ms  = (sum_i h_i * h_i) / K
+ *     n_i = (h_i * (1 / sqrt(ms + eps))) * g_i
+ * every f32 operation rounded on its own; sqrt and the two divisions are IEEE-correctly
+ * rounded.  The packed codes depend on the bits of n, so the order of the sum of squares is
+ * declared (the GPU path declares the same one):
+ *     lane t in [0, 256) adds the squares h_{t+256j}^2 for j = 0, 1, 2, ... left to right;
+ *     each group of 32 lanes (32w .. 32w+31) is added as a pairwise tree, v[l] = v[l] + v[l+s]
+ *     for s = 16, 8, 4, 2, 1 and l < s, leaving the group total in v[0];
+ *     the eight group totals are added left to right.
+ * x, r, h, n: f32 [K]; g: f32 [K]; K % 256 == 0.                                             */
+void oracle_rmsnorm(const float *x, const float *r, const float *g, float eps, int64_t K, float *h, float *n)
+{
+    float lane[256];
+    for (int t = 0; t < 256; ++t)
+        lane[t] = 0.0f;
+    for (int64_t i = 0; i < K; ++i) {
+        h[i] = r ? x[i] + r[i] : x[i];
+        const float sq = h[i] * h[i];
+        lane[i % 256] = lane[i % 256] + sq;
+    }
+    float total = 0.0f;
+    for (int w = 0; w < 8; ++w) {
+        float *v = lane + 32 * w;
+        for (int s = 16; s >= 1; s /= 2)
+            for (int l = 0; l < s; ++l)
+                v[l] = v[l] + v[l + s];
+        total = (w == 0) ? v[0] : total + v[0];
+    }
+    const float ms = total / (float)K;
+    const float inv = 1.0f / sqrtf(ms + eps);
+    for (int64_t i = 0; i < K; ++i) {
+        const float hn = h[i] * inv;
+        n[i] = hn * g[i];
+    }
+}
+
+/* RMSNorm (above) of one vector, then its q8_K pack (oracle_q8k_pack). */
+void oracle_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, int64_t K, float *h,
+                             float *n, int8_t *qs, float *d, int16_t *bsums)
+{
+    oracle_rmsnorm(x, r, g, eps, K, h, n);
+    oracle_q8k_pack(n, K, qs, d, bsums);
 }

@@ -30,7 +30,7 @@ Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
 
 # tensor ids used in stream keys
-T_Q4K, T_Q6K, T_ACT = 1, 2, 3
+T_Q4K, T_Q6K, T_ACT, T_RES, T_GAIN = 1, 2, 3, 4, 5
 # sub-streams inside a tensor
 _S_D, _S_DMIN, _S_SCALES, _S_QS, _S_QL, _S_QH, _S_U1, _S_U2 = range(8)
 
@@ -121,6 +121,22 @@ def activations(seed: int, batch: int, K: int, layer: int = 0, tensor: int = 0) 
     u2 = uniform01(stream_key(*base, _S_U2), n)
     x = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
     return x.astype(np.float32).reshape(batch, K)
+
+
+def residual(seed: int, batch: int, K: int, layer: int = 0, tensor: int = 0) -> np.ndarray:
+    """f32 [batch, K] ~ N(0, 1): the residual stream added before an RMSNorm."""
+    n = batch * K
+    base = (seed, T_RES, layer, tensor)
+    u1 = uniform01(stream_key(*base, _S_U1), n)
+    u2 = uniform01(stream_key(*base, _S_U2), n)
+    x = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    return x.astype(np.float32).reshape(batch, K)
+
+
+def norm_gain(seed: int, K: int, layer: int = 0, tensor: int = 0) -> np.ndarray:
+    """f32 [K] ~ U[0.5, 1.5]: an RMSNorm's per-element gain."""
+    u = uniform01(stream_key(seed, T_GAIN, layer, tensor, _S_D), K)
+    return (0.5 + u).astype(np.float32)
 
 
 # ---------------------------------------------------------------------------------------------

@@ -423,3 +423,117 @@ def test_golden_regression():
     assert set(now) == set(stored)
     for k in now:
         assert now[k] == stored[k], k
+
+
+# ---- RMSNorm (+ residual) before the pack --------------------------------------------------------
+def test_rmsnorm_power_of_two_scaling_is_exact():
+    """With eps = 0, scaling h by 2^k scales every square by 4^k exactly, so the norm's output
+    is bit-identical; scaling g by 2 doubles n exactly."""
+    x = synth.activations(21, 2, 1024)
+    g = synth.norm_gain(21, 1024)
+    _, n = O.rmsnorm(x, None, g, 0.0)
+    for k in (-3, 1, 5):
+        _, nk = O.rmsnorm(x * np.float32(2.0 ** k), None, g, 0.0)
+        assert np.array_equal(nk.view(np.uint32), n.view(np.uint32))
+    _, n2 = O.rmsnorm(x, None, g * np.float32(2.0), 0.0)
+    assert np.array_equal(n2, n * np.float32(2.0))
+
+
+def test_rmsnorm_constant_vector_closed_form():
+    """h = a everywhere: every partial sum is exact, ms = a^2, n = a / sqrt(a^2 + eps) * g."""
+    K = 768
+    for a, eps in ((0.75, 0.0), (-1.5, 0.25), (3.0, 1e-5)):
+        x = np.full((1, K), a, np.float32)
+        g = np.linspace(0.5, 1.5, K).astype(np.float32)
+        h, n = O.rmsnorm(x, None, g, eps)
+        assert np.array_equal(h, x)
+        inv = np.float32(1.0) / np.sqrt(np.float32(a * a) + np.float32(eps), dtype=np.float32)
+        want = (np.float32(a) * inv) * g
+        assert np.array_equal(n[0].view(np.uint32), want.view(np.uint32))
+
+
+def test_rmsnorm_residual_is_the_f32_sum():
+    x = synth.activations(22, 3, 512)
+    r = synth.residual(22, 3, 512)
+    g = synth.norm_gain(22, 512)
+    h, n = O.rmsnorm(x, r, g, 1e-6)
+    assert np.array_equal(h, x + r)
+    h0, n0 = O.rmsnorm(x + r, None, g, 1e-6)
+    assert np.array_equal(h0, h) and np.array_equal(n0.view(np.uint32), n.view(np.uint32))
+
+
+def test_rmsnorm_matches_f64_within_the_rounding_bound():
+    """f32 against the same formula in f64 from the same h: the sum of K squares in any order
+    is within K*u relative, the rest adds a few u, so 1e-5 relative bounds K <= 16384."""
+    for K, eps in ((256, 1e-6), (4096, 1e-5), (14336, 1e-6)):
+        x = synth.activations(23, 2, K)
+        r = synth.residual(23, 2, K)
+        g = synth.norm_gain(23, K)
+        h, n = O.rmsnorm(x, r, g, eps)
+        h64 = h.astype(np.float64)
+        n64 = h64 / np.sqrt(np.mean(h64 * h64, axis=1, keepdims=True) + eps) * g.astype(np.float64)
+        assert np.max(np.abs(n - n64) / np.abs(n64)) < 1e-5
+
+
+def test_rmsnorm_sum_of_squares_is_the_declared_tree():
+    """The declared order: 256 lane sums (left to right over the lane's elements), a pairwise
+    tree inside each group of 32 lanes, the eight group sums left to right.  Values spread over
+    many orders of magnitude make other orders round differently."""
+    K = 1024
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((1, K)) * np.exp2(rng.integers(-12, 12, size=(1, K)))).astype(np.float32)
+    g = np.ones(K, np.float32)
+    _, n = O.rmsnorm(x, None, g, 0.0)
+    sq = (x[0] * x[0]).astype(np.float32)
+    lane = np.zeros(256, np.float32)
+    for i in range(K):
+        lane[i % 256] = np.float32(lane[i % 256] + sq[i])
+    total = None
+    for w in range(8):
+        v = lane[32 * w: 32 * w + 32].copy()
+        s = 16
+        while s >= 1:
+            v[:s] = (v[:s] + v[s: 2 * s]).astype(np.float32)
+            s //= 2
+        total = v[0] if total is None else np.float32(total + v[0])
+    ms = np.float32(total / np.float32(K))
+    inv = np.float32(np.float32(1.0) / np.sqrt(ms, dtype=np.float32))
+    want = (x[0] * inv).astype(np.float32) * g
+    assert np.array_equal(n[0].view(np.uint32), want.view(np.uint32))
+    # a sequential sum of the same squares gives other bits for some elements
+    seq = np.float32(0.0)
+    for v in sq:
+        seq = np.float32(seq + v)
+    assert seq != total
+
+
+def test_rmsnorm_pack_is_pack_of_the_norm():
+    x = synth.activations(24, 2, 2048)
+    r = synth.residual(24, 2, 2048)
+    g = synth.norm_gain(24, 2048)
+    h, qs, d, bs = O.rmsnorm_q8k_pack(x, r, g, 1e-5)
+    _, n = O.rmsnorm(x, r, g, 1e-5)
+    qs2, d2, bs2 = O.q8k_pack(n)
+    assert np.array_equal(qs, qs2) and np.array_equal(d.view(np.uint32), d2.view(np.uint32)) and np.array_equal(bs, bs2)
+    # zero gain: a zero vector, packed as zeros with d = 0
+    _, qz, dz, bz = O.rmsnorm_q8k_pack(x, r, np.zeros(2048, np.float32), 1e-5)
+    assert not qz.any() and not dz.any() and not bz.any()
+
+
+def test_rmsnorm_sum_order_by_absorption():
+    """One square of 2^24 among squares of 1: adding a 1 to 2^24 rounds back to 2^24 (ties to
+    even), so the total counts exactly the 1s that were summed before meeting the large value.
+    Declared order, K = 1024: lane 0 holds 2^24 and absorbs its own three 1s; the other 255
+    lanes hold 4 each and are added exactly, so the total is 2^24 + 1020.  A sequential sum
+    gives 2^24, and lanes of stride 128 give 2^24 + 1016."""
+    K = 1024
+    x = np.ones((1, K), np.float32)
+    x[0, 0] = np.float32(4096.0)
+    g = np.ones(K, np.float32)
+    _, n = O.rmsnorm(x, None, g, 0.0)
+    total = np.float32(2.0 ** 24 + 1020)
+    inv = np.float32(np.float32(1.0) / np.sqrt(np.float32(total / np.float32(K)), dtype=np.float32))
+    assert np.array_equal(n[0].view(np.uint32), (x[0] * inv).view(np.uint32))
+    for other in (2.0 ** 24, 2.0 ** 24 + 1016):
+        inv_o = np.float32(np.float32(1.0) / np.sqrt(np.float32(np.float32(other) / np.float32(K)), dtype=np.float32))
+        assert inv_o != inv
