@@ -55,7 +55,8 @@ typedef enum qmd_status {
     QMD_ERR_SHAPE = 6,                 /* rows < 1, K < 256, K above the call's limit, or a size overflow */
     QMD_ERR_LAUNCH = 7,                /* the CUDA runtime refused the launch (see qmd_last_error_detail) */
     QMD_ERR_DEVICE_TIMEOUT = 8,        /* a bounded wait inside a kernel gave up (qmd_get_device_error) */
-    QMD_ERR_DEVICE = 9                 /* no usable CUDA device, or it is not an sm_103 part */
+    QMD_ERR_DEVICE = 9,                /* no usable CUDA device, or it is not an sm_103 part */
+    QMD_ERR_VALUE = 10                 /* a scalar argument is out of its range (e.g. eps < 0 or not finite) */
 } qmd_status;
 
 /* Weight formats, named by their GGUF type ids. */
@@ -100,6 +101,32 @@ typedef struct qmd_q8k_const {
 qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *stream);
 
 /*
+ * qmd_rmsnorm_q8k_pack -- RMSNorm with an optional residual add, then the q8_K pack, in one
+ * launch ("Language models on the device: the cajeta-llm kernels", §2.6: the normalisation and
+ * residual kernels that produce the activation the device q8_K quantiser of §1 packs):
+ *     h = x + r                     (r NULL: h = x)
+ *     n = (h * (1 / sqrt(sum(h * h) / K + eps))) * g
+ *     xq = qmd_q8k_pack(n)
+ * per vector, each f32 operation rounded on its own (sqrt and the divisions correctly
+ * rounded).  The sum of squares is taken in this order, so that results are reproducible
+ * bit for bit: partial sum t (t < 256) adds the squares of elements t, t + 256, t + 512, ...
+ * left to right; each group of 32 partials (32w .. 32w+31) is added as a pairwise tree,
+ * p[l] += p[l + s] for s = 16, 8, 4, 2, 1 and l < s; the eight group totals left to right.
+ *
+ *   x      f32 [batch][K], 16-byte aligned                               (read)
+ *   r      f32 [batch][K] residual stream, 16-byte aligned, or NULL        (read)
+ *   g      f32 [K] gain, shared by every vector, 16-byte aligned           (read)
+ *   eps    added to the mean square; finite and >= 0
+ *   h_out  f32 [batch][K], 16-byte aligned, receives h; or NULL.  It may be the same buffer
+ *          as x or r (an in-place residual update); it must not overlap g or xq.
+ *   xq     as qmd_q8k_pack (written)
+ * Errors: NULL (x, g or xq), K_NOT_MULTIPLE_OF_256, SHAPE (K < 256 or batch*K overflows),
+ * BATCH, MISALIGNED, VALUE (eps), DEVICE, LAUNCH.
+ */
+qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, float *h_out,
+                                qmd_q8k xq, int64_t K, int batch, void *stream);
+
+/*
  * qmd_qmatvec -- y[v][r] = sum over the row's blocks of the rank-one epilogue of integer
  * sub-block dots, for v < batch, r < rows
  * ("Language models on the device: the cajeta-llm kernels", §1, §2.1 one row finished by a
@@ -112,8 +139,9 @@ qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *
  *   Q6_K_SPLIT:  S = sum_s sc_s * dot'_s, dot'_s over 16 values of (q - 32) * q8   (s = 0..15)
  *                term = d_x * ( f32(d) * (float)S )
  * and the row's terms are summed in f32 in this order: blocks in groups of four, each group
- * (t0 + t1) + (t2 + t3) with absent blocks past the row's end counted as +0, then the group
- * sums left to right.  y is overwritten, not accumulated.
+ * (t0 + t1) + (t2 + t3) with absent blocks past the row's end counted as +0; groups in runs
+ * of four (16 blocks), each run ((G0 + G1) + G2) + G3 with absent groups counted as +0; then
+ * the run sums left to right.  y is overwritten, not accumulated.
  *
  *   fmt    QMD_Q4_K or QMD_Q6_K_SPLIT
  *   W      Q4_K: GGUF blocks u8 [rows][nb][144] (16-byte aligned; read in place as u32 words)

@@ -30,6 +30,7 @@ STATUS = {
     7: "QMD_ERR_LAUNCH",
     8: "QMD_ERR_DEVICE_TIMEOUT",
     9: "QMD_ERR_DEVICE",
+    10: "QMD_ERR_VALUE",
 }
 
 
@@ -61,6 +62,7 @@ def lib() -> ctypes.CDLL:
         sizep = ctypes.POINTER(ctypes.c_size_t)
         sigs = {
             "qmd_q8k_pack": ([vp, Q8KPtrs, i64, i32, vp], i32),
+            "qmd_rmsnorm_q8k_pack": ([vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, i64, i32, vp], i32),
             "qmd_qmatvec": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_qmatvec_x": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_q6k_prefix_stride": ([i64], i64),
@@ -137,6 +139,17 @@ def q8k_pack(x, out: Q8K | None = None, stream=None) -> Q8K:
     if out is None:
         out = Q8K.empty(batch, K, x.device)
     _check(lib().qmd_q8k_pack(_ptr(x), out.ptrs(), K, batch, _stream(stream)))
+    return out
+
+
+def rmsnorm_q8k_pack(x, r, g, eps: float, h_out=None, out: Q8K | None = None, stream=None) -> Q8K:
+    """qmd_rmsnorm_q8k_pack: h = x + r (r may be None), n = RMSNorm(h) * g, packed to q8_K.
+    x, r, h_out f32 [batch, K]; g f32 [K].  h_out (optional, may be x or r) receives h."""
+    batch, K = x.shape
+    if out is None:
+        out = Q8K.empty(batch, K, x.device)
+    _check(lib().qmd_rmsnorm_q8k_pack(_ptr(x), _ptr(r), _ptr(g), float(eps), _ptr(h_out), out.ptrs(), K, batch,
+                                      _stream(stream)))
     return out
 
 

@@ -291,6 +291,28 @@ qmd_status qmd_q8k_pack(const float *x, qmd_q8k xq, int64_t K, int batch, void *
                            static_cast<cudaStream_t>(stream));
 }
 
+qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, float *h_out,
+                                qmd_q8k xq, int64_t K, int batch, void *stream)
+{
+    if (!x || !g || !xq.qs || !xq.d || !xq.bsums)
+        return QMD_ERR_NULL;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return QMD_ERR_BATCH;
+    if (!aligned(x, 16) || (r && !aligned(r, 16)) || !aligned(g, 16) || (h_out && !aligned(h_out, 16)) ||
+        !aligned(xq.qs, 16) || !aligned(xq.bsums, 16) || !aligned(xq.d, 4))
+        return QMD_ERR_MISALIGNED;
+    if (!(eps >= 0.0f) || !(eps <= 3.4028234663852886e38f))  // rejects NaN, negatives and +inf
+        return QMD_ERR_VALUE;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return st;
+    return launch_rmsnorm_q8k_pack(x, r, g, eps, h_out, xq.qs, xq.d, xq.bsums, K, batch,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                        int64_t rows, int64_t K, int batch, void *stream)
 {
@@ -383,6 +405,7 @@ const char *qmd_status_str(qmd_status s)
     case QMD_ERR_LAUNCH: return "QMD_ERR_LAUNCH";
     case QMD_ERR_DEVICE_TIMEOUT: return "QMD_ERR_DEVICE_TIMEOUT";
     case QMD_ERR_DEVICE: return "QMD_ERR_DEVICE";
+    case QMD_ERR_VALUE: return "QMD_ERR_VALUE";
     }
     return "QMD_ERR_UNKNOWN";
 }

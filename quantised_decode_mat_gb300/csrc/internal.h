@@ -73,6 +73,8 @@ qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
 qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 
 // ---- pack, bind, debug ---------------------------------------------------------------------
+qmd_status launch_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, float *h_out,
+                                   int8_t *qs, float *d, int16_t *bsums, int64_t K, int batch, cudaStream_t s);
 qmd_status launch_q8k_pack(const float *x, int8_t *qs, float *d, int16_t *bsums, int64_t nblocks,
                            cudaStream_t s);
 qmd_status launch_q6k_split(const uint8_t *gguf, uint8_t *body, uint16_t *prefix, int64_t rows,
