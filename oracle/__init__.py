@@ -5,7 +5,7 @@ CPU-baseline leg may import this package.  It shares no code with the CUDA path 
 imports it; the library's product path never imports this package.
 
 Arrays are numpy; weights are canonical GGUF blocks (uint8 [rows, K/256, 144 or 210]).
-Formats are named by their GGUF type ids: 12 = Q4_K, 14 = Q6_K.
+Formats are named by their GGUF type ids: 12 = Q4_K, 13 = Q5_K, 14 = Q6_K.
 """
 from __future__ import annotations
 
@@ -22,9 +22,10 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "liboracle.so")
 
 FMT_Q4_K = 12
+FMT_Q5_K = 13
 FMT_Q6_K = 14
 QK = 256
-BLOCK_BYTES = {FMT_Q4_K: 144, FMT_Q6_K: 210}
+BLOCK_BYTES = {FMT_Q4_K: 144, FMT_Q5_K: 176, FMT_Q6_K: 210}
 ORDER_SEQUENTIAL = 0
 ORDER_GROUPS_OF_FOUR = 1
 ORDER_RUNS_OF_SIXTEEN = 2
@@ -60,6 +61,9 @@ def lib():
             L.oracle_q4k_fields.argtypes = [p, p, p, p, p, p]
             L.oracle_q4k_dequant.argtypes = [p, p]
             L.oracle_q6k_fields.argtypes = [p, p, p, p]
+            L.oracle_q5k_fields.argtypes = [p, p, p, p, p, p]
+            L.oracle_q5k_dequant.argtypes = [p, p]
+            L.oracle_q5k_subdots.argtypes = [p, p, i64, p]
             L.oracle_q6k_dequant.argtypes = [p, p]
             L.oracle_q8k_pack.argtypes = [p, i64, p, p, p]
             L.oracle_q4k_subdots.argtypes = [p, p, i64, p]
@@ -73,6 +77,7 @@ def lib():
             for name in ("oracle_q4k_fields", "oracle_q4k_dequant", "oracle_q6k_fields",
                          "oracle_q6k_dequant", "oracle_q8k_pack", "oracle_q4k_subdots",
                          "oracle_q6k_subdots", "oracle_block_terms", "oracle_qmatvec",
+                         "oracle_q5k_fields", "oracle_q5k_dequant", "oracle_q5k_subdots",
                          "oracle_qmatvec_f64", "oracle_q6k_split", "oracle_rmsnorm",
                          "oracle_rmsnorm_q8k_pack"):
                 getattr(L, name).restype = None
@@ -107,6 +112,19 @@ def q4k_fields(block: np.ndarray):
     return float(d[0]), float(dm[0]), sc, m, q
 
 
+def q5k_fields(block: np.ndarray):
+    """-> (d, dmin, sc[8], m[8], q[256] in 0..31) of one 176-byte block."""
+    b = _c(block, np.uint8)
+    assert b.size == 176
+    d = np.zeros(1, np.float32)
+    dm = np.zeros(1, np.float32)
+    sc = np.zeros(8, np.int32)
+    m = np.zeros(8, np.int32)
+    q = np.zeros(256, np.int32)
+    lib().oracle_q5k_fields(_ptr(b), _ptr(d), _ptr(dm), _ptr(sc), _ptr(m), _ptr(q))
+    return float(d[0]), float(dm[0]), sc, m, q
+
+
 def q6k_fields(block: np.ndarray):
     """-> (d, sc[16] (signed), q[256] in 0..63) of one 210-byte block."""
     b = _c(block, np.uint8)
@@ -124,6 +142,8 @@ def dequant(fmt: int, block: np.ndarray) -> np.ndarray:
     w = np.zeros(256, np.float64)
     if fmt == FMT_Q4_K:
         lib().oracle_q4k_dequant(_ptr(b), _ptr(w))
+    elif fmt == FMT_Q5_K:
+        lib().oracle_q5k_dequant(_ptr(b), _ptr(w))
     else:
         lib().oracle_q6k_dequant(_ptr(b), _ptr(w))
     return w
@@ -147,15 +167,17 @@ def q8k_pack(x: np.ndarray):
 
 # ---- integer dots, block terms and the mat-vec -------------------------------------------------
 def subdots(fmt: int, row: np.ndarray, qs: np.ndarray) -> np.ndarray:
-    """One row's int32 sub-block dots against one packed vector: [nb, 8] (Q4_K) or [nb, 16] (Q6_K)."""
+    """One row's int32 sub-block dots against one packed vector: [nb, 8] (Q4_K, Q5_K) or [nb, 16] (Q6_K)."""
     row = _c(row, np.uint8)
     qs = _c(qs, np.int8).reshape(-1)
     K = qs.size
     nb = K // QK
-    per = 8 if fmt == FMT_Q4_K else 16
+    per = 16 if fmt == FMT_Q6_K else 8
     out = np.zeros((nb, per), np.int32)
     if fmt == FMT_Q4_K:
         lib().oracle_q4k_subdots(_ptr(row), _ptr(qs), K, _ptr(out))
+    elif fmt == FMT_Q5_K:
+        lib().oracle_q5k_subdots(_ptr(row), _ptr(qs), K, _ptr(out))
     else:
         lib().oracle_q6k_subdots(_ptr(row), _ptr(qs), K, _ptr(out))
     return out

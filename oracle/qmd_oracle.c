@@ -22,14 +22,17 @@
  *   "Why a kernel declines": a K-quant tensor whose last dimension is not a multiple of 256
  *   is rejected.
  *
- * The pages do not print the bit layout of a Q4_K or Q6_K block, the q8_K rounding rule, or
- * the epilogue's order of operations.  The readings taken here:
+ * The same page, §2.3: a Q5_K kernel differs from the Q4_K one only in how it stages the
+ * codes: the fifth-bit plane is OR-ed into bit four of each 4-bit code.
+ *
+ * The pages do not print the bit layout of a Q4_K, Q5_K or Q6_K block, the q8_K rounding
+ * rule, or the epilogue's order of operations.  The readings taken here:
  *   - block layouts: the public GGUF format definition (byte offsets in the decoders below);
  *   - q8_K: symmetric absmax scale, d = amax/127, codes round(x * 127/amax) to nearest-even
  *     in f32, clamped to [-127, 127]; an all-zero block has d = 0 and zero codes; the eight
  *     sums are over 32-value sub-blocks (the pages say eight);
  *   - epilogue per 256-value block, each f32 operation rounded separately:
- *       Q4_K: term = dx * ( f32(d) * (float)S  -  f32(dmin) * (float)M ),
+ *       Q4_K, Q5_K: term = dx * ( f32(d) * (float)S  -  f32(dmin) * (float)M ),
  *             S = sum_j sc_j * dot_j,  M = sum_j m_j * bsum_j   (exact int32, j = 0..7)
  *       Q6_K: term = dx * ( f32(d) * (float)S ),  S = sum_s sc_s * dot_s   (s = 0..15)
  *   - row sum over blocks in f32, in one of two declared orders (see oracle_qmatvec).
@@ -50,8 +53,10 @@
 
 #define QK 256
 #define Q4K_BYTES 144
+#define Q5K_BYTES 176
 #define Q6K_BYTES 210
 #define FMT_Q4_K 12 /* GGUF type id */
+#define FMT_Q5_K 13 /* GGUF type id */
 #define FMT_Q6_K 14 /* GGUF type id */
 
 /* ---- IEEE 754 binary16 -> value, from the format's definition (exact). ----------------- */
@@ -116,6 +121,46 @@ void oracle_q4k_dequant(const uint8_t *blk, double *w)
     float d, dmin;
     int32_t sc[8], m[8], q[QK];
     oracle_q4k_fields(blk, &d, &dmin, sc, m, q);
+    for (int e = 0; e < QK; ++e) {
+        int j = e / 32;
+        w[e] = (double)d * sc[j] * q[e] - (double)dmin * m[j];
+    }
+}
+
+/* ---- Q5_K block (176 bytes): [0,2) d f16, [2,4) dmin f16, [4,16) the twelve scale/min
+ *      bytes packed as in Q4_K, [16,48) qh: the fifth bits, [48,176) 128 bytes of low 4-bit
+ *      codes laid out as in Q4_K.  Element e = 64c + t (c = 0..3): the low four bits are
+ *      q4k_code's; the fifth bit is bit 2c of qh[t] for t < 32 and bit 2c+1 of qh[t - 32]
+ *      for t >= 32, so a code is in 0..31.  Sub-block j = e / 32 as in Q4_K. ------------ */
+static int q5k_code(const uint8_t *blk, int e)
+{
+    const int c = e / 64, t = e % 64;
+    const uint8_t *qh = blk + 16;
+    const int high = t < 32 ? (qh[t] >> (2 * c)) & 1 : (qh[t - 32] >> (2 * c + 1)) & 1;
+    return q4k_code(blk + 48, e) | (high << 4);
+}
+
+void oracle_q5k_fields(const uint8_t *blk, float *d, float *dmin, int32_t *sc, int32_t *m,
+                       int32_t *q)
+{
+    *d = oracle_f16_to_f32(le16(blk));
+    *dmin = oracle_f16_to_f32(le16(blk + 2));
+    for (int j = 0; j < 8; ++j) {
+        int a, b;
+        q4k_scale_min(blk + 4, j, &a, &b);
+        sc[j] = a;
+        m[j] = b;
+    }
+    for (int e = 0; e < QK; ++e)
+        q[e] = q5k_code(blk, e);
+}
+
+/* weight value w_e = d * sc_j * q_e - dmin * m_j, evaluated exactly in f64 */
+void oracle_q5k_dequant(const uint8_t *blk, double *w)
+{
+    float d, dmin;
+    int32_t sc[8], m[8], q[QK];
+    oracle_q5k_fields(blk, &d, &dmin, sc, m, q);
     for (int e = 0; e < QK; ++e) {
         int j = e / 32;
         w[e] = (double)d * sc[j] * q[e] - (double)dmin * m[j];
@@ -214,6 +259,21 @@ void oracle_q4k_subdots(const uint8_t *row, const int8_t *qs, int64_t K, int32_t
     }
 }
 
+void oracle_q5k_subdots(const uint8_t *row, const int8_t *qs, int64_t K, int32_t *dots)
+{
+    for (int64_t b = 0; b < K / QK; ++b) {
+        float d, dmin;
+        int32_t sc[8], m[8], q[QK];
+        oracle_q5k_fields(row + b * Q5K_BYTES, &d, &dmin, sc, m, q);
+        for (int j = 0; j < 8; ++j) {
+            int32_t s = 0;
+            for (int i = 0; i < 32; ++i)
+                s += q[32 * j + i] * qs[b * QK + 32 * j + i];
+            dots[b * 8 + j] = s;
+        }
+    }
+}
+
 void oracle_q6k_subdots(const uint8_t *row, const int8_t *qs, int64_t K, int32_t *dots)
 {
     for (int64_t b = 0; b < K / QK; ++b) {
@@ -235,12 +295,18 @@ void oracle_block_terms(int fmt, const uint8_t *row, const int8_t *qs, const flo
 {
     int64_t nb = K / QK;
     for (int64_t b = 0; b < nb; ++b) {
-        if (fmt == FMT_Q4_K) {
-            const uint8_t *blk = row + b * Q4K_BYTES;
+        if (fmt == FMT_Q4_K || fmt == FMT_Q5_K) {
             float d, dmin;
             int32_t sc[8], m[8], q[QK], dots[8];
-            oracle_q4k_fields(blk, &d, &dmin, sc, m, q);
-            oracle_q4k_subdots(blk, qs + b * QK, QK, dots);
+            if (fmt == FMT_Q4_K) {
+                const uint8_t *blk = row + b * Q4K_BYTES;
+                oracle_q4k_fields(blk, &d, &dmin, sc, m, q);
+                oracle_q4k_subdots(blk, qs + b * QK, QK, dots);
+            } else {
+                const uint8_t *blk = row + b * Q5K_BYTES;
+                oracle_q5k_fields(blk, &d, &dmin, sc, m, q);
+                oracle_q5k_subdots(blk, qs + b * QK, QK, dots);
+            }
             int32_t S = 0, M = 0;
             for (int j = 0; j < 8; ++j) {
                 S += sc[j] * dots[j];
@@ -277,7 +343,7 @@ void oracle_block_terms(int fmt, const uint8_t *row, const int8_t *qs, const flo
  *          +0.0f; then the run sums added left to right: ((R0 + R1) + R2) + ...
  *          This is the order the GPU path declares for its reduction (for rows of at most 16
  *          blocks it equals order 1); the oracle states it independently.
- * W is canonical GGUF blocks [rows][K/256][144 or 210]; the packed vectors are batch-major:
+ * W is canonical GGUF blocks [rows][K/256][144, 176 or 210]; the packed vectors are batch-major:
  * qs [batch][K], xd [batch][K/256], bsums [batch][K/256][8]; y is [batch][rows].          */
 #define MAX_NB 4096
 void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd,
@@ -285,7 +351,7 @@ void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd
                     float *y)
 {
     int64_t nb = K / QK;
-    int64_t bb = fmt == FMT_Q4_K ? Q4K_BYTES : Q6K_BYTES;
+    int64_t bb = fmt == FMT_Q4_K ? Q4K_BYTES : fmt == FMT_Q5_K ? Q5K_BYTES : Q6K_BYTES;
     float terms[MAX_NB];
     if (nb > MAX_NB)
         return;
@@ -332,7 +398,7 @@ void oracle_qmatvec_f64(int fmt, const uint8_t *W, const int8_t *qs, const float
                         int64_t rows, int64_t K, int batch, double *y)
 {
     int64_t nb = K / QK;
-    int64_t bb = fmt == FMT_Q4_K ? Q4K_BYTES : Q6K_BYTES;
+    int64_t bb = fmt == FMT_Q4_K ? Q4K_BYTES : fmt == FMT_Q5_K ? Q5K_BYTES : Q6K_BYTES;
     double w[QK];
     for (int v = 0; v < batch; ++v) {
         for (int64_t r = 0; r < rows; ++r) {
@@ -341,6 +407,8 @@ void oracle_qmatvec_f64(int fmt, const uint8_t *W, const int8_t *qs, const float
                 const uint8_t *blk = W + (r * nb + b) * bb;
                 if (fmt == FMT_Q4_K)
                     oracle_q4k_dequant(blk, w);
+                else if (fmt == FMT_Q5_K)
+                    oracle_q5k_dequant(blk, w);
                 else
                     oracle_q6k_dequant(blk, w);
                 for (int i = 0; i < QK; ++i)

@@ -27,10 +27,11 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 QK_K = 256
 Q4K_BLOCK_BYTES = 144
+Q5K_BLOCK_BYTES = 176
 Q6K_BLOCK_BYTES = 210
 
 # tensor ids used in stream keys
-T_Q4K, T_Q6K, T_ACT, T_RES, T_GAIN = 1, 2, 3, 4, 5
+T_Q4K, T_Q6K, T_ACT, T_RES, T_GAIN, T_Q5K = 1, 2, 3, 4, 5, 6
 # sub-streams inside a tensor
 _S_D, _S_DMIN, _S_SCALES, _S_QS, _S_QL, _S_QH, _S_U1, _S_U2 = range(8)
 
@@ -96,6 +97,23 @@ def q4k_weights(seed: int, rows: int, K: int, layer: int = 0, tensor: int = 0) -
     out[:, 4:16] = rand_bytes(stream_key(*base, _S_SCALES), n * 12).reshape(n, 12)
     out[:, 16:144] = rand_bytes(stream_key(*base, _S_QS), n * 128).reshape(n, 128)
     return out.reshape(rows, nb, Q4K_BLOCK_BYTES)
+
+
+def q5k_weights(seed: int, rows: int, K: int, layer: int = 0, tensor: int = 0) -> np.ndarray:
+    """uint8 [rows, K/256, 176]: canonical GGUF Q5_K blocks (d, dmin, 12 scale/min bytes, 32
+    bytes of fifth bits, 128 bytes of low nibbles); the same value distributions as Q4_K with
+    uniform fifth bits."""
+    assert K % QK_K == 0
+    nb = K // QK_K
+    n = rows * nb
+    base = (seed, T_Q5K, layer, tensor)
+    out = np.empty((n, Q5K_BLOCK_BYTES), dtype=np.uint8)
+    out[:, 0:2] = _f16_uniform(stream_key(*base, _S_D), n).view(np.uint8).reshape(n, 2)
+    out[:, 2:4] = _f16_uniform(stream_key(*base, _S_DMIN), n).view(np.uint8).reshape(n, 2)
+    out[:, 4:16] = rand_bytes(stream_key(*base, _S_SCALES), n * 12).reshape(n, 12)
+    out[:, 16:48] = rand_bytes(stream_key(*base, _S_QH), n * 32).reshape(n, 32)
+    out[:, 48:176] = rand_bytes(stream_key(*base, _S_QS), n * 128).reshape(n, 128)
+    return out.reshape(rows, nb, Q5K_BLOCK_BYTES)
 
 
 def q6k_weights(seed: int, rows: int, K: int, layer: int = 0, tensor: int = 0) -> np.ndarray:
@@ -168,6 +186,8 @@ def step_seed(layer: int) -> int:
 def weights(fmt: str, seed: int, rows: int, K: int, layer: int = 0, tensor: int = 0) -> np.ndarray:
     if fmt == "q4k":
         return q4k_weights(seed, rows, K, layer, tensor)
+    if fmt == "q5k":
+        return q5k_weights(seed, rows, K, layer, tensor)
     if fmt == "q6k":
         return q6k_weights(seed, rows, K, layer, tensor)
     raise ValueError(fmt)

@@ -537,3 +537,102 @@ def test_rmsnorm_sum_order_by_absorption():
     for other in (2.0 ** 24, 2.0 ** 24 + 1016):
         inv_o = np.float32(np.float32(1.0) / np.sqrt(np.float32(np.float32(other) / np.float32(K)), dtype=np.float32))
         assert inv_o != inv
+
+
+# ---- Q5_K: Q4_K's layout plus a plane of fifth bits --------------------------------------------------
+def test_q5k_handworked_block():
+    """d = 1, dmin = 0, every scale 1 and min 0, so w_e is the 5-bit code itself.  Worked by hand
+    from the GGUF layout: element 64c + t takes the low nibble of qs[32c + t] (t < 32) or the
+    high nibble of qs[32c + t - 32] (t >= 32), plus 16 x bit 2c of qh[t] (t < 32) or bit 2c+1
+    of qh[t - 32] (t >= 32)."""
+    blk = np.zeros(176, np.uint8)
+    blk[0:2] = [0x00, 0x3C]            # d = 1.0
+    blk[2:4] = [0x00, 0x00]            # dmin = 0
+    blk[4:16] = _q4k_encode_scales([1] * 8, [0] * 8)
+    qh, qs = blk[16:48], blk[48:176]
+    qs[0] = 0x21                       # element 0: low nibble 1; element 32: high nibble 2
+    qh[0] = 0b00000011                 # +16 on element 0 (bit 0) and element 32 (bit 1)
+    qs[69] = 0x03                      # element 133 = 64*2 + 5: low nibble 3
+    qh[5] = 0b00010000                 # bit 4 = 2c for c = 2: +16 on element 133
+    qs[127] = 0xF0                     # element 255 = 64*3 + 32 + 31: high nibble 15
+    qh[31] = 0b10000000                # bit 7 = 2c+1 for c = 3: +16 on element 255
+    qs[40] = 0x50                      # element 64*1 + 32 + 8 = 104: high nibble 5, no fifth bit
+    want = np.zeros(256)
+    want[[0, 32, 133, 255, 104]] = [17, 18, 19, 31, 5]
+    d, dmin, sc, m, q = O.q5k_fields(blk)
+    assert (d, dmin) == (1.0, 0.0) and list(sc) == [1] * 8 and list(m) == [0] * 8
+    assert np.array_equal(q, want.astype(np.int32))
+    assert np.array_equal(O.dequant(O.FMT_Q5_K, blk), want)
+
+
+def test_q5k_code_bits_are_a_bijection_onto_elements():
+    """Each of the 160 code bytes' bits drives exactly one element's bit: nibble bits 0..3 and
+    fifth bit 4, every (element, bit) pair exactly once."""
+    seen = set()
+    for byte in range(160):
+        for bit in range(8):
+            blk = np.zeros(176, np.uint8)
+            blk[16 + byte] = 1 << bit
+            _, _, _, _, q = O.q5k_fields(blk)
+            nz = np.nonzero(q)[0]
+            assert len(nz) == 1
+            v = int(q[nz[0]])
+            assert v in (1, 2, 4, 8, 16)
+            seen.add((int(nz[0]), v))
+    assert seen == {(e, 1 << b) for e in range(256) for b in range(5)}
+
+
+def test_q5k_with_zero_fifth_bits_is_q4k():
+    """qh = 0: a Q5_K block decodes, dots and sums exactly as the Q4_K block with the same d,
+    dmin, scales and nibbles."""
+    K, rows = 1536, 6
+    W5 = synth.q5k_weights(12, rows, K).copy()
+    W5[:, :, 16:48] = 0
+    W4 = np.concatenate([W5[:, :, 0:16], W5[:, :, 48:176]], axis=2)
+    x = synth.activations(12, 2, K)
+    qs, xd, bs = O.q8k_pack(x)
+    for r in range(rows):
+        assert np.array_equal(O.subdots(O.FMT_Q5_K, W5[r], qs[0]), O.subdots(O.FMT_Q4_K, W4[r], qs[0]))
+        assert np.array_equal(O.dequant(O.FMT_Q5_K, W5[r, 0]), O.dequant(O.FMT_Q4_K, W4[r, 0]))
+    y5 = O.qmatvec(O.FMT_Q5_K, W5, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN)
+    y4 = O.qmatvec(O.FMT_Q4_K, W4, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN)
+    assert np.array_equal(y5.view(np.uint32), y4.view(np.uint32))
+
+
+def test_q5k_fifth_bits_add_sixteen_times_the_block_sums():
+    """All fifth bits set: every code is its nibble + 16, so each sub-block dot grows by exactly
+    16 x the sub-block's q8 sum (the bsums)."""
+    K = 1024
+    W5 = synth.q5k_weights(13, 3, K).copy()
+    x = synth.activations(13, 1, K)
+    qs, xd, bs = O.q8k_pack(x)
+    Wz = W5.copy()
+    Wz[:, :, 16:48] = 0
+    W5[:, :, 16:48] = 0xFF
+    for r in range(3):
+        d1 = O.subdots(O.FMT_Q5_K, W5[r], qs[0]).astype(np.int64)
+        d0 = O.subdots(O.FMT_Q5_K, Wz[r], qs[0]).astype(np.int64)
+        assert np.array_equal(d1 - d0, 16 * bs[0].astype(np.int64))
+
+
+def test_q5k_subdots_and_epilogue_brute_force():
+    K, rows, batch = 768, 5, 2
+    W = synth.q5k_weights(14, rows, K)
+    x = synth.activations(14, batch, K)
+    qs, xd, bs = O.q8k_pack(x)
+    for r in range(rows):
+        dots = O.subdots(O.FMT_Q5_K, W[r], qs[1])
+        for b in range(3):
+            _, _, _, _, q = O.q5k_fields(W[r, b])
+            ref = [int(np.dot(q[32 * j:32 * j + 32], qs[1, 256 * b + 32 * j: 256 * b + 32 * j + 32].astype(np.int64)))
+                   for j in range(8)]
+            assert list(dots[b]) == ref
+    y64 = O.qmatvec_f64(O.FMT_Q5_K, W, qs, xd)
+    y = O.qmatvec(O.FMT_Q5_K, W, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN)
+    assert O.rel_err(y, y64).max() < 1e-5
+    # f64 brute force from the dequantised weights and the dequantised activations
+    for v in range(batch):
+        for r in range(rows):
+            w = np.concatenate([O.dequant(O.FMT_Q5_K, W[r, b]) for b in range(3)])
+            xh = np.repeat(xd[v].astype(np.float64), 256) * qs[v].astype(np.float64)
+            assert np.isclose(y64[v, r], float(np.dot(w, xh)), rtol=1e-12, atol=1e-12)
