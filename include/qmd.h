@@ -42,6 +42,7 @@ extern "C" {
 #define QMD_QK 256        /* values per K-quant and q8_K block */
 #define QMD_MAX_BATCH 8   /* activation columns per weight pass */
 #define QMD_Q4K_BLOCK_BYTES 144
+#define QMD_Q5K_BLOCK_BYTES 176
 #define QMD_Q6K_BLOCK_BYTES 210
 #define QMD_Q6K_BODY_BYTES 208
 
@@ -62,6 +63,7 @@ typedef enum qmd_status {
 /* Weight formats, named by their GGUF type ids. */
 typedef enum qmd_fmt {
     QMD_Q4_K = 12,       /* canonical GGUF Q4_K blocks, used in place (viewed as 32-bit words) */
+    QMD_Q5_K = 13,       /* canonical GGUF Q5_K blocks, used in place */
     QMD_Q6_K_SPLIT = 14  /* GGUF Q6_K after qmd_bind_q6k: 208-byte bodies + f16 scale prefix */
 } qmd_fmt;
 
@@ -130,11 +132,13 @@ qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, 
  * qmd_qmatvec -- y[v][r] = sum over the row's blocks of the rank-one epilogue of integer
  * sub-block dots, for v < batch, r < rows
  * ("Language models on the device: the cajeta-llm kernels", §1, §2.1 one row finished by a
- * reduction; §2.2 the batched "Cols" form: one pass over a weight row serves all columns).
+ * reduction; §2.2 the batched "Cols" form: one pass over a weight row serves all columns;
+ * §2.3 Q5_K is Q4_K with a fifth-bit plane OR-ed into bit four of each code).
  *
  * Per 256-value block b of row r against vector v (exact int32 S and M, f32 elsewhere, each
  * operation rounded on its own):
- *   Q4_K:        S = sum_j sc_j * dot_j,  M = sum_j m_j * bsums[v][b][j]   (j = 0..7, 32 values)
+ *   Q4_K, Q5_K:  S = sum_j sc_j * dot_j,  M = sum_j m_j * bsums[v][b][j]   (j = 0..7, 32 values;
+ *                Q4_K codes 0..15, Q5_K codes 0..31)
  *                term = d_x * ( f32(d) * (float)S - f32(dmin) * (float)M )
  *   Q6_K_SPLIT:  S = sum_s sc_s * dot'_s, dot'_s over 16 values of (q - 32) * q8   (s = 0..15)
  *                term = d_x * ( f32(d) * (float)S )
@@ -143,10 +147,11 @@ qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, 
  * of four (16 blocks), each run ((G0 + G1) + G2) + G3 with absent groups counted as +0; then
  * the run sums left to right.  y is overwritten, not accumulated.
  *
- *   fmt    QMD_Q4_K or QMD_Q6_K_SPLIT
+ *   fmt    QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT
  *   W      Q4_K: GGUF blocks u8 [rows][nb][144] (16-byte aligned; read in place as u32 words)
+ *          Q5_K: GGUF blocks u8 [rows][nb][176] (16-byte aligned; read in place)
  *          Q6_K_SPLIT: bodies u8 [rows][nb][208] from qmd_bind_q6k (16-byte aligned)
- *   W_aux  Q4_K: ignored (may be NULL).  Q6_K_SPLIT: the f16 scale prefix from qmd_bind_q6k,
+ *   W_aux  Q4_K, Q5_K: ignored (may be NULL).  Q6_K_SPLIT: the f16 scale prefix from qmd_bind_q6k,
  *          [rows][qmd_q6k_prefix_stride(K)] (16-byte aligned)
  *   xq     packed activations for `batch` vectors of length K (qs, bsums 16-byte aligned,
  *          d 4-byte aligned; bsums may be NULL for Q6_K_SPLIT, which does not read them)
@@ -252,9 +257,9 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
  * qmd_debug_qmatvec_dump -- qmd_qmatvec plus a record of its integer arithmetic, from the
  * same kernel code with extra stores.
  *   dots  int32 [batch][rows][nb][16], zeroed by the caller:
- *         Q4_K: entry j < 8 is dot_j of sub-block j (entries 8..15 stay 0);
+ *         Q4_K, Q5_K: entry j < 8 is dot_j of sub-block j (entries 8..15 stay 0);
  *         Q6_K_SPLIT: entry s is dot'_s of group s.
- *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K) M; M = 0 for Q6_K_SPLIT.
+ *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K, Q5_K) M; M = 0 for Q6_K_SPLIT.
  * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm; this entry also
  * refuses K > 16384 (QMD_ERR_SHAPE).
  */

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(HERE, "libqmd.so")
 QMD_QK = 256
 QMD_MAX_BATCH = 8
 Q4_K = 12
+Q5_K = 13
 Q6_K_SPLIT = 14
 
 STATUS = {

@@ -132,7 +132,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
 {
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
     const bool fused = mode == QMV_PACK;
-    const int row_bytes = nb * (q6 ? 208 : 144);
+    const int row_bytes = nb * (q6 ? 208 : fmt == QMD_Q5_K ? 176 : 144);
     const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
     pl->row_bytes = row_bytes;
     pl->pre_bytes = pre_bytes;
@@ -217,7 +217,7 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
                           int64_t rows, int64_t K, int batch, int32_t *dots, int32_t *sm, bool dump,
                           const float *x, qmd_q8k xq_out, void *stream)
 {
-    if (fmt != QMD_Q4_K && fmt != QMD_Q6_K_SPLIT)
+    if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
         return QMD_ERR_FORMAT;
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
     const bool fused = x != nullptr;
@@ -266,7 +266,7 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
     a.xq_d_out = fused && want_out ? xq_out.d : nullptr;
     a.xq_bs_out = fused && want_out ? xq_out.bsums : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return q6 ? launch_qmv_q6k(a, plan, s) : launch_qmv_q4k(a, plan, s);
+    return q6 ? launch_qmv_q6k(a, plan, s) : fmt == QMD_Q5_K ? launch_qmv_q5k(a, plan, s) : launch_qmv_q4k(a, plan, s);
 }
 
 }  // namespace
@@ -446,7 +446,7 @@ void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int 
 qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int batch, int *grid,
                                    int *threads, int *smem_bytes, int *stages, int *rows_per_stage)
 {
-    if (fmt != QMD_Q4_K && fmt != QMD_Q6_K_SPLIT)
+    if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
         return QMD_ERR_FORMAT;
     qmd_status st = check_k(K);
     if (st != QMD_OK)

@@ -40,7 +40,7 @@ qmd_status fail(qmd_status st, const char *what, cudaError_t e);
 
 // ---- mat-vec -------------------------------------------------------------------------------
 struct QmvArgs {
-    int fmt;  // QMD_Q4_K or QMD_Q6_K_SPLIT
+    int fmt;  // QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT
     const uint8_t *W;
     const uint8_t *Wpre;
     const int8_t *xqs;
@@ -70,6 +70,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
                     int mode = 0);
 
 qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
+qmd_status launch_qmv_q5k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 
 // ---- pack, bind, debug ---------------------------------------------------------------------

@@ -1,12 +1,14 @@
-// qmv.cuh -- the Q4_K / Q6_K x q8_K decode mat-vec kernel (templated on format, batch, rows
-// per stage).
+// qmv.cuh -- the Q4_K / Q5_K / Q6_K x q8_K decode mat-vec kernel (templated on format, batch,
+// rows per stage).
 //
 // What it computes ("Language models on the device: the cajeta-llm kernels"):
 //   §1   integer dot products of weight codes against q8_K activation bytes, with the
 //        per-sub-block scales (and Q4_K's mins, through the q8_K sub-block sums) folded in by a
 //        rank-one epilogue per 256-value block;
 //   §2.1 a reduction over the row's blocks finishes each output row;
-//   §2.2 batched decode: one pass over a weight row is dotted against up to 8 vectors.
+//   §2.2 batched decode: one pass over a weight row is dotted against up to 8 vectors;
+//   §2.3 a Q5_K member differs from the Q4_K one only in staging, the fifth-bit plane OR-ed
+//        into bit four of each code (here: in registers, before the dot products).
 //
 // How, on sm_103a.  The pages' design has one wave own a row, each lane loading its own words
 // from global memory, with "prefetch twins" issuing the next block's loads early.  Here:
@@ -162,9 +164,12 @@ __host__ __device__ constexpr int qmv_max_threads(int B, int mode)
     return (B <= 2 && mode != QMV_DUMP) ? 1024 : 512;
 }
 
-template <bool Q6, int B, int PR, int MODE>
+// F is the format: QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT.
+template <int F, int B, int PR, int MODE>
 __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const QmvKParams p)
 {
+    constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
+    constexpr bool Q5 = F == QMD_Q5_K;
     constexpr bool DUMP = MODE == QMV_DUMP;
     constexpr bool PACK = MODE == QMV_PACK;
     constexpr int P = PR * B;                                       // (row, vector) slots
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
     constexpr int PP = P > 4 ? 8 : P > 2 ? 4 : P > 1 ? 2 : 1;       // padded to a power of two
     constexpr int LP = PP == 8 ? 3 : PP == 4 ? 2 : PP == 2 ? 1 : 0;
     constexpr int DUP = 8 >> LP;  // lanes of a block holding the same slot
-    constexpr int BLOCK_BYTES = Q6 ? 208 : 144;
+    constexpr int BLOCK_BYTES = Q6 ? 208 : Q5 ? 176 : 144;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -321,6 +326,9 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
     const int q6_sc_off = 192 + 8 * (k >> 2);
     const int q6_sl = 4 - 2 * ((k >> 1) & 1);  // low run: 2-bit field t=tl moved to bits 4..5
     const int q6_sh = 2 * ((k >> 1) & 1);      // high run: field t=tl+2 moved to bits 4..5
+    // Q5_K: this lane's fifth bits are bits 2c (low run) and 2c+1 (high run) of the 16 qh
+    // bytes 16 (k & 1) ..; a rotation right by these amounts brings each to bit 4 of its byte
+    const int q5_rl = (2 * (k >> 1) - 4) & 31, q5_rh = (2 * (k >> 1) - 3) & 31;
 
     const int slot = k >> (3 - LP);
     const bool slot_ok = slot < P;
@@ -353,14 +361,43 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
 
         // ---- integer slice dots, folded with the sub-block scales -------------------------
         // Q4_K partials are carried as 16 x S (the high-nibble dots come out scaled by 16);
-        // Q6_K partials are S itself.
+        // Q5_K and Q6_K partials are S itself.
         int S[PP];
 #pragma unroll
         for (int i = 0; i < PP; ++i)
             S[i] = 0;
         auto row_dots = [&](int i, int pr) {
             const uint8_t *bp = stage + i * p.row_stride + blk * BLOCK_BYTES;
-            if (!Q6) {
+            if (Q5) {
+                const uint4 h = lds128(bp);
+                const uint4 q = lds128(bp + 48 + 16 * k);
+                const uint4 qh = lds128(bp + 16 + 16 * (k & 1));
+                const uint32_t scw = hiw ? ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u))
+                                         : (h.y & 0x3F3F3F3Fu);
+                const int sc_lo = (int)__byte_perm(scw, 0u, sel_lo);
+                const int sc_hi = (int)__byte_perm(scw, 0u, sel_hi);
+                // 5-bit codes, one per byte: the nibble, with the fifth bit OR-ed into bit 4
+                uint4 wlo, whi;
+                wlo.x = (q.x & 0x0F0F0F0Fu) | (__funnelshift_r(qh.x, qh.x, q5_rl) & 0x10101010u);
+                wlo.y = (q.y & 0x0F0F0F0Fu) | (__funnelshift_r(qh.y, qh.y, q5_rl) & 0x10101010u);
+                wlo.z = (q.z & 0x0F0F0F0Fu) | (__funnelshift_r(qh.z, qh.z, q5_rl) & 0x10101010u);
+                wlo.w = (q.w & 0x0F0F0F0Fu) | (__funnelshift_r(qh.w, qh.w, q5_rl) & 0x10101010u);
+                whi.x = ((q.x >> 4) & 0x0F0F0F0Fu) | (__funnelshift_r(qh.x, qh.x, q5_rh) & 0x10101010u);
+                whi.y = ((q.y >> 4) & 0x0F0F0F0Fu) | (__funnelshift_r(qh.y, qh.y, q5_rh) & 0x10101010u);
+                whi.z = ((q.z >> 4) & 0x0F0F0F0Fu) | (__funnelshift_r(qh.z, qh.z, q5_rh) & 0x10101010u);
+                whi.w = ((q.w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_r(qh.w, qh.w, q5_rh) & 0x10101010u);
+#pragma unroll
+                for (int v = 0; v < B; ++v) {
+                    const int dl = dp4a_chain(wlo, alo[v]);
+                    const int dh = dp4a_chain(whi, ahi[v]);
+                    S[pr * B + v] = sc_lo * dl + sc_hi * dh;
+                    if (DUMP) {  // sub-blocks 2c, 2c+1: this lane holds half of each
+                        int32_t *dd = p.dbg_dots + ((v * p.rows + rs + i) * nb + blk) * 16;
+                        atomicAdd(dd + 2 * (k >> 1), dl);
+                        atomicAdd(dd + 2 * (k >> 1) + 1, dh);
+                    }
+                }
+            } else if (!Q6) {
                 const uint4 h = lds128(bp);
                 const uint4 q = lds128(bp + 16 + 16 * k);
                 // this lane's sub-blocks' 6-bit scales (bytes of scw), then the two it needs
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
         if (blk_ok && slot_ok && srow < nr) {
             const uint8_t *bp = stage + srow * p.row_stride + blk * BLOCK_BYTES;
             const float dx = s_dx[sv * nb + blk];
-            const int Sb = Q6 ? Sv : (Sv >> 4);  // exact: Q4_K carried 16 x S
+            const int Sb = (Q6 || Q5) ? Sv : (Sv >> 4);  // exact: Q4_K carried 16 x S
             const float fS = __int2float_rn(Sb);
             int M = 0;
             if (!Q6) {
@@ -555,30 +592,30 @@ qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t
     return QMD_OK;
 }
 
-template <bool Q6, int B, int PR, int MODE>
+template <int F, int B, int PR, int MODE>
 qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
-    return launch_kernel<qmv_kernel<Q6, B, PR, MODE>>(kp, plan, s);
+    return launch_kernel<qmv_kernel<F, B, PR, MODE>>(kp, plan, s);
 }
 
 // Rows per stage and row group (PR x B <= 8); the plan picks one.
-template <bool Q6, int B, int MODE>
+template <int F, int B, int MODE>
 qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
     switch (plan.PR) {
     case 1:
-        return launch_one<Q6, B, 1, MODE>(kp, plan, s);
+        return launch_one<F, B, 1, MODE>(kp, plan, s);
     case 2:
         if constexpr (2 * B <= 8)
-            return launch_one<Q6, B, 2, MODE>(kp, plan, s);
+            return launch_one<F, B, 2, MODE>(kp, plan, s);
         break;
     case 4:
         if constexpr (4 * B <= 8)
-            return launch_one<Q6, B, 4, MODE>(kp, plan, s);
+            return launch_one<F, B, 4, MODE>(kp, plan, s);
         break;
     case 8:
         if constexpr (B == 1)
-            return launch_one<Q6, B, 8, MODE>(kp, plan, s);
+            return launch_one<F, B, 8, MODE>(kp, plan, s);
         break;
     }
     return QMD_ERR_SHAPE;
@@ -616,14 +653,14 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     return QMD_OK;
 }
 
-template <bool Q6>
+template <int F>
 qmd_status launch_qmv_slice(const QmvKParams &kp, const QmvPlan &plan, int batch, int mode, cudaStream_t s)
 {
 #define QMD_CASE(BB)                                                                                 \
     case BB:                                                                                         \
-        return mode == QMV_PACK   ? launch_rows<Q6, BB, QMV_PACK>(kp, plan, s)                       \
-               : mode == QMV_DUMP ? launch_rows<Q6, BB, QMV_DUMP>(kp, plan, s)                       \
-                                  : launch_rows<Q6, BB, QMV_PLAIN>(kp, plan, s);
+        return mode == QMV_PACK   ? launch_rows<F, BB, QMV_PACK>(kp, plan, s)                        \
+               : mode == QMV_DUMP ? launch_rows<F, BB, QMV_DUMP>(kp, plan, s)                        \
+                                  : launch_rows<F, BB, QMV_PLAIN>(kp, plan, s);
     switch (batch) {
         QMD_CASE(1)
         QMD_CASE(2)

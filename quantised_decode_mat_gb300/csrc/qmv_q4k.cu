@@ -10,7 +10,7 @@ qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     const qmd_status st = make_params(a, plan, kp, mode);
     if (st != QMD_OK)
         return st;
-    return launch_qmv_slice<false>(kp, plan, a.batch, mode, s);
+    return launch_qmv_slice<QMD_Q4_K>(kp, plan, a.batch, mode, s);
 }
 
 }  // namespace qmd

@@ -1,0 +1,16 @@
+// qmv_q5k.cu -- Q5_K instances of the decode mat-vec (batch 1..8, plus the recording variant).
+#include "qmv.cuh"
+
+namespace qmd {
+
+qmd_status launch_qmv_q5k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
+{
+    QmvKParams kp;
+    int mode = QMV_PLAIN;
+    const qmd_status st = make_params(a, plan, kp, mode);
+    if (st != QMD_OK)
+        return st;
+    return launch_qmv_slice<QMD_Q5_K>(kp, plan, a.batch, mode, s);
+}
+
+}  // namespace qmd

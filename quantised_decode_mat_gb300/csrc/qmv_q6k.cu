@@ -11,7 +11,7 @@ qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     const qmd_status st = make_params(a, plan, kp, mode);
     if (st != QMD_OK)
         return st;
-    return launch_qmv_slice<true>(kp, plan, a.batch, mode, s);
+    return launch_qmv_slice<QMD_Q6_K_SPLIT>(kp, plan, a.batch, mode, s);
 }
 
 }  // namespace qmd

@@ -74,7 +74,7 @@ def st_qmatvec(L, fmt=q.Q4_K, W=A, Wa=A, xq=None, y=A, rows=16, K=512, batch=1):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=13), 2),
+    (dict(fmt=15), 2), (dict(fmt=11), 2),
     (dict(W=None), 1),
     (dict(y=None), 1),
     (dict(xq=_xq(qs=None)), 1),

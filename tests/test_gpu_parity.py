@@ -63,8 +63,8 @@ def gpu_pack(x):
 def run_matvec(fmtname, Wg, xq, rows, K, batch):
     """Upload canonical GGUF weights, bind (Q6_K), run the mat-vec into a poisoned buffer."""
     buf, y = poisoned_y(batch, rows)
-    if fmtname == "q4k":
-        q.qmatvec(q.Q4_K, dev(Wg.reshape(rows, -1)), None, xq, y, rows)
+    if fmtname in ("q4k", "q5k"):
+        q.qmatvec(QFMT[fmtname], dev(Wg.reshape(rows, -1)), None, xq, y, rows)
     else:
         body, prefix = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
         q.qmatvec(q.Q6_K_SPLIT, body, prefix, xq, y, rows)
@@ -73,7 +73,8 @@ def run_matvec(fmtname, Wg, xq, rows, K, batch):
     return y.cpu().numpy()
 
 
-OFMT = {"q4k": O.FMT_Q4_K, "q6k": O.FMT_Q6_K}
+OFMT = {"q4k": O.FMT_Q4_K, "q5k": O.FMT_Q5_K, "q6k": O.FMT_Q6_K}
+QFMT = {"q4k": q.Q4_K, "q5k": q.Q5_K, "q6k": q.Q6_K_SPLIT}
 
 
 def check_against_oracle(fmtname, Wg, x, y, rows_idx=None, exact=True):
@@ -120,7 +121,7 @@ def test_pack_bit_exact(name, x):
 
 
 # ---- integer dots, S and M, bit-exact (recording variant of the same kernel) -----------------------
-@pytest.mark.parametrize("fmtname", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmtname", ["q4k", "q5k", "q6k"])
 @pytest.mark.parametrize("batch,rows,K", [(1, 37, 1024), (2, 19, 2304), (3, 11, 256), (5, 7, 3072), (8, 13, 4096),
                                           (1, 9, 14336), (2, 5, 5376)])
 def test_subblock_dots_exact(fmtname, batch, rows, K):
@@ -128,8 +129,8 @@ def test_subblock_dots_exact(fmtname, batch, rows, K):
     x = synth.activations(7, batch, K)
     xq = gpu_pack(x)
     Wd = dev(Wg.reshape(rows, -1))
-    if fmtname == "q4k":
-        y, dots, sm = q.debug_qmatvec_dump(q.Q4_K, Wd, None, xq)
+    if fmtname in ("q4k", "q5k"):
+        y, dots, sm = q.debug_qmatvec_dump(QFMT[fmtname], Wd, None, xq)
     else:
         body, prefix = q.bind_q6k(Wd, rows, K)
         y, dots, sm = q.debug_qmatvec_dump(q.Q6_K_SPLIT, body, prefix, xq, rows)
@@ -141,15 +142,15 @@ def test_subblock_dots_exact(fmtname, batch, rows, K):
     for v in range(batch):
         for r in range(rows):
             od_ = O.subdots(OFMT[fmtname], Wg[r], oqs[v])
-            if fmtname == "q4k":
+            if fmtname in ("q4k", "q5k"):
                 got = dots[v, r][:, :8]  # entry j: sub-block j
                 assert not dots[v, r][:, 8:].any()
             else:
                 got = dots[v, r]
             assert np.array_equal(got, od_), (v, r)
             for b in range(nb):
-                if fmtname == "q4k":
-                    _, _, sc, m, _ = O.q4k_fields(Wg[r, b])
+                if fmtname in ("q4k", "q5k"):
+                    _, _, sc, m, _ = (O.q4k_fields if fmtname == "q4k" else O.q5k_fields)(Wg[r, b])
                     S = int(np.dot(sc, od_[b]))
                     M = int(np.dot(m, obs[v, b].astype(np.int64)))
                 else:
@@ -201,6 +202,9 @@ SWEEP = [
     ("q6k", 1, 256, 1), ("q6k", 5, 512, 2), ("q6k", 130, 1792, 1), ("q6k", 257, 2304, 3),
     ("q6k", 64, 3328, 4), ("q6k", 300, 14336, 1), ("q6k", 40, 14336, 2), ("q6k", 31, 14336, 4),
     ("q6k", 17, 14336, 8), ("q6k", 4, 32768, 1), ("q6k", 9, 16384, 7),
+    ("q5k", 1, 256, 1), ("q5k", 4096, 4096, 1), ("q5k", 129, 768, 3), ("q5k", 333, 2048, 4),
+    ("q5k", 77, 4352, 5), ("q5k", 500, 4096, 8), ("q5k", 9, 32768, 1), ("q5k", 6, 32768, 2),
+    ("q5k", 40, 14336, 2), ("q5k", 5, 16384, 7), ("q5k", 1000, 1280, 2),
 ]
 
 
@@ -218,7 +222,8 @@ def test_sweep_shapes(fmtname, rows, K, batch):
                                   (2, 2, 8, 2), (5, 1, 2, 3)])
 @pytest.mark.parametrize("fmtname,rows,K,batch", [("q4k", 2000, 4096, 1), ("q4k", 700, 2048, 3),
                                                   ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2),
-                                                  ("q6k", 90, 14336, 1)])
+                                                  ("q6k", 90, 14336, 1), ("q5k", 1500, 4096, 1),
+                                                  ("q5k", 300, 3072, 4)])
 def test_pipeline_plans(plan, fmtname, rows, K, batch):
     """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits."""
     q.debug_set_plan(*plan)
@@ -250,6 +255,19 @@ def test_degenerate_inputs():
     W6[:, :, 128:192] = 0xAA
     y = run_matvec("q6k", W6, gpu_pack(x), rows, K, 1)
     assert np.all(y == 0.0)
+    # Q5_K with no fifth bits gives the Q4_K block's bits exactly
+    W5 = synth.q5k_weights(1, rows, K).copy()
+    W5[:, :, 16:48] = 0
+    W4 = np.ascontiguousarray(np.concatenate([W5[:, :, 0:16], W5[:, :, 48:176]], axis=2))
+    xq = gpu_pack(x)
+    y5 = run_matvec("q5k", W5, xq, rows, K, 1)
+    y4 = run_matvec("q4k", W4, xq, rows, K, 1)
+    assert np.array_equal(y5.view(np.uint32), y4.view(np.uint32))
+    # Q5_K with every fifth bit set and zero nibbles: codes all 16
+    W5[:, :, 16:48] = 0xFF
+    W5[:, :, 48:176] = 0
+    y = run_matvec("q5k", W5, xq, rows, K, 1)
+    check_against_oracle("q5k", W5, x, y)
 
 
 def test_bind_q6k_matches_oracle_split():
@@ -308,7 +326,8 @@ def test_launch_info_shapes():
 # ---- fused pack + mat-vec: the same bits as the two-call path -----------------------------------------
 FUSED = [("q4k", 256, 2048, 1), ("q4k", 4096, 4096, 1), ("q6k", 4096, 14336, 1), ("q4k", 333, 2048, 4),
          ("q4k", 77, 4352, 5), ("q6k", 64, 3328, 4), ("q6k", 17, 14336, 8), ("q4k", 9, 32768, 1),
-         ("q6k", 130, 1792, 3), ("q4k", 1000, 1280, 2)]
+         ("q6k", 130, 1792, 3), ("q4k", 1000, 1280, 2), ("q5k", 4096, 4096, 1), ("q5k", 200, 2048, 3),
+         ("q5k", 50, 14336, 8)]
 
 
 @pytest.mark.parametrize("fmtname,rows,K,batch", FUSED)
@@ -317,8 +336,8 @@ def test_fused_equals_pack_then_matvec(fmtname, rows, K, batch):
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
     xd = dev(x)
-    if fmtname == "q4k":
-        W, Wa, f = dev(Wg.reshape(rows, -1)), None, q.Q4_K
+    if fmtname in ("q4k", "q5k"):
+        W, Wa, f = dev(Wg.reshape(rows, -1)), None, QFMT[fmtname]
     else:
         W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
         f = q.Q6_K_SPLIT
