@@ -286,8 +286,9 @@ void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int 
 
 /*
  * qmd_debug_set_launch_flags -- test-only launch options for later launches: bit 0 launches
- * qmd_q8k_pack and qmd_qmatvec without programmatic dependent launch (plain stream order).
- * Results are the same either way.  Process-wide.
+ * qmd_q8k_pack and qmd_qmatvec without programmatic dependent launch (plain stream order);
+ * bit 1 computes batches of 5..8 vectors with the dp4a kernel even where the tensor-core
+ * kernel would be chosen.  Results are the same either way.  Process-wide.
  */
 void qmd_debug_set_launch_flags(unsigned flags);
 

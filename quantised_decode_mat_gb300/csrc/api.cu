@@ -13,7 +13,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
-#include "qmv.cuh"
+#include "qmv_tc.cuh"
 
 namespace qmd {
 
@@ -137,6 +137,46 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->row_bytes = row_bytes;
     pl->pre_bytes = pre_bytes;
     pl->row_stride = row_bytes;
+    // Tensor-core kernel: batches of 5..8 vectors, Q4_K / Q5_K rows of at most 16 blocks (below
+    // 5 vectors the dp4a kernel is as fast or faster).  One warp per block, each with its own
+    // ring of 16-row tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per
+    // warp) that fits.  A forced ring cap below 3 selects the dp4a kernel.
+    const int fst = g_force_stages.load();
+    if (batch >= TC_MIN_BATCH && nb <= 16 && fmt != QMD_Q6_K_SPLIT && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
+        (fst <= 0 || fst >= 3)) {
+        const bool q5 = fmt == QMD_Q5_K;
+        const int64_t ntiles = (rows + TC_ROWS - 1) / TC_ROWS;
+        int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / nb > 0 ? 16 / nb : 1);
+        if (cps > 8)
+            cps = 8;
+        int st = 0;
+        for (; cps >= 1; --cps) {
+            int budget = dev.smem_per_sm / cps - 1024;
+            if (budget > dev.smem_optin)
+                budget = dev.smem_optin;
+            for (st = 4; st >= 3; --st)
+                if ((fst <= 0 || st <= fst) &&
+                    qmv_tc_layout(st, q5, nb, batch, fused).total <= budget)
+                    break;
+            if (st >= 3)
+                break;
+        }
+        if (cps >= 1 && st >= 3) {  // otherwise the dp4a kernel below takes the call
+            int64_t grid = (int64_t)dev.sm_count * cps;
+            if (grid > ntiles)
+                grid = ntiles;
+            pl->layout = 1;
+            pl->grid = (int)grid;
+            pl->stages = st;
+            pl->threads = 32 * nb;
+            pl->smem = qmv_tc_layout(st, q5, nb, batch, fused).total;
+            pl->WR = nb;
+            pl->RG = 1;
+            pl->PR = TC_ROWS;
+            pl->stage_bytes = tc_slot_bytes(q5);
+            return QMD_OK;
+        }
+    }
     // A warp covers 4 blocks of a row, 8 lanes per block; a row takes ceil(nb / 4) warps.
     const int max_threads = qmv_max_threads(batch, mode);  // the kernels' launch bounds
     const int WR = (nb + 3) / 4;
@@ -170,6 +210,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused).total + 64;
     if (!fit_stages(dev, rows, TR, stage_bytes, extra, fixed, cps, pl))
         return QMD_ERR_SHAPE;
+    pl->layout = 0;
     pl->threads = RG * WR * 32;
     pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused).total;
     pl->WR = WR;

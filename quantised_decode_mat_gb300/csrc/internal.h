@@ -31,9 +31,10 @@ unsigned *device_error_word();
 
 uint64_t wait_limit_ns();
 
-// Test-only launch flags (bit 0: launch without programmatic dependent launch).
+// Test-only launch flags (bit 0: launch without programmatic dependent launch; bit 1: compute
+// batches of 5..8 vectors with the dp4a kernel even where the tensor-core kernel applies).
 unsigned launch_flags();
-enum : unsigned { LAUNCH_NO_PDL = 1u };
+enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u };
 
 // Record a CUDA error for qmd_last_error_detail and map it to a status.
 qmd_status fail(qmd_status st, const char *what, cudaError_t e);
@@ -59,6 +60,7 @@ struct QmvArgs {
 };
 
 struct QmvPlan {
+    int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh)
     int grid, threads, smem, stages;
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;

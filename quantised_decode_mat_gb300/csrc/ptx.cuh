@@ -1,6 +1,6 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a: shared-memory mbarriers, 1-D bulk async copies
-// (global -> this CTA's shared memory, no multicast), programmatic dependent launch, and a
-// bounded barrier wait that gives up instead of hanging.
+// (global -> this CTA's shared memory, no multicast), per-thread 16-byte async copies,
+// programmatic dependent launch, and a bounded barrier wait that gives up instead of hanging.
 #pragma once
 
 #include <cstdint>
@@ -88,6 +88,23 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared by one thread (no L1 allocation, L2 policy as
+// given); completion is tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Programmatic dependent launch: let the next kernel in the stream be scheduled, and wait

@@ -52,6 +52,7 @@ struct QmvKParams {
     float *y;
     int64_t rows;
     int nb, WR, RG, stages, row_bytes, pre_bytes, stage_bytes, row_stride;
+    int batch;
     int32_t *dbg_dots;
     int32_t *dbg_sm;
     const float *x;       // fused form: f32 activations [B][K], packed inside the kernel
@@ -632,6 +633,7 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     kp.y = a.y;
     kp.rows = a.rows;
     kp.nb = a.nb;
+    kp.batch = a.batch;
     kp.WR = plan.WR;
     kp.RG = plan.RG;
     kp.stages = plan.stages;

@@ -1,5 +1,5 @@
 // qmv_q5k.cu -- Q5_K instances of the decode mat-vec (batch 1..8, plus the recording variant).
-#include "qmv.cuh"
+#include "qmv_tc.cuh"
 
 namespace qmd {
 
@@ -10,6 +10,8 @@ qmd_status launch_qmv_q5k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     const qmd_status st = make_params(a, plan, kp, mode);
     if (st != QMD_OK)
         return st;
+    if (plan.layout == 1)
+        return launch_qmv_tc<QMD_Q5_K>(kp, plan, mode, s);
     return launch_qmv_slice<QMD_Q5_K>(kp, plan, a.batch, mode, s);
 }
 

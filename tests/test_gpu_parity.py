@@ -223,7 +223,7 @@ def test_sweep_shapes(fmtname, rows, K, batch):
 @pytest.mark.parametrize("fmtname,rows,K,batch", [("q4k", 2000, 4096, 1), ("q4k", 700, 2048, 3),
                                                   ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2),
                                                   ("q6k", 90, 14336, 1), ("q5k", 1500, 4096, 1),
-                                                  ("q5k", 300, 3072, 4)])
+                                                  ("q5k", 300, 3072, 4), ("q4k", 900, 4096, 6)])
 def test_pipeline_plans(plan, fmtname, rows, K, batch):
     """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits."""
     q.debug_set_plan(*plan)
@@ -367,3 +367,56 @@ def test_fused_refusals():
     assert L.qmd_qmatvec_x(q.Q4_K, W.data_ptr(), None, x.data_ptr(), part, y.data_ptr(), rows, K, 1, None) == 1
     torch.cuda.synchronize()
     assert torch.isnan(y).all() and guard_intact(buf, 1, rows)
+
+
+# ---- batches of 3..8 on the tensor cores: the same bits as the dp4a kernel -----------------------------
+DP4A_ONLY = 2  # launch flag: keep batches of 5..8 on the dp4a kernel
+
+
+@pytest.mark.parametrize("fmtname", ["q4k", "q5k"])
+@pytest.mark.parametrize("batch", [5, 6, 7, 8])
+@pytest.mark.parametrize("rows,K", [(1000, 4096), (37, 256), (300, 2048), (17, 3840), (4099, 1280)])
+def test_tensor_core_path_equals_dp4a_path(fmtname, batch, rows, K):
+    seed = 3 * rows + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xq = gpu_pack(x)
+    info = q.launch_info(QFMT[fmtname], rows, K, batch)
+    assert info["threads"] == 32 * (K // 256) and info["rows_per_stage"] == 16  # the tensor-core plan
+    y_tc = run_matvec(fmtname, Wg, xq, rows, K, batch)
+    q.debug_set_launch_flags(DP4A_ONLY)
+    try:
+        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] != 16
+        y_dp = run_matvec(fmtname, Wg, xq, rows, K, batch)
+    finally:
+        q.debug_set_launch_flags(0)
+    assert np.array_equal(y_tc.view(np.uint32), y_dp.view(np.uint32))
+    idx = _sample_rows(rows, 96, seed)
+    check_against_oracle(fmtname, Wg, x, y_tc, rows_idx=idx)
+
+
+@pytest.mark.parametrize("fmtname", ["q4k", "q5k"])
+def test_tensor_core_extreme_magnitudes(fmtname):
+    """The largest codes and scales against activations of +-127: the accumulator's partial
+    sums reach their bound, and the integer dots must still be exact."""
+    rows, K, batch = 48, 4096, 8
+    Wg = synth.weights(fmtname, 77, rows, K).copy()
+    off = 48 if fmtname == "q5k" else 16
+    Wg[:, :, 4:16] = 0xFF                  # every scale and min 63
+    Wg[:, :, off:] = 0xFF                  # every nibble 15
+    if fmtname == "q5k":
+        Wg[:, :, 16:48] = 0xFF             # every fifth bit: codes 31
+    Wg[::2, :, off:] = 0x00                # even rows: codes 0 (only the min term)
+    x = np.ones((batch, K), np.float32)
+    x[1::2] = -1.0                         # +-1 everywhere: codes +-127
+    x[2, ::3] = -1.0                       # mixed signs
+    x[4] = synth.activations(78, 1, K)[0]
+    y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    check_against_oracle(fmtname, Wg, x, y)
+    yd, dots, sm = q.debug_qmatvec_dump(QFMT[fmtname], dev(Wg.reshape(rows, -1)), None, gpu_pack(x))
+    q.get_device_error()
+    oqs, _, _ = O.q8k_pack(x)
+    dots = dots.cpu().numpy()
+    for v in range(batch):
+        for r in (0, 1, 2, 47):
+            assert np.array_equal(dots[v, r][:, :8], O.subdots(OFMT[fmtname], Wg[r], oqs[v]))
