@@ -5,8 +5,10 @@
 A step is one pass of the whole hot path over one batch of synthetic input: for each of 32
 layers and each projection {q|k|v Q4_K 6144x4096, o Q4_K 4096x4096, gate|up Q4_K 28672x4096,
 down Q6_K 4096x14336}, the q8_K pack of that projection's activation and the mat-vec of its
-weight -- by default in one launch per projection (qmd_qmatvec_x, which packs inside the
-kernel), with --unfused as qmd_q8k_pack followed by qmd_qmatvec.  Each launch depends on the
+weight.  By default (and with --fused) a batch of one vector runs one launch per projection
+(qmd_qmatvec_x, which packs inside the kernel); larger batches, or --unfused, run
+qmd_q8k_pack followed by qmd_qmatvec (every CTA of a fused launch packs the whole batch for
+itself, which costs more than the extra launch once there are two or more vectors).  Each launch depends on the
 previous one in stream order, as in a real decode where a projection's input comes from the
 layer before.  The step's launches are captured once into a CUDA graph and replayed.  Weights
 (4.41 GB) exceed L2 many times over, so consecutive steps read them from HBM.
@@ -232,12 +234,21 @@ def run_reference(args):
     return 0
 
 
+def use_fused(args) -> bool:
+    """One launch per projection at batch 1, pack + mat-vec above, unless a flag says otherwise."""
+    if getattr(args, "fused", False):
+        return True
+    if getattr(args, "unfused", False):
+        return False
+    return args.batch == 1
+
+
 def workload_config(args):
     from quantised_decode_mat_gb300 import synth
     layers = getattr(args, "layers", synth.STEP_LAYERS)
     return {"workload": f"decode_step_7b_q4k_q6k_{layers}layers_b{args.batch}",
-            "launch": "pack+mat-vec as two kernels" if getattr(args, "unfused", False)
-            else "pack fused into the mat-vec (one kernel per projection)",
+            "launch": "pack fused into the mat-vec (one kernel per projection)" if use_fused(args)
+            else "pack+mat-vec as two kernels",
             "layers": layers,
             "projections": [f"{n}:{f}:{r}x{k}" for (n, f, r, k) in synth.STEP_PROJECTIONS],
             "batch": args.batch,
@@ -274,7 +285,7 @@ def run_ours(args):
     from quantised_decode_mat_gb300 import step as qstep
     q.lib()  # fails loudly if the CUDA library is missing
 
-    step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=not args.unfused)
+    step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=use_fused(args))
     nbytes = step.bytes()
     stream = torch.cuda.current_stream()
 
@@ -339,7 +350,8 @@ def run_ours(args):
         "rows_per_s": world * rows_per_step / (ms_max * 1e-3),
         "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm",
-                     "kernel": "qmv_kernel<Q4_K, batch %d, %s>" % (args.batch, "fused pack" if step.fused else "packed input"),
+                     "kernel": "%s<Q4_K, batch %d, %s>" % ("qmv_tc_kernel" if args.batch >= 5 else "qmv_kernel", args.batch,
+                                                            "fused pack" if step.fused else "packed input"),
                      "achieved": ach4, "peak": peak,
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
                      "traffic": profiled_traffic("qmv_q4k"),
@@ -381,7 +393,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--batch", type=int, default=1, choices=range(1, 9))
     ap.add_argument("--unfused", action="store_true",
-                    help="run each projection as qmd_q8k_pack + qmd_qmatvec (two launches)")
+                    help="run each projection as qmd_q8k_pack + qmd_qmatvec (two launches; the default above batch 1)")
+    ap.add_argument("--fused", action="store_true",
+                    help="run each projection as one qmd_qmatvec_x launch (the default at batch 1)")
     ap.add_argument("--layers", type=int, default=32,
                     help="decoder layers in the step (32 for the 7B-shaped step; fewer only for profiling "
                          "captures, which must stay small)")

@@ -135,13 +135,17 @@ def _gen_layer(layer: int, projections, batch: int, seed_fn):
 
 def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STEP_PROJECTIONS,
               device="cuda", seed_fn=synth.step_seed, keep_host_layers=(), threads: int = 8,
-              fused: bool = True) -> DecodeStep:
+              fused: bool | None = None) -> DecodeStep:
     """Generate the seeded weights and activations of a decode step and place them on the device.
 
     keep_host_layers: layers whose canonical GGUF weight bytes stay in host memory (for the
-    oracle).  Q6_K weights are bound (split) on the device."""
+    oracle).  Q6_K weights are bound (split) on the device.  fused: one launch per projection
+    (qmd_qmatvec_x) or pack + mat-vec; None picks the faster, fused at batch 1 only (every CTA
+    of a fused launch packs the whole batch for itself)."""
     import torch
     dev = torch.device(device)
+    if fused is None:
+        fused = batch == 1
     step = DecodeStep(batch=batch, fused=fused)
     x_sizes = [batch * K for (_, _, _, K) in projections] * layers
     y_sizes = [(batch * rows + 3) // 4 * 4 for (_, _, rows, _) in projections] * layers
