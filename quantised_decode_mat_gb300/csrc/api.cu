@@ -86,7 +86,9 @@ unsigned *device_error_word()
     return addr[dev];
 }
 
-// Rows per row group per stage (PR x B <= 8).
+// Rows per row group per stage: 8 (row, vector) slots per warp for one or two vectors, 16
+// above (measured: more rows per stage pay from three vectors up; at two they slowed the
+// 14336-wide Q6_K rows, which then lose the 1024-thread launch bound).
 static int default_rows_per_stage(bool q6, int batch)
 {
     (void)q6;
@@ -95,8 +97,8 @@ static int default_rows_per_stage(bool q6, int batch)
     if (batch == 2)
         return 4;
     if (batch <= 4)
-        return 2;
-    return 1;
+        return 4;
+    return 2;
 }
 
 // Ring depth and CTAs per SM for a stage geometry; false if nothing fits.
@@ -178,15 +180,20 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         }
     }
     // A warp covers 4 blocks of a row, 8 lanes per block; a row takes ceil(nb / 4) warps.
-    const int max_threads = qmv_max_threads(batch, mode);  // the kernels' launch bounds
     const int WR = (nb + 3) / 4;
-    if (WR * 32 > max_threads)
-        return QMD_ERR_SHAPE;
     int PR = g_force_rows.load() > 0 ? g_force_rows.load() : default_rows_per_stage(q6, batch);
     while (PR & (PR - 1))  // the slice kernel is built for 1, 2, 4 or 8 rows
         PR &= PR - 1;
-    while (PR > 1 && PR * batch > 8)
+    while (PR > 1 && PR * batch > 16)
         PR >>= 1;
+    // more than 8 (row, vector) slots per warp lower the launch bound to 512 threads; long rows
+    // keep 8 slots and the 1024-thread bound
+    while (PR > 1 && PR * batch > 8 && WR * 32 > qmv_max_threads(batch, PR, mode))
+        PR >>= 1;
+    const int max_threads = qmv_max_threads(batch, PR, mode);  // the kernel's launch bound
+    if (WR * 32 > max_threads)
+        return QMD_ERR_SHAPE;
+    const int slots = PR * batch > 8 ? 16 : 8;
     // Row groups per CTA: the fused form at batch 1 takes 2 (half as many CTAs, so half the
     // reads of the f32 activations that every CTA packs for itself); otherwise 1.
     int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (fused && batch == 1 ? 2 : 1);
@@ -199,7 +206,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (sb64 > dev.smem_optin)
         return QMD_ERR_SHAPE;
     const int stage_bytes = align_up((int)sb64, 128);
-    const int extra = RG * WR * 8 * 4 + 16;  // partials + counter + barrier per stage
+    const int extra = RG * WR * slots * 4 + 16;  // partials + counter + barrier per stage
     // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
     // matter more than stage depth); capped at launch by the occupancy calculator.
     int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1);
@@ -207,12 +214,12 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         cps = 8;
     if (fused && batch == 1 && g_force_cps.load() <= 0 && cps > 2)
         cps = 2;
-    const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused).total + 64;
+    const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused, slots).total + 64;
     if (!fit_stages(dev, rows, TR, stage_bytes, extra, fixed, cps, pl))
         return QMD_ERR_SHAPE;
     pl->layout = 0;
     pl->threads = RG * WR * 32;
-    pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused).total;
+    pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused, slots).total;
     pl->WR = WR;
     pl->RG = RG;
     pl->PR = PR;

@@ -72,16 +72,18 @@ struct SmemLayout {
     int red_off, cnt_off, bar_off, dx_off, bs_off, acts_off, total;
 };
 
-// Shared memory: ring [stages][stage_bytes] | red f32 [stages][RG][WR][8] | counters u32
+// Shared memory: ring [stages][stage_bytes] | red f32 [stages][RG][WR][slots] | counters u32
 // [stages] | mbarriers u64 [stages] | dx f32 [B][nb] | Q4_K bsums i16 [B][nb][8] | fused form:
-// the packed codes i8 [B][K]
+// the packed codes i8 [B][K].  slots: 8, or 16 when a stage has more than 8 (row, vector)
+// pairs per warp.
 __host__ __device__ inline SmemLayout qmv_smem_layout(int stages, int stage_bytes, int RG, int WR,
-                                                      int B, int nb, bool q6, bool pack = false)
+                                                      int B, int nb, bool q6, bool pack = false,
+                                                      int slots = 8)
 {
     SmemLayout L;
     int o = stages * stage_bytes;
     L.red_off = o;
-    o += stages * RG * WR * 8 * 4;
+    o += stages * RG * WR * slots * 4;
     L.cnt_off = o;
     o = align_up(o + stages * 4, 8);
     L.bar_off = o;
@@ -125,6 +127,24 @@ __device__ __forceinline__ int reduce_scatter(int (&v)[P], int k)
     return s;
 }
 
+// The same for 16 slots: after the three halving steps lane k holds the 8-lane totals of slots
+// 2k and 2k+1 in v[0], v[1].
+__device__ __forceinline__ void reduce_scatter16(int (&v)[16], int k)
+{
+#pragma unroll
+    for (int st = 0; st < 3; ++st) {
+        const int half = 16 >> (st + 1);
+        const int m = 4 >> st;
+        const bool up = k & m;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const int send = up ? v[i] : v[i + half];
+            const int keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+}
+
 __device__ __forceinline__ int dp4a_chain(const uint4 &w, const uint4 &a)
 {
     int s = __dp4a((int)w.x, (int)a.x, 0);
@@ -158,26 +178,29 @@ __device__ __forceinline__ int dp4a_chain_lo(const uint4 &w, const uint4 &a)
     return __dp4a((int)(w.w & 0x0F0F0F0Fu), (int)a.w, s);
 }
 
-// Threads a CTA may have: 1024 for one or two vectors (32 warps cover K = 32768), else 512.
-// The recording variant keeps the lower bound so that it never spills.
-__host__ __device__ constexpr int qmv_max_threads(int B, int mode)
+// Threads a CTA may have: 1024 for one or two vectors with at most 8 (row, vector) slots per
+// warp (32 warps cover K = 32768), else 512.  The recording variant keeps the lower bound so
+// that it never spills.
+__host__ __device__ constexpr int qmv_max_threads(int B, int PR, int mode)
 {
-    return (B <= 2 && mode != QMV_DUMP) ? 1024 : 512;
+    return (B <= 2 && PR * B <= 8 && mode != QMV_DUMP) ? 1024 : 512;
 }
 
 // F is the format: QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT.
 template <int F, int B, int PR, int MODE>
-__global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const QmvKParams p)
+__global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(const QmvKParams p)
 {
     constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
     constexpr bool Q5 = F == QMD_Q5_K;
     constexpr bool DUMP = MODE == QMV_DUMP;
     constexpr bool PACK = MODE == QMV_PACK;
-    constexpr int P = PR * B;                                       // (row, vector) slots
-    static_assert(P >= 1 && P <= 8, "PR x B must be at most 8");
-    constexpr int PP = P > 4 ? 8 : P > 2 ? 4 : P > 1 ? 2 : 1;       // padded to a power of two
-    constexpr int LP = PP == 8 ? 3 : PP == 4 ? 2 : PP == 2 ? 1 : 0;
+    constexpr int P = PR * B;                                               // (row, vector) slots
+    static_assert(P >= 1 && P <= 16, "PR x B must be at most 16");
+    constexpr int PP = P > 8 ? 16 : P > 4 ? 8 : P > 2 ? 4 : P > 1 ? 2 : 1;  // padded to a power of two
+    constexpr int NS = PP > 8 ? 2 : 1;                                      // slots per lane
+    constexpr int LP = PP >= 8 ? 3 : PP == 4 ? 2 : PP == 2 ? 1 : 0;
     constexpr int DUP = 8 >> LP;  // lanes of a block holding the same slot
+    constexpr int SL = 8 * NS;    // block-group sums per warp per stage
     constexpr int BLOCK_BYTES = Q6 ? 208 : Q5 ? 176 : 144;
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -192,7 +215,7 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
     const int64_t r0 = p.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = p.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
     const int nch = (int)((r1 - r0 + TR - 1) / TR);
-    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, RG, WR, B, nb, Q6, PACK);
+    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, RG, WR, B, nb, Q6, PACK, SL);
     float *s_red = reinterpret_cast<float *>(smem + L.red_off);
     unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + L.cnt_off);
     const float *s_dx = reinterpret_cast<const float *>(smem + L.dx_off);
@@ -331,10 +354,17 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
     // bytes 16 (k & 1) ..; a rotation right by these amounts brings each to bit 4 of its byte
     const int q5_rl = (2 * (k >> 1) - 4) & 31, q5_rh = (2 * (k >> 1) - 3) & 31;
 
-    const int slot = k >> (3 - LP);
-    const bool slot_ok = slot < P;
-    const int spr = slot_ok ? slot / B : PR, sv = slot_ok ? slot - (slot / B) * B : 0;
-    const int srow = rg * PR + spr;  // the slot's row within the stage
+    // this lane's slot(s) after the reduce-scatter: k >> (3 - LP), or 2k and 2k+1 for 16
+    int slot[NS], spr[NS], sv[NS], srow[NS];
+    bool slot_ok[NS];
+#pragma unroll
+    for (int e = 0; e < NS; ++e) {
+        slot[e] = NS == 2 ? 2 * k + e : k >> (3 - LP);
+        slot_ok[e] = slot[e] < P;
+        spr[e] = slot_ok[e] ? slot[e] / B : PR;
+        sv[e] = slot_ok[e] ? slot[e] - (slot[e] / B) * B : 0;
+        srow[e] = rg * PR + spr[e];  // the slot's row within the stage
+    }
 
     const unsigned long long wait_ns = p.wait_ns;
 #pragma unroll 1
@@ -459,13 +489,23 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
             }
         }
 
-        // ---- exact block totals, then this lane's slot epilogue ----------------------------
-        const int Sv = reduce_scatter<PP>(S, k);
-        float t = 0.0f;
-        if (blk_ok && slot_ok && srow < nr) {
-            const uint8_t *bp = stage + srow * p.row_stride + blk * BLOCK_BYTES;
-            const float dx = s_dx[sv * nb + blk];
-            const int Sb = (Q6 || Q5) ? Sv : (Sv >> 4);  // exact: Q4_K carried 16 x S
+        // ---- exact block totals, then this lane's slot epilogue(s) -------------------------
+        int Sv[NS];
+        if constexpr (NS == 2) {
+            reduce_scatter16(S, k);
+            Sv[0] = S[0];
+            Sv[NS - 1] = S[1];
+        } else {
+            Sv[0] = reduce_scatter<PP>(S, k);
+        }
+        float t[NS];
+#pragma unroll
+        for (int e = 0; e < NS; ++e) {
+        t[e] = 0.0f;
+        if (blk_ok && slot_ok[e] && srow[e] < nr) {
+            const uint8_t *bp = stage + srow[e] * p.row_stride + blk * BLOCK_BYTES;
+            const float dx = s_dx[sv[e] * nb + blk];
+            const int Sb = (Q6 || Q5) ? Sv[e] : (Sv[e] >> 4);  // exact: Q4_K carried 16 x S
             const float fS = __int2float_rn(Sb);
             int M = 0;
             if (!Q6) {
@@ -474,31 +514,35 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
                 const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
                 const uint32_t m0 = h.z & 0x3F3F3F3Fu;
                 const uint32_t m1 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-                const int4 bs = *reinterpret_cast<const int4 *>(s_bs + (sv * nb + blk) * 8);
+                const int4 bs = *reinterpret_cast<const int4 *>(s_bs + (sv[e] * nb + blk) * 8);
                 M = __dp2a_lo(bs.x, (int)m0, 0);
                 M = __dp2a_hi(bs.y, (int)m0, M);
                 M = __dp2a_lo(bs.z, (int)m1, M);
                 M = __dp2a_hi(bs.w, (int)m1, M);
                 const float fM = __int2float_rn(M);
-                t = __fmul_rn(dx, __fsub_rn(__fmul_rn(d, fS), __fmul_rn(dmin, fM)));
+                t[e] = __fmul_rn(dx, __fsub_rn(__fmul_rn(d, fS), __fmul_rn(dmin, fM)));
             } else {
                 const unsigned short dbits = *reinterpret_cast<const unsigned short *>(
-                    stage + TR * p.row_stride + srow * p.pre_bytes + 2 * blk);
+                    stage + TR * p.row_stride + srow[e] * p.pre_bytes + 2 * blk);
                 const float d = __half2float(__ushort_as_half(dbits));
-                t = __fmul_rn(dx, __fmul_rn(d, fS));
+                t[e] = __fmul_rn(dx, __fmul_rn(d, fS));
             }
             if (DUMP && (k & (DUP - 1)) == 0) {
-                int32_t *sm = p.dbg_sm + ((sv * p.rows + rs + srow) * nb + blk) * 2;
+                int32_t *sm = p.dbg_sm + ((sv[e] * p.rows + rs + srow[e]) * nb + blk) * 2;
                 sm[0] = Sb;
                 sm[1] = M;
             }
         }
+        }
         // blocks 4wr .. 4wr+3 of this warp: (t0 + t1) + (t2 + t3)
-        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 8));
-        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16));
-        float *red = s_red + (size_t)st * RG * WR * 8;
-        if (g == 0)
-            red[(rg * WR + wr) * 8 + k] = t;
+        float *red = s_red + (size_t)st * RG * WR * SL;
+#pragma unroll
+        for (int e = 0; e < NS; ++e) {
+            float te = __fadd_rn(t[e], __shfl_xor_sync(0xffffffffu, t[e], 8));
+            te = __fadd_rn(te, __shfl_xor_sync(0xffffffffu, te, 16));
+            if (g == 0)
+                red[(rg * WR + wr) * SL + NS * k + e] = te;
+        }
         __syncwarp();
 
         // ---- arrive; the last warp of the stage finishes its rows and refills it -----------
@@ -510,20 +554,21 @@ __global__ void __launch_bounds__(qmv_max_threads(B, MODE), 1) qmv_kernel(const 
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence_block();
-            // lane l finishes slot (l % 8) of row group l / 8, four row groups at a time.  The
-            // warps' group sums (one group of four blocks each) are added in runs of four
-            // groups, ((G0 + G1) + G2) + G3 with absent groups as +0, then the runs left to right.
-            for (int rgb = 0; rgb < RG; rgb += 4) {
-                const int frg = rgb + (lane >> 3), fk = lane & 7;
-                const int fslot = fk >> (3 - LP);
+            // entry (row group frg, ri) of the warps' group sums: slot ri (16 slots) or
+            // ri >> (3 - LP) (kept by DUP lanes, the first one counts).  The group sums (four
+            // blocks each) are added in runs of four groups, ((G0 + G1) + G2) + G3 with absent
+            // groups as +0, then the runs left to right.
+            for (int idx = lane; idx < RG * SL; idx += 32) {
+                const int frg = idx / SL, ri = idx - (idx / SL) * SL;
+                const int fslot = NS == 2 ? ri : ri >> (3 - LP);
                 const int frow = frg * PR + (fslot < P ? fslot / B : PR);
-                if (frg < RG && (fk & (DUP - 1)) == 0 && fslot < P && frow < nr) {
-                    const float *rr = red + (frg * WR) * 8 + fk;
+                if ((NS == 2 || (ri & (DUP - 1)) == 0) && fslot < P && frow < nr) {
+                    const float *rr = red + (frg * WR) * SL + ri;
                     float acc = 0.0f;
                     for (int w0 = 0; w0 < WR; w0 += 4) {
-                        float run = rr[w0 * 8];
+                        float run = rr[w0 * SL];
                         for (int w = w0 + 1; w < w0 + 4; ++w)
-                            run = __fadd_rn(run, w < WR ? rr[w * 8] : 0.0f);
+                            run = __fadd_rn(run, w < WR ? rr[w * SL] : 0.0f);
                         acc = w0 == 0 ? run : __fadd_rn(acc, run);
                     }
                     p.y[(fslot - (fslot / B) * B) * p.rows + rs + frow] = acc;
@@ -599,7 +644,7 @@ qmd_status launch_one(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
     return launch_kernel<qmv_kernel<F, B, PR, MODE>>(kp, plan, s);
 }
 
-// Rows per stage and row group (PR x B <= 8); the plan picks one.
+// Rows per stage and row group (PR x B <= 16); the plan picks one.
 template <int F, int B, int MODE>
 qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
@@ -607,15 +652,15 @@ qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s
     case 1:
         return launch_one<F, B, 1, MODE>(kp, plan, s);
     case 2:
-        if constexpr (2 * B <= 8)
+        if constexpr (2 * B <= 16)
             return launch_one<F, B, 2, MODE>(kp, plan, s);
         break;
     case 4:
-        if constexpr (4 * B <= 8)
+        if constexpr (4 * B <= 16)
             return launch_one<F, B, 4, MODE>(kp, plan, s);
         break;
     case 8:
-        if constexpr (B == 1)
+        if constexpr (8 * B <= 16)
             return launch_one<F, B, 8, MODE>(kp, plan, s);
         break;
     }
