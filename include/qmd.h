@@ -277,8 +277,9 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream);
 /*
  * qmd_debug_set_plan -- override the mat-vec launch plan for launches made after the call:
  * row groups per CTA (each ceil(K/1024) warps; capped by the thread limit), rows per row group
- * per stage (rounded down to 1, 2, 4 or 8, then halved until rows x batch <= 8), a cap on
- * pipeline stages, and CTAs per multiprocessor (1..8); 0 keeps the default of each.
+ * per stage (1..8, rounded down to 1, 2, 4 or 8, then halved until rows x batch <= 16), a
+ * cap on pipeline stages (a cap below 3 keeps batches of 5..8 off the tensor-core kernel), and
+ * CTAs per multiprocessor (1..8); 0 keeps the default of each.
  * Results do not depend on the plan; tests use this to drive the stage ring through many
  * wrap-arounds on small inputs.  Process-wide.
  */
