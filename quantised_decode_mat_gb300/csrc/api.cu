@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -41,6 +42,7 @@ qmd_status current_device(DeviceInfo *out)
 {
     static DeviceInfo cache[64];
     static std::atomic<bool> have[64];
+    static std::mutex fill;  // the first call per device fills its entry
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -48,6 +50,11 @@ qmd_status current_device(DeviceInfo *out)
     if (dev < 0 || dev >= 64)
         return QMD_ERR_DEVICE;
     if (!have[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(fill);
+        if (have[dev].load(std::memory_order_acquire)) {
+            *out = cache[dev];
+            return QMD_OK;
+        }
         DeviceInfo d = {};
         d.device = dev;
         if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
@@ -70,20 +77,22 @@ qmd_status current_device(DeviceInfo *out)
 
 unsigned *device_error_word()
 {
-    static unsigned *addr[64];
+    static std::atomic<unsigned *> addr[64];
+    static std::mutex fill;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return nullptr;
-    if (addr[dev] == nullptr) {
+    if (addr[dev].load(std::memory_order_acquire) == nullptr) {
+        std::lock_guard<std::mutex> lock(fill);
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
         if (e != cudaSuccess) {
             fail(QMD_ERR_DEVICE, "cudaGetSymbolAddress(error word)", e);
             return nullptr;
         }
-        addr[dev] = static_cast<unsigned *>(p);
+        addr[dev].store(static_cast<unsigned *>(p), std::memory_order_release);
     }
-    return addr[dev];
+    return addr[dev].load(std::memory_order_acquire);
 }
 
 // Rows per row group per stage: 8 (row, vector) slots per warp for one or two vectors, 16

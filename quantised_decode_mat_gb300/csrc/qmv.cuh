@@ -34,6 +34,8 @@
 //     (bounded) for the CTA's copies in flight, and exits.
 #pragma once
 
+#include <mutex>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -591,23 +593,32 @@ template <auto Kern>
 qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
 {
     auto kern = Kern;
-    static int set_bytes[64] = {0};  // dynamic shared memory opted in, per device
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return QMD_ERR_DEVICE;
-    if (set_bytes[dev] < plan.smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
-        if (e != cudaSuccess)
-            return fail(QMD_ERR_LAUNCH, "qmv smem attribute", e);
-        set_bytes[dev] = plan.smem;
-    }
-    // Persistent grid: no more CTAs than can be resident at once (rows are split by gridDim).
-    int grid = plan.grid;
+    // Per instance: the shared memory opted in per device, and the resident-CTA count per
+    // (device, threads, shared bytes).  Filled on first use; callers may launch from several
+    // host threads, so the tables sit behind a lock (launches themselves do not).
+    struct Occ {
+        int dev, threads, smem, max_ctas;
+    };
+    static std::mutex mu;
+    static int set_bytes[64] = {0};
+    static Occ occ[16] = {};
+    static int n_occ = 0;
+    int cap = 0;
     {
-        // cached per device for the last (threads, shared bytes) this instance was asked for
-        static int c_threads[64] = {0}, c_smem[64] = {0}, c_max[64] = {0};
-        if (c_threads[dev] != plan.threads || c_smem[dev] != plan.smem) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (set_bytes[dev] < plan.smem) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
+            if (e != cudaSuccess)
+                return fail(QMD_ERR_LAUNCH, "qmv smem attribute", e);
+            set_bytes[dev] = plan.smem;
+        }
+        for (int i = 0; i < n_occ && i < 16; ++i)
+            if (occ[i].dev == dev && occ[i].threads == plan.threads && occ[i].smem == plan.smem)
+                cap = occ[i].max_ctas;
+        if (cap == 0) {
             int per_sm = 0, sms = 0;
             cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, plan.threads, plan.smem);
             if (e != cudaSuccess)
@@ -615,13 +626,13 @@ qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t
             if (per_sm < 1)
                 return QMD_ERR_SHAPE;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            c_max[dev] = per_sm * sms;
-            c_threads[dev] = plan.threads;
-            c_smem[dev] = plan.smem;
+            cap = per_sm * sms;
+            occ[n_occ % 16] = Occ{dev, plan.threads, plan.smem, cap};
+            ++n_occ;
         }
-        if (grid > c_max[dev])
-            grid = c_max[dev];
     }
+    // Persistent grid: no more CTAs than can be resident at once (rows are split by gridDim).
+    int grid = plan.grid < cap ? plan.grid : cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)plan.threads);

@@ -420,3 +420,48 @@ def test_tensor_core_extreme_magnitudes(fmtname):
     for v in range(batch):
         for r in (0, 1, 2, 47):
             assert np.array_equal(dots[v, r][:, :8], O.subdots(OFMT[fmtname], Wg[r], oqs[v]))
+
+
+# ---- several host threads, each with its own stream: the same bits as one thread ---------------------
+def test_concurrent_host_threads():
+    import threading
+    shapes = [("q4k", 700, 4096, 1), ("q6k", 300, 14336, 1), ("q5k", 500, 2048, 6), ("q4k", 260, 1280, 3),
+              ("q6k", 90, 3584, 2), ("q4k", 1000, 4096, 8)]
+    jobs = []
+    for i, (f, rows, K, batch) in enumerate(shapes):
+        Wg = synth.weights(f, 60 + i, rows, K)
+        if f == "q6k":
+            W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+        else:
+            W, Wa = dev(Wg.reshape(rows, -1)), None
+        x = dev(synth.activations(60 + i, batch, K))
+        ref = q.qmatvec_x(QFMT[f], W, Wa, x, rows=rows)
+        jobs.append((QFMT[f], W, Wa, x, rows, ref))
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(job):
+        f, W, Wa, x, rows, ref = job
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                outs = []
+                for it in range(30):
+                    if it % 2:
+                        outs.append(q.qmatvec_x(f, W, Wa, x, rows=rows, stream=s))
+                    else:
+                        outs.append(q.qmatvec(f, W, Wa, q.q8k_pack(x, stream=s), rows=rows, stream=s))
+            s.synchronize()
+            for y in outs:
+                if not torch.equal(y.view(torch.int32), ref.view(torch.int32)):
+                    errors.append("differs")
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(j,)) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    q.get_device_error()
+    assert not errors, errors[:3]
