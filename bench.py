@@ -19,7 +19,8 @@ f32 outputs written, once per step (4.419 GB at batch 1).
 Printed (rank 0, one JSON line): the step's algorithmic bytes / time as GB/s (value), the
 same through host buffers (e2e: inputs copied in and outputs copied out every step), the
 dominant kernel's roofline, the oracle's throughput on the host cores (cpu_baseline), SM
-clocks sampled during the timed region, and launch counts.
+clocks sampled during the timed region, launch counts, and (configs) each of configs 0-3 as
+a single mat-vec on packed input, timed apart from the step.
 
 --impl reference times the CPU oracle on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs an independent replica of the step (replicas only; the
@@ -270,6 +271,59 @@ def time_graph(torch, g, reps: int, stream) -> float:
     return e0.elapsed_time(e1) / reps
 
 
+def time_configs(torch, q, device, peak: float) -> dict:
+    """Configs 0-3 as single mat-vecs on packed input (the batches each config names): a
+    CUDA-graph chain of launches rotating over seeded weight copies that together exceed 3 x L2,
+    so every launch reads its weights from HBM.  Bytes per launch as the workload tables count
+    them: weights + q8_K blocks (276 B each) + f32 outputs."""
+    from quantised_decode_mat_gb300 import synth
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    out = {}
+    for cid in (0, 1, 2, 3):
+        c = synth.CONFIGS[cid]
+        rows, K, fmt = c["rows"], c["K"], c["fmt"]
+        nb = K // 256
+        g = torch.from_numpy(synth.weights(fmt, c["seed"], rows, K).reshape(rows, -1)).to(device)
+        if fmt == "q6k":
+            W, Wa = q.bind_q6k(g, rows, K)
+            wbytes, f = rows * nb * 210, q.Q6_K_SPLIT
+        else:
+            W, Wa = g, None
+            wbytes, f = rows * nb * 144, q.Q4_K
+        ncopy = min(2000, max(2, -(-3 * l2 // wbytes)))
+        copies = [(W.clone(), None if Wa is None else Wa.clone()) for _ in range(ncopy)]
+        del g, W, Wa
+        for B in c["batches"]:
+            xq = q.q8k_pack(torch.from_numpy(synth.activations(c["seed"], B, K)).to(device))
+            y = torch.empty((B, rows), dtype=torch.float32, device=device)
+            s = torch.cuda.Stream(device)
+            s.wait_stream(torch.cuda.current_stream(device))
+            with torch.cuda.stream(s):
+                for (Wc, Ac) in copies:  # first launches set kernel attributes outside capture
+                    q.qmatvec(f, Wc, Ac, xq, y, rows, s)
+            torch.cuda.synchronize(device)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                for (Wc, Ac) in copies:
+                    q.qmatvec(f, Wc, Ac, xq, y, rows, s)
+            for _ in range(3):
+                gr.replay()
+            ms = time_graph(torch, gr, 10, torch.cuda.current_stream(device)) / ncopy  # replays go there
+            alg = wbytes + B * nb * 276 + B * rows * 4
+            gbs = alg / (ms * 1e-3) / 1e9
+            info = q.launch_info(f, rows, K, B)
+            out[f"config{cid}_b{B}"] = {
+                "shape": f"{fmt} {rows}x{K} batch {B}", "us_per_launch": ms * 1e3, "gbs": gbs,
+                "frac_of_peak": gbs / peak, "bytes_per_launch": alg, "weight_copies_rotated": ncopy,
+                "kernel": ("qmv_tc_kernel" if info["rows_per_stage"] == 16 and B >= 5 else "qmv_kernel"),
+                "grid": info["grid"], "threads": info["threads"]}
+            del gr
+        del copies
+        torch.cuda.empty_cache()
+    q.get_device_error()
+    return out
+
+
 def run_ours(args):
     import torch
     rank, world, local_rank = dist_env()
@@ -370,6 +424,8 @@ def run_ours(args):
         "gpu_launches": step.launches * args.steps,
     }
     del g, g4, g6, gp, ge
+    if rank == 0 and not args.no_configs:
+        line["configs"] = time_configs(torch, q, torch.device(f"cuda:{local_rank}"), peak)
     if rank == 0 and args.cpu_layers > 0:
         import oracle
         oracle.build()
@@ -399,6 +455,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=32,
                     help="decoder layers in the step (32 for the 7B-shaped step; fewer only for profiling "
                          "captures, which must stay small)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config mat-vec timings (configs 0-3) reported beside the step")
     ap.add_argument("--cpu-layers", type=int, default=8,
                     help="layers of the step the oracle is timed on for cpu_baseline (0: skip)")
     args = ap.parse_args(argv)
