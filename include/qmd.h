@@ -221,6 +221,14 @@ qmd_status qmd_bind_q6k(const void *gguf, void *body, void *prefix, int64_t rows
  */
 qmd_status qmd_bind_q4k(const void *gguf, int64_t rows, int64_t K);
 
+/*
+ * qmd_bind_q5k -- the Q5_K bind is a view as well: the GGUF slab u8 [rows][nb][176] (176 =
+ * 11 x 16 bytes) is read in place.  Copies nothing; checks that the slab can be (16-byte
+ * aligned, K a multiple of 256, size without overflow).
+ * Errors: NULL, K_NOT_MULTIPLE_OF_256, SHAPE, MISALIGNED.
+ */
+qmd_status qmd_bind_q5k(const void *gguf, int64_t rows, int64_t K);
+
 /* Name of a status code (static string). */
 const char *qmd_status_str(qmd_status s);
 

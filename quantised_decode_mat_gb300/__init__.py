@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "qmd_q6k_split_bytes": ([i64, i64, sizep, sizep], i32),
             "qmd_bind_q6k": ([vp, vp, vp, i64, i64, vp], i32),
             "qmd_bind_q4k": ([vp, i64, i64], i32),
+            "qmd_bind_q5k": ([vp, i64, i64], i32),
             "qmd_status_str": ([i32], ctypes.c_char_p),
             "qmd_last_error_detail": ([], ctypes.c_char_p),
             "qmd_get_device_error": ([vp], i32),
@@ -207,6 +208,12 @@ def bind_q6k(gguf, rows: int, K: int, body=None, prefix=None, stream=None):
 def bind_q4k(gguf, rows: int, K: int):
     """qmd_bind_q4k: checks the slab can be read in place as 32-bit words; returns it unchanged."""
     _check(lib().qmd_bind_q4k(_ptr(gguf), rows, K))
+    return gguf
+
+
+def bind_q5k(gguf, rows: int, K: int):
+    """qmd_bind_q5k: checks the slab can be read in place; returns it unchanged."""
+    _check(lib().qmd_bind_q5k(_ptr(gguf), rows, K))
     return gguf
 
 

@@ -449,6 +449,8 @@ qmd_status qmd_bind_q4k(const void *gguf, int64_t rows, int64_t K)
     return QMD_OK;
 }
 
+qmd_status qmd_bind_q5k(const void *gguf, int64_t rows, int64_t K) { return qmd_bind_q4k(gguf, rows, K); }
+
 const char *qmd_status_str(qmd_status s)
 {
     switch (s) {

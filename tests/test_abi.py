@@ -153,3 +153,52 @@ def test_no_gpu_means_a_named_refusal_not_a_fallback(L):
     assert L.qmd_qmatvec_launch_info(q.Q4_K, 4096, 4096, 1, None, None, None, None, None) == 9
     assert st_qmatvec(L) == 9
     assert L.qmd_q8k_pack(A, _xq(), 512, 1, None) == 9
+
+
+def test_bind_q5k_is_a_checked_view(L):
+    assert L.qmd_bind_q5k(A, 4, 512) == 0
+    assert L.qmd_bind_q5k(A + 8, 4, 512) == 5
+    assert L.qmd_bind_q5k(None, 4, 512) == 1
+    assert L.qmd_bind_q5k(A, 0, 512) == 6
+    assert L.qmd_bind_q5k(A, 4, 500) == 3
+
+
+def test_q5k_is_a_known_format_with_q4k_limits(L):
+    # validation passes for Q5_K (no prefix needed), so without a GPU the call reaches the
+    # device check; K above the limits is refused on the host either way
+    st = st_qmatvec(L, fmt=q.Q5_K, Wa=None)
+    assert st in (0, 9, 7)
+    assert st_qmatvec(L, fmt=q.Q5_K, K=500) == 3
+    assert st_qmatvec(L, fmt=q.Q5_K, W=A + 4) == 5
+
+
+def st_rms(L, x=A, r=None, g=A, eps=1e-6, h=None, xq=None, K=512, batch=2):
+    return L.qmd_rmsnorm_q8k_pack(x, r, g, ctypes.c_float(eps), h, xq or _xq(), K, batch, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(g=None), 1), (dict(xq=_xq(qs=None)), 1), (dict(xq=_xq(bs=None)), 1),
+    (dict(K=300), 3), (dict(K=0), 6), (dict(batch=0), 4), (dict(batch=9), 4),
+    (dict(x=A + 4), 5), (dict(r=A + 8), 5), (dict(g=A + 12), 5), (dict(h=A + 4), 5),
+    (dict(xq=_xq(d=A + 2)), 5), (dict(eps=-1e-3), 10), (dict(eps=float("nan")), 10),
+    (dict(eps=float("inf")), 10),
+])
+def test_rmsnorm_pack_refusals(L, kw, status):
+    assert st_rms(L, **kw) == status
+
+
+def test_rmsnorm_pack_valid_arguments_reach_the_device_check(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    assert st_rms(L) == 9
+    assert st_rms(L, r=A, h=A, eps=0.0) == 9
+
+
+def test_fused_entry_point_reaches_the_device_check(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    none = q.Q8KPtrs(None, None, None)
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, A, 16, 512, 1, None) == 9
+    assert L.qmd_qmatvec_x(q.Q5_K, A, None, A, none, A, 16, 512, 8, None) == 9
