@@ -327,7 +327,7 @@ def test_launch_info_shapes():
 FUSED = [("q4k", 256, 2048, 1), ("q4k", 4096, 4096, 1), ("q6k", 4096, 14336, 1), ("q4k", 333, 2048, 4),
          ("q4k", 77, 4352, 5), ("q6k", 64, 3328, 4), ("q6k", 17, 14336, 8), ("q4k", 9, 32768, 1),
          ("q6k", 130, 1792, 3), ("q4k", 1000, 1280, 2), ("q5k", 4096, 4096, 1), ("q5k", 200, 2048, 3),
-         ("q5k", 50, 14336, 8)]
+         ("q5k", 50, 14336, 8), ("q4k", 500, 2048, 8), ("q5k", 300, 4096, 6), ("q4k", 45, 3840, 5)]
 
 
 @pytest.mark.parametrize("fmtname,rows,K,batch", FUSED)
