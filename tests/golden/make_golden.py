@@ -33,6 +33,21 @@ def compute():
         out[f"{name}_y_seq"] = _hex(O.qmatvec(fmt, W, qs, xd, bs, O.ORDER_SEQUENTIAL))
         out[f"{name}_y_grp4"] = _hex(O.qmatvec(fmt, W, qs, xd, bs, O.ORDER_GROUPS_OF_FOUR))
         out[f"{name}_dots_r0_v0"] = _hex(O.subdots(fmt, W[0], qs[0]).astype(np.int32))
+    W5 = synth.weights("q5k", 100, 6, 1024)
+    out["q5k_y_run16"] = _hex(O.qmatvec(O.FMT_Q5_K, W5, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN))
+    out["q5k_dots_r0_v0"] = _hex(O.subdots(O.FMT_Q5_K, W5[0], qs[0]).astype(np.int32))
+    W6 = synth.weights("q6k", 101, 3, 5120)  # 20 blocks: two runs of sixteen
+    x6 = synth.activations(101, 1, 5120)
+    q6, d6, b6 = O.q8k_pack(x6)
+    out["q6k_y_run16_nb20"] = _hex(O.qmatvec(O.FMT_Q6_K, W6, q6, d6, b6, O.ORDER_RUNS_OF_SIXTEEN))
+    xr = synth.activations(102, 1, 512)
+    rr = synth.residual(102, 1, 512)
+    gr = synth.norm_gain(102, 512)
+    h, n = O.rmsnorm(xr, rr, gr, 1e-6)
+    out["rmsnorm_n_first16"] = _hex(n[0, :16])
+    _, rq, rd, rb = O.rmsnorm_q8k_pack(xr, rr, gr, 1e-6)
+    out["rmsnorm_pack_d"] = _hex(rd)
+    out["rmsnorm_pack_bsums"] = [format(int(v) & 0xFFFF, "04x") for v in rb.reshape(-1)]
     return out
 
 
