@@ -465,3 +465,79 @@ def test_concurrent_host_threads():
         t.join(timeout=120)
     q.get_device_error()
     assert not errors, errors[:3]
+
+
+# ---- census: every kernel variant the library can launch, value-checked --------------------------------
+CENSUS = [(f, b, fused, dp4a) for f in ("q4k", "q5k", "q6k") for b in range(1, 9) for fused in (False, True)
+          for dp4a in ((False, True) if (b >= 5 and f != "q6k") else (False,))]
+
+
+@pytest.mark.parametrize("fmtname,batch,fused,dp4a_only", CENSUS,
+                         ids=[f"{f}-b{b}-{'fused' if fu else 'packed'}{'-dp4a' if d else ''}" for f, b, fu, d in CENSUS])
+def test_census_every_variant(fmtname, batch, fused, dp4a_only):
+    """Each (format, batch, fused or packed input, kernel layout) the plan can choose, on a small
+    ragged case, bit-identical to the same-order oracle; plus the recording variant's dots."""
+    rows, K = 45, 1024
+    seed = 1000 + 10 * batch + (3 if fused else 0)
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xd = dev(x)
+    if fmtname == "q6k":
+        W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+    else:
+        W, Wa = dev(Wg.reshape(rows, -1)), None
+    q.debug_set_launch_flags(DP4A_ONLY if dp4a_only else 0)
+    try:
+        buf, y = poisoned_y(batch, rows)
+        if fused:
+            q.qmatvec_x(QFMT[fmtname], W, Wa, xd, y, rows=rows)
+        else:
+            q.qmatvec(QFMT[fmtname], W, Wa, q.q8k_pack(xd), y, rows=rows)
+        q.get_device_error()
+        if not fused:
+            _, dots, _ = q.debug_qmatvec_dump(QFMT[fmtname], W, Wa, q.q8k_pack(xd), rows)
+            q.get_device_error()
+    finally:
+        q.debug_set_launch_flags(0)
+    assert guard_intact(buf, batch, rows)
+    check_against_oracle(fmtname, Wg, x, y.cpu().numpy())
+    if not fused:
+        oqs, _, _ = O.q8k_pack(x)
+        d = dots.cpu().numpy()
+        per = 16 if fmtname == "q6k" else 8
+        for v in range(batch):
+            assert np.array_equal(d[v, rows - 1][:, :per], O.subdots(OFMT[fmtname], Wg[rows - 1], oqs[v]))
+
+
+# ---- a seeded random sweep of small shapes (stands in for a property-based sweep) -------------------------
+def _random_cases(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        f = ("q4k", "q5k", "q6k")[i % 3]
+        nb = int(rng.choice([1, 1, 2, 3, 5, 8, 13, 16, 17, 31, 40, 56]))
+        rows = int(rng.integers(1, 300))
+        batch = int(rng.integers(1, 9))
+        out.append((f, rows, 256 * nb, batch, bool(rng.integers(0, 2)), int(rng.integers(0, 1 << 20))))
+    return out
+
+
+@pytest.mark.parametrize("fmtname,rows,K,batch,fused,seed", _random_cases())
+def test_random_small_shapes(fmtname, rows, K, batch, fused, seed):
+    if batch > 2 and K > 16384:
+        pytest.skip("above the batch's K limit")
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xd = dev(x)
+    if fmtname == "q6k":
+        W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+    else:
+        W, Wa = dev(Wg.reshape(rows, -1)), None
+    buf, y = poisoned_y(batch, rows)
+    if fused:
+        q.qmatvec_x(QFMT[fmtname], W, Wa, xd, y, rows=rows)
+    else:
+        q.qmatvec(QFMT[fmtname], W, Wa, q.q8k_pack(xd), y, rows=rows)
+    q.get_device_error()
+    assert guard_intact(buf, batch, rows)
+    check_against_oracle(fmtname, Wg, x, y.cpu().numpy())
