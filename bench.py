@@ -387,6 +387,21 @@ def run_ours(args):
     b6 = sum(per(p) for p in step.projs if p.fmt == q.Q6_K_SPLIT) / nq6
     bp = nbytes["pack"] / len(step.projs)
 
+    # RMSNorm + residual + pack (qmd_rmsnorm_q8k_pack) on the inputs of the 4096-wide projections
+    # (q|k|v and gate|up read a normalised residual stream in a decode step), a chain of launches
+    rms = [p for p in step.projs if p.K == 4096]
+    gain = torch.full((4096,), 1.0, dtype=torch.float32, device=stream.device)
+    resid = [torch.zeros_like(p.x) for p in rms]
+
+    def run_rms():
+        for p, r in zip(rms, resid):
+            q.rmsnorm_q8k_pack(p.x, r, gain, 1e-6, h_out=r, out=p.xq)
+
+    gr = step.capture(run_rms)
+    gr.replay()
+    msr = time_graph(torch, gr, reps, stream) / len(rms)
+    br = sum(4 * p.x.numel() * 3 + 4 * 4096 + p.xq.batch * (4096 + 16 * 4 + 16 * 16) for p in rms) / len(rms)
+
     # end to end: inputs from pinned host memory in, outputs to pinned host memory out, every step
     x_host = torch.empty(step.x_all.shape, dtype=step.x_all.dtype, pin_memory=True)
     y_host = torch.empty(step.y_all.shape, dtype=step.y_all.dtype, pin_memory=True)
@@ -429,6 +444,10 @@ def run_ours(args):
             "q8k_pack": {"launches_per_step": 0 if step.fused else len(step.projs),
                          "us_per_launch": msp * 1e3, "gbs": bp / (msp * 1e-3) / 1e9,
                          "note": "stand-alone pack kernel, timed as a chain of its launches"},
+            "rmsnorm_q8k_pack": {"launches_per_step": 0, "us_per_launch": msr * 1e3, "gbs": br / (msr * 1e-3) / 1e9,
+                                 "note": "RMSNorm + residual add + pack of a 4096-wide input (x, residual in "
+                                         "place, gain read; codes, scales, sums written), timed as a chain of "
+                                         "its launches beside the step"},
         },
         "e2e": {"value": world * nbytes["algorithmic"] / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": step.x_all.numel() * 4, "d2h_bytes_per_step": step.y_all.numel() * 4,
@@ -436,7 +455,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": step.launches * args.steps,
     }
-    del g, g4, g6, gp, ge
+    del g, g4, g6, gp, ge, gr
     if rank == 0 and not args.no_configs:
         line["configs"] = time_configs(torch, q, torch.device(f"cuda:{local_rank}"), peak)
     if rank == 0 and args.cpu_layers > 0:

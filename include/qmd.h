@@ -22,10 +22,10 @@
  *    launch refusals; "Kernel SPI and the selection algorithm", "Why a kernel declines").
  *  - Layouts are batch-major and row-major; K is the reduction length (columns of W), a
  *    multiple of 256; nb = K / 256.
- *  - Launch order: qmd_q8k_pack and qmd_qmatvec are launched as programmatic dependents of
- *    the preceding kernel in the stream.  Before waiting for that kernel to finish they read
- *    only the weight buffers (W, W_aux); everything else is read and written after it has
- *    finished.  Weights therefore must not be written by the kernel launched immediately
+ *  - Launch order: qmd_q8k_pack, qmd_rmsnorm_q8k_pack and qmd_qmatvec are launched as
+ *    programmatic dependents of the preceding kernel in the stream.  Before waiting for that
+ *    kernel to finish they read only weight buffers (W, W_aux; the norm gain g); everything
+ *    else is read and written after it has finished.  Weights therefore must not be written by the kernel launched immediately
  *    before them in the same stream unless that kernel signals completion only by exiting
  *    (every kernel not written for programmatic launch does; so do this library's bind calls).
  */

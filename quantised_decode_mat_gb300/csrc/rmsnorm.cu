@@ -14,9 +14,13 @@
 // warp combines its 32 partials by xor-shuffles 16, 8, 4, 2, 1 (a pairwise tree); the eight
 // warp totals are added left to right.
 //
-// One CTA per vector.  Phase 1 streams x (and r), writes h when asked and sums the squares;
-// phase 2 normalises and quantises one 256-value block per warp, reading h back (written by
-// this CTA in phase 1) or recomputing it from x and r with the same addition.
+// One CTA per vector.  Phase 1 streams x (and r) -- all of a thread's loads of a round in flight
+// before any store, since h may be the same buffer as x or r -- writes h when asked, keeps it
+// in shared memory when it fits, and sums the squares; phase 2 normalises and quantises one
+// 256-value block per warp from that copy (or re-reads h / recomputes x + r with the same
+// addition for rows too long for shared memory).
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -26,18 +30,35 @@
 namespace qmd {
 
 constexpr int RMS_THREADS = 256;
+constexpr int RMS_SMEM_MAX_K = 16384;  // h kept in shared memory up to this width (64 KB)
 
+template <bool HS>
 __global__ void __launch_bounds__(RMS_THREADS)
     rmsnorm_q8k_pack_kernel(const float *x, const float *r, const float *__restrict__ g, float eps, float *h_out,
                             int8_t *__restrict__ qs, float *__restrict__ d, int16_t *__restrict__ bsums, int64_t K)
 {
     __shared__ float s_part[RMS_THREADS / 32];
     __shared__ float s_inv;
+    extern __shared__ __align__(16) float s_h[];  // HS: h of this vector
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t nb = K / 256;
+    // The gain is a weight: this lane's slice of it for the warp's first GP blocks is fetched
+    // before waiting on the preceding kernel, so its latency overlaps that wait and phase 1.
+    constexpr int GP = 2;
+    float4 gpre[GP][2];
+#pragma unroll
+    for (int j = 0; j < GP; ++j) {
+        const int64_t b = warp + (int64_t)j * (RMS_THREADS / 32);
+        if (b < nb) {
+            gpre[j][0] = *reinterpret_cast<const float4 *>(g + b * 256 + 8 * lane);
+            gpre[j][1] = *reinterpret_cast<const float4 *>(g + b * 256 + 8 * lane + 4);
+        }
+    }
 
     pdl_launch_dependents();
     pdl_wait();  // x and r are produced by earlier work in the stream
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t base = (int64_t)blockIdx.x * K;
     const float *xv = x + base;
     const float *rv = r ? r + base : nullptr;
@@ -45,22 +66,25 @@ __global__ void __launch_bounds__(RMS_THREADS)
 
     // ---- phase 1: h, and this thread's sum of squares (elements tid + 256 j, j ascending) ----
     float p = 0.0f;
-    constexpr int U = 4;  // loads in flight per thread; the adds stay in ascending j
+    constexpr int U = 16;  // loads in flight per thread per round; the adds stay in ascending j
     for (int64_t i0 = tid; i0 < K; i0 += (int64_t)U * RMS_THREADS) {
-        float hu[U];
+        float xu[U], ru[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = i0 + (int64_t)u * RMS_THREADS;
-            if (i < K)
-                hu[u] = rv ? __fadd_rn(xv[i], rv[i]) : xv[i];
+            xu[u] = i < K ? xv[i] : 0.0f;
+            ru[u] = (rv && i < K) ? rv[i] : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = i0 + (int64_t)u * RMS_THREADS;
             if (i < K) {
+                const float hu = rv ? __fadd_rn(xu[u], ru[u]) : xu[u];
                 if (hv)
-                    hv[i] = hu[u];
-                p = __fadd_rn(p, __fmul_rn(hu[u], hu[u]));
+                    hv[i] = hu;
+                if (HS)
+                    s_h[i] = hu;
+                p = __fadd_rn(p, __fmul_rn(hu, hu));
             }
         }
     }
@@ -81,11 +105,15 @@ __global__ void __launch_bounds__(RMS_THREADS)
     const float inv = s_inv;
 
     // ---- phase 2: normalise and quantise, one warp per 256-value block ---------------------
-    const int64_t nb = K / 256;
-    for (int64_t b = warp; b < nb; b += RMS_THREADS / 32) {
+    for (int64_t b = warp, j = 0; b < nb; b += RMS_THREADS / 32, ++j) {
         const int64_t e = b * 256 + 8 * lane;
         float h8[8];
-        if (hv) {
+        if (HS) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(s_h + e);
+            const float4 a1 = *reinterpret_cast<const float4 *>(s_h + e + 4);
+            h8[0] = a0.x; h8[1] = a0.y; h8[2] = a0.z; h8[3] = a0.w;
+            h8[4] = a1.x; h8[5] = a1.y; h8[6] = a1.z; h8[7] = a1.w;
+        } else if (hv) {
             const float4 a0 = *reinterpret_cast<const float4 *>(hv + e);
             const float4 a1 = *reinterpret_cast<const float4 *>(hv + e + 4);
             h8[0] = a0.x; h8[1] = a0.y; h8[2] = a0.z; h8[3] = a0.w;
@@ -104,8 +132,14 @@ __global__ void __launch_bounds__(RMS_THREADS)
                     h8[i] = __fadd_rn(h8[i], c8[i]);
             }
         }
-        const float4 g0 = *reinterpret_cast<const float4 *>(g + e);
-        const float4 g1 = *reinterpret_cast<const float4 *>(g + e + 4);
+        float4 g0, g1;
+        if (j < GP) {
+            g0 = j == 0 ? gpre[0][0] : gpre[1][0];
+            g1 = j == 0 ? gpre[0][1] : gpre[1][1];
+        } else {
+            g0 = *reinterpret_cast<const float4 *>(g + e);
+            g1 = *reinterpret_cast<const float4 *>(g + e + 4);
+        }
         const float g8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float n8[8];
 #pragma unroll
@@ -124,17 +158,36 @@ __global__ void __launch_bounds__(RMS_THREADS)
 qmd_status launch_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, float *h_out,
                                    int8_t *qs, float *d, int16_t *bsums, int64_t K, int batch, cudaStream_t s)
 {
+    const bool hs = K <= RMS_SMEM_MAX_K;
+    if (hs) {
+        // Opt in to 64 KB of dynamic shared memory once per device; host threads may race here.
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return QMD_ERR_DEVICE;
+        static std::mutex mu;
+        static bool opted[64] = {false};
+        std::lock_guard<std::mutex> lock(mu);
+        if (!opted[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(rmsnorm_q8k_pack_kernel<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)(RMS_SMEM_MAX_K * sizeof(float)));
+            if (e != cudaSuccess)
+                return fail(QMD_ERR_LAUNCH, "rmsnorm_q8k_pack smem attribute", e);
+            opted[dev] = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)batch);
     cfg.blockDim = dim3(RMS_THREADS);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = hs ? (size_t)K * sizeof(float) : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_NO_PDL) ? 0 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, rmsnorm_q8k_pack_kernel, x, r, g, eps, h_out, qs, d, bsums, K);
+    cudaError_t e = hs ? cudaLaunchKernelEx(&cfg, rmsnorm_q8k_pack_kernel<true>, x, r, g, eps, h_out, qs, d, bsums, K)
+                       : cudaLaunchKernelEx(&cfg, rmsnorm_q8k_pack_kernel<false>, x, r, g, eps, h_out, qs, d, bsums, K);
     if (e != cudaSuccess)
         return fail(QMD_ERR_LAUNCH, "rmsnorm_q8k_pack launch", e);
     return QMD_OK;

@@ -42,7 +42,9 @@ def check_pack(xq, h_gpu, x, r, g, eps, h_written):
 
 
 CASES = [(1, 256, True, 1e-6), (1, 4096, True, 1e-5), (2, 14336, True, 1e-6), (8, 4096, False, 1e-6),
-         (3, 768, True, 0.0), (5, 2304, False, 0.5), (4, 16384, True, 1e-5), (1, 1280, False, 1e-6)]
+         (3, 768, True, 0.0), (5, 2304, False, 0.5), (4, 16384, True, 1e-5), (1, 1280, False, 1e-6),
+         # wider than 16384: h is not kept in shared memory, phase 2 re-reads or recomputes it
+         (2, 16640, True, 1e-6), (3, 32768, False, 1e-6), (1, 65536, True, 1e-5)]
 
 
 @pytest.mark.parametrize("batch,K,with_r,eps", CASES)
