@@ -95,24 +95,54 @@ unsigned *device_error_word()
     return addr[dev].load(std::memory_order_acquire);
 }
 
-// Rows per row group per stage: 8 (row, vector) slots per warp for one or two vectors, 16
-// above (measured: more rows per stage pay from three vectors up; at two they slowed the
-// 14336-wide Q6_K rows, which then lose the 1024-thread launch bound).
+// Rows per row group per stage: 8 at one or two vectors, 4 at three or four, 2 above (16 (row,
+// vector) slots per warp from two vectors up; measured on the 7B shapes with the CTA counts
+// chosen below).
 static int default_rows_per_stage(bool q6, int batch)
 {
     (void)q6;
-    if (batch == 1)
+    if (batch <= 2)
         return 8;
-    if (batch == 2)
-        return 4;
     if (batch <= 4)
         return 4;
     return 2;
 }
 
+// Registers per thread of a dp4a kernel instance, looked up once per (format, batch, rows per
+// stage, mode); if the lookup fails, the launch bound's worst case.
+static int kernel_regs(int fmt, int batch, int PR, int mode)
+{
+    static std::atomic<int> cache[3][QMD_MAX_BATCH + 1][4][3];
+    const int fi = fmt == QMD_Q6_K_SPLIT ? 2 : fmt == QMD_Q5_K ? 1 : 0;
+    const int pi = PR >= 8 ? 3 : PR >= 4 ? 2 : PR >= 2 ? 1 : 0;
+    if (batch < 1 || batch > QMD_MAX_BATCH || mode < 0 || mode > 2)
+        return 65536 / qmv_max_threads(batch, PR, mode);
+    std::atomic<int> &slot = cache[fi][batch][pi][mode];
+    int r = slot.load();
+    if (r == 0) {
+        r = fi == 2 ? qmv_regs_q6k(batch, PR, mode) : fi == 1 ? qmv_regs_q5k(batch, PR, mode)
+                                                     : qmv_regs_q4k(batch, PR, mode);
+        if (r <= 0)
+            r = 65536 / qmv_max_threads(batch, PR, mode);
+        slot.store(r);
+    }
+    return r;
+}
+
+// CTAs of `threads` threads that fit on an SM by registers (allocated per thread in units of 8)
+// and by threads.
+static int reg_cap_ctas(int regs, int threads)
+{
+    const int r = (regs + 7) & ~7;
+    int cap = 65536 / (r * threads);
+    if (cap > 2048 / threads)
+        cap = 2048 / threads;
+    return cap < 1 ? 1 : cap;
+}
+
 // Ring depth and CTAs per SM for a stage geometry; false if nothing fits.
 static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_bytes, int per_stage_extra,
-                       int fixed, int cps, QmvPlan *pl)
+                       int fixed, int cps, int max_stages, QmvPlan *pl)
 {
     for (; cps >= 1; --cps) {
         int budget = dev.smem_per_sm / cps - 1024;
@@ -124,8 +154,8 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
         const int64_t rows_per_cta = (rows + grid - 1) / grid;
         const int64_t chunks = (rows_per_cta + TR - 1) / TR;
         int64_t stages = (budget - fixed) / (stage_bytes + per_stage_extra);
-        if (stages > 8)
-            stages = 8;
+        if (stages > max_stages)
+            stages = max_stages;
         if (stages > chunks)
             stages = chunks;
         if (g_force_stages.load() > 0 && stages > g_force_stages.load())
@@ -203,9 +233,57 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (WR * 32 > max_threads)
         return QMD_ERR_SHAPE;
     const int slots = PR * batch > 8 ? 16 : 8;
-    // Row groups per CTA: the fused form at batch 1 takes 2 (half as many CTAs, so half the
-    // reads of the f32 activations that every CTA packs for itself); otherwise 1.
-    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : (fused && batch == 1 ? 2 : 1);
+    // Row groups per CTA: 1, except in the fused form at batch 1 (below).
+    int RG = g_force_rg.load() > 0 ? g_force_rg.load() : 1;
+    // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
+    // matter more than stage depth); capped at launch by the occupancy calculator.
+    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : 0;
+    const int64_t per_sm = (rows + dev.sm_count - 1) / dev.sm_count;
+    if (fused && batch == 1) {
+        // Every CTA packs the whole f32 vector for itself, after the dependency wait, so the
+        // pack's latency is on the critical path of every launch.  Measured on the 7B shapes:
+        //  * few rows per SM (up to two 8-row stages per row group): wide CTAs of at least 16
+        //    warps (two row groups at least), each streaming its rows as one chunk, one or two
+        //    CTAs per SM -- the pack then costs one block per warp;
+        //  * many rows per SM: 8-warp CTAs, about 32 warps per SM, several chunks each;
+        //  * a stage of at most 96 KB, so that two fit in an SM's shared memory.
+        int rg_small = 16 / WR > 2 ? 16 / WR : 2;
+        if (rg_small * WR * 32 > max_threads)
+            rg_small = max_threads / (WR * 32);
+        if (rg_small < 1)
+            rg_small = 1;
+        const bool small = per_sm <= 2 * rg_small * 8;
+        if (g_force_rg.load() <= 0)
+            RG = small ? rg_small : (8 / WR > 1 ? 8 / WR : 1);
+        if (g_force_rows.load() <= 0)
+            while (PR > 1 && (int64_t)RG * PR * (row_bytes + pre_bytes) > 96 * 1024)
+                PR >>= 1;
+        if (cps <= 0) {
+            const int rgc = RG < max_threads / (WR * 32) ? RG : max_threads / (WR * 32);
+            const int tr = rgc * PR;
+            cps = small ? (int)((per_sm + tr - 1) / (tr > 0 ? tr : 1)) : 32 / (rgc * WR);
+            const int cap = reg_cap_ctas(kernel_regs(fmt, batch, PR, mode), rgc * WR * 32);
+            if (cps > cap)
+                cps = cap;
+            if (cps < 1)
+                cps = 1;
+        }
+    } else if (batch <= 4) {
+        // Packed input, one to four vectors: 8-warp CTAs (one row group per 8 warps of a row), as
+        // many per SM as the registers allow but no more than it takes for each CTA to stream
+        // its rows as one chunk (measured on the 7B shapes at batches 1, 2 and 4).
+        if (g_force_rg.load() <= 0)
+            RG = 8 / WR > 1 ? 8 / WR : 1;
+        if (cps <= 0) {
+            const int rgc = RG < max_threads / (WR * 32) ? RG : max_threads / (WR * 32);
+            const int tr = (rgc > 0 ? rgc : 1) * PR;
+            const int64_t want = (per_sm + tr - 1) / tr;
+            const int cap = reg_cap_ctas(kernel_regs(fmt, batch, PR, mode), (rgc > 0 ? rgc : 1) * WR * 32);
+            cps = want < cap ? (int)want : cap;
+            if (cps < 1)
+                cps = 1;
+        }
+    }
     if (RG * WR * 32 > max_threads)
         RG = max_threads / (WR * 32);
     if (RG < 1)
@@ -216,15 +294,16 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         return QMD_ERR_SHAPE;
     const int stage_bytes = align_up((int)sb64, 128);
     const int extra = RG * WR * slots * 4 + 16;  // partials + counter + barrier per stage
-    // CTAs per SM: about 32 warps per SM (the kernel is bound by instruction latency, so warps
-    // matter more than stage depth); capped at launch by the occupancy calculator.
-    int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1);
+    if (cps <= 0)
+        cps = 32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1;
     if (cps > 8)
         cps = 8;
-    if (fused && batch == 1 && g_force_cps.load() <= 0 && cps > 2)
-        cps = 2;
     const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused, slots).total + 64;
-    if (!fit_stages(dev, rows, TR, stage_bytes, extra, fixed, cps, pl))
+    // Ring depth: up to 8 stages, but 2 for two to four vectors -- bulk copies in flight together
+    // share the SM's bandwidth, so a deeper ring delays its first stage, and the dot products,
+    // with little headroom over the copies, never catch up (measured on the 7B shapes).
+    const int max_stages = (g_force_stages.load() <= 0 && batch >= 2 && batch <= 4) ? 2 : 8;
+    if (!fit_stages(dev, rows, TR, stage_bytes, extra, fixed, cps, max_stages, pl))
         return QMD_ERR_SHAPE;
     pl->layout = 0;
     pl->threads = RG * WR * 32;

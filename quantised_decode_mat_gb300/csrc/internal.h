@@ -74,6 +74,10 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
 qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 qmd_status launch_qmv_q5k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
 qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s);
+// Registers per thread of the dp4a kernel instance (batch, rows per stage, mode); 0 if unknown.
+int qmv_regs_q4k(int batch, int PR, int mode);
+int qmv_regs_q5k(int batch, int PR, int mode);
+int qmv_regs_q6k(int batch, int PR, int mode);
 
 // ---- pack, bind, debug ---------------------------------------------------------------------
 qmd_status launch_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, float eps, float *h_out,

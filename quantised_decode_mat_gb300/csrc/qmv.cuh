@@ -678,6 +678,59 @@ qmd_status launch_rows(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s
     return QMD_ERR_SHAPE;
 }
 
+// Registers per thread of one instance (the plan sizes CTAs per SM by them); 0 if unknown.
+template <int F, int B, int MODE>
+int instance_regs(int PR)
+{
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (PR) {
+    case 1:
+        e = cudaFuncGetAttributes(&fa, qmv_kernel<F, B, 1, MODE>);
+        break;
+    case 2:
+        if constexpr (2 * B <= 16)
+            e = cudaFuncGetAttributes(&fa, qmv_kernel<F, B, 2, MODE>);
+        break;
+    case 4:
+        if constexpr (4 * B <= 16)
+            e = cudaFuncGetAttributes(&fa, qmv_kernel<F, B, 4, MODE>);
+        break;
+    case 8:
+        if constexpr (8 * B <= 16)
+            e = cudaFuncGetAttributes(&fa, qmv_kernel<F, B, 8, MODE>);
+        break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return fa.numRegs;
+}
+
+template <int F>
+int qmv_slice_regs(int batch, int PR, int mode)
+{
+#define QMD_CASE(BB)                                                                                 \
+    case BB:                                                                                         \
+        return mode == QMV_PACK   ? instance_regs<F, BB, QMV_PACK>(PR)                               \
+               : mode == QMV_DUMP ? instance_regs<F, BB, QMV_DUMP>(PR)                               \
+                                  : instance_regs<F, BB, QMV_PLAIN>(PR);
+    switch (batch) {
+        QMD_CASE(1)
+        QMD_CASE(2)
+        QMD_CASE(3)
+        QMD_CASE(4)
+        QMD_CASE(5)
+        QMD_CASE(6)
+        QMD_CASE(7)
+        QMD_CASE(8)
+    default:
+        return 0;
+    }
+#undef QMD_CASE
+}
+
 // Kernel parameters from the call's arguments and the plan; mode is the kernel variant.
 inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams &kp, int &mode)
 {

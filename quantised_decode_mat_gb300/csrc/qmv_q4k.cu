@@ -15,4 +15,6 @@ qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     return launch_qmv_slice<QMD_Q4_K>(kp, plan, a.batch, mode, s);
 }
 
+int qmv_regs_q4k(int batch, int PR, int mode) { return qmv_slice_regs<QMD_Q4_K>(batch, PR, mode); }
+
 }  // namespace qmd

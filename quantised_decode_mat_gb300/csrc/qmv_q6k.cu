@@ -14,4 +14,6 @@ qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     return launch_qmv_slice<QMD_Q6_K_SPLIT>(kp, plan, a.batch, mode, s);
 }
 
+int qmv_regs_q6k(int batch, int PR, int mode) { return qmv_slice_regs<QMD_Q6_K_SPLIT>(batch, PR, mode); }
+
 }  // namespace qmd
