@@ -5,10 +5,11 @@
 A step is one pass of the whole hot path over one batch of synthetic input: for each of 32
 layers and each projection {q|k|v Q4_K 6144x4096, o Q4_K 4096x4096, gate|up Q4_K 28672x4096,
 down Q6_K 4096x14336}, the q8_K pack of that projection's activation and the mat-vec of its
-weight.  By default (and with --fused) a batch of one vector runs one launch per projection
-(qmd_qmatvec_x, which packs inside the kernel); larger batches, or --unfused, run
-qmd_q8k_pack followed by qmd_qmatvec (every CTA of a fused launch packs the whole batch for
-itself, which costs more than the extra launch once there are two or more vectors).  Each launch depends on the
+weight.  By default a batch of one vector runs one launch per projection of 4096-wide rows
+(qmd_qmatvec_x, which packs inside the kernel) and qmd_q8k_pack followed by qmd_qmatvec for
+the 14336-wide down projection and for larger batches (every CTA of a fused launch packs the
+whole input for itself, which costs more than the extra launch once the input is long or holds
+two or more vectors); --fused and --unfused force one form everywhere.  Each launch depends on the
 previous one in stream order, as in a real decode where a projection's input comes from the
 layer before.  The step's launches are captured once into a CUDA graph and replayed.  Weights
 (4.41 GB) exceed L2 many times over, so consecutive steps read them from HBM.
@@ -248,21 +249,33 @@ def run_reference(args):
     return 0
 
 
-def use_fused(args) -> bool:
-    """One launch per projection at batch 1, pack + mat-vec above, unless a flag says otherwise."""
+def use_fused(args):
+    """True / False when a flag forces one launch form everywhere; None for the per-projection
+    default (quantised_decode_mat_gb300.step.fuse_pack)."""
     if getattr(args, "fused", False):
         return True
     if getattr(args, "unfused", False):
         return False
-    return args.batch == 1
+    return None
+
+
+def launch_form(args) -> str:
+    from quantised_decode_mat_gb300 import synth
+    from quantised_decode_mat_gb300.step import fuse_pack
+    f = use_fused(args)
+    fused = [n for (n, _, _, K) in synth.STEP_PROJECTIONS if (fuse_pack(args.batch, K) if f is None else f)]
+    if len(fused) == len(synth.STEP_PROJECTIONS):
+        return "pack fused into the mat-vec (one kernel per projection)"
+    if not fused:
+        return "pack+mat-vec as two kernels"
+    return f"pack fused into the mat-vec for {', '.join(fused)}; pack+mat-vec as two kernels for the rest"
 
 
 def workload_config(args):
     from quantised_decode_mat_gb300 import synth
     layers = getattr(args, "layers", synth.STEP_LAYERS)
     return {"workload": f"decode_step_7b_q4k_q6k_{layers}layers_b{args.batch}",
-            "launch": "pack fused into the mat-vec (one kernel per projection)" if use_fused(args)
-            else "pack+mat-vec as two kernels",
+            "launch": launch_form(args),
             "layers": layers,
             "projections": [f"{n}:{f}:{r}x{k}" for (n, f, r, k) in synth.STEP_PROJECTIONS],
             "batch": args.batch,
@@ -382,7 +395,8 @@ def run_ours(args):
     ms4 = time_graph(torch, g4, reps, stream) / nq4
     ms6 = time_graph(torch, g6, reps, stream) / nq6
     msp = time_graph(torch, gp, reps, stream) / len(step.projs)
-    per = (lambda p: p.algorithmic_bytes()) if step.fused else (lambda p: p.matvec_bytes())
+    per = lambda p: p.algorithmic_bytes() if p.fused else p.matvec_bytes()
+    q4_fused = all(p.fused for p in step.projs if p.fmt == q.Q4_K)
     b4 = sum(per(p) for p in step.projs if p.fmt == q.Q4_K) / nq4
     b6 = sum(per(p) for p in step.projs if p.fmt == q.Q6_K_SPLIT) / nq6
     bp = nbytes["pack"] / len(step.projs)
@@ -433,7 +447,7 @@ def run_ours(args):
         "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm",
                      "kernel": "%s<Q4_K, batch %d, %s>" % ("qmv_tc_kernel" if args.batch >= 5 else "qmv_kernel", args.batch,
-                                                            "fused pack" if step.fused else "packed input"),
+                                                            "fused pack" if q4_fused else "packed input"),
                      "achieved": ach4, "peak": peak,
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
                      "traffic": profiled_traffic("qmv_q4k"),
@@ -441,7 +455,7 @@ def run_ours(args):
         "kernels": {
             "qmv_q4k": {"launches_per_step": nq4, "us_per_launch": ms4 * 1e3, "gbs": ach4},
             "qmv_q6k": {"launches_per_step": nq6, "us_per_launch": ms6 * 1e3, "gbs": b6 / (ms6 * 1e-3) / 1e9},
-            "q8k_pack": {"launches_per_step": 0 if step.fused else len(step.projs),
+            "q8k_pack": {"launches_per_step": sum(1 for p in step.projs if not p.fused),
                          "us_per_launch": msp * 1e3, "gbs": bp / (msp * 1e-3) / 1e9,
                          "note": "stand-alone pack kernel, timed as a chain of its launches"},
             "rmsnorm_q8k_pack": {"launches_per_step": 0, "us_per_launch": msr * 1e3, "gbs": br / (msr * 1e-3) / 1e9,

@@ -36,6 +36,7 @@ class Projection:
     xq: Q8K
     y: "object"            # device f32 [B, rows] (view into DecodeStep.y_all)
     weight_bytes: int
+    fused: bool = True     # one launch that packs inside the mat-vec, or pack + mat-vec
 
     def act_bytes(self) -> int:
         """q8_K bytes the mat-vec reads: codes + scale (+ the eight sums for Q4_K) per block."""
@@ -60,6 +61,20 @@ class Projection:
         return self.weight_bytes + B * self.K * 4 + B * self.rows * 4
 
 
+# Longest row (values) whose q8_K pack the default step fuses into the mat-vec.
+FUSE_MAX_K = 8192
+
+
+def fuse_pack(batch: int, K: int) -> bool:
+    """Default launch form of a projection: one launch that packs inside the mat-vec
+    (qmd_qmatvec_x) for a single vector and rows of at most FUSE_MAX_K values; the stand-alone
+    pack followed by the mat-vec otherwise.  Every CTA of a fused launch packs the whole input
+    for itself after the dependency wait, which costs more than a second launch once the input
+    is long (the 14336-wide down projection: 36.9 against 38.0 us per layer) or holds several
+    vectors (measured on the 7B shapes)."""
+    return batch == 1 and K <= FUSE_MAX_K
+
+
 @dataclass
 class DecodeStep:
     batch: int
@@ -67,11 +82,17 @@ class DecodeStep:
     x_all: "object" = None
     y_all: "object" = None
     host_weights: dict = field(default_factory=dict)  # (layer, name) -> canonical GGUF bytes, if kept
-    fused: bool = True  # one launch per projection (qmd_qmatvec_x) or pack + mat-vec
+
+    @property
+    def form(self) -> str:
+        """'fused' (every projection one launch), 'two-kernel' (pack + mat-vec everywhere) or
+        'mixed'."""
+        f = {p.fused for p in self.projs}
+        return "fused" if f == {True} else "two-kernel" if f == {False} else "mixed"
 
     def run(self, stream=None) -> None:
         for p in self.projs:
-            if self.fused:
+            if p.fused:
                 qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
             else:
                 q8k_pack(p.x, p.xq, stream)
@@ -82,7 +103,7 @@ class DecodeStep:
         n = 0
         for p in self.projs:
             if fmt is None or p.fmt == fmt:
-                if self.fused:
+                if p.fused:
                     qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
                 else:
                     qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
@@ -111,7 +132,7 @@ class DecodeStep:
 
     @property
     def launches(self) -> int:
-        return (1 if self.fused else 2) * len(self.projs)
+        return sum(1 if p.fused else 2 for p in self.projs)
 
     def bytes(self) -> dict:
         """algorithmic: weights + f32 activations + f32 outputs of every projection (the
@@ -139,14 +160,12 @@ def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STE
     """Generate the seeded weights and activations of a decode step and place them on the device.
 
     keep_host_layers: layers whose canonical GGUF weight bytes stay in host memory (for the
-    oracle).  Q6_K weights are bound (split) on the device.  fused: one launch per projection
-    (qmd_qmatvec_x) or pack + mat-vec; None picks the faster, fused at batch 1 only (every CTA
-    of a fused launch packs the whole batch for itself)."""
+    oracle).  Q6_K weights are bound (split) on the device.  fused: True for one launch per
+    projection (qmd_qmatvec_x), False for pack + mat-vec, None for the faster of the two per
+    projection (fuse_pack)."""
     import torch
     dev = torch.device(device)
-    if fused is None:
-        fused = batch == 1
-    step = DecodeStep(batch=batch, fused=fused)
+    step = DecodeStep(batch=batch)
     x_sizes = [batch * K for (_, _, _, K) in projections] * layers
     y_sizes = [(batch * rows + 3) // 4 * 4 for (_, _, rows, _) in projections] * layers
     step.x_all = torch.empty(sum(x_sizes), dtype=torch.float32, device=dev)
@@ -176,7 +195,7 @@ def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STE
                 if l in keep_host_layers:
                     step.host_weights[(l, name)] = Wh
                 step.projs.append(Projection(name, l, qfmt, rows, K, W, Wa, x, Q8K.empty(batch, K, dev), y,
-                                             wbytes))
+                                             wbytes, fuse_pack(batch, K) if fused is None else bool(fused)))
     torch.cuda.synchronize(dev)
     return step
 
