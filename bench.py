@@ -422,9 +422,7 @@ def run_ours(args):
     x_host.copy_(step.x_all)
 
     def e2e_step():
-        step.x_all.copy_(x_host, non_blocking=True)
-        step.run()
-        y_host.copy_(step.y_all, non_blocking=True)
+        step.run_through_host(x_host, y_host)
 
     ge = step.capture(e2e_step)
     for _ in range(max(1, args.warmup)):

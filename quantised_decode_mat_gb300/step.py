@@ -110,6 +110,67 @@ class DecodeStep:
                 n += 1
         return n
 
+    def run_through_host(self, x_host, y_host, chunks: int = 4) -> None:
+        """One step with its inputs copied in from pinned host memory (x_host, shaped like
+        x_all) and its outputs copied out (y_host, shaped like y_all), the copies overlapped
+        with the mat-vecs on two side streams: layer 0's inputs first, then the other layers';
+        the outputs in `chunks` groups of layers, each as soon as its group has run.  The
+        current stream waits for every copy before it continues."""
+        import torch
+        cur = torch.cuda.current_stream()
+        if not hasattr(self, "_copy_streams"):
+            self._copy_streams = (torch.cuda.Stream(), torch.cuda.Stream())
+        h2d, d2h = self._copy_streams
+        layers = sorted({p.layer for p in self.projs})
+        span = {l: [p for p in self.projs if p.layer == l] for l in layers}
+
+        def x_range(ls):
+            ps = [p for l in ls for p in span[l]]
+            lo = ps[0].x.data_ptr() - self.x_all.data_ptr()
+            hi = ps[-1].x.data_ptr() + ps[-1].x.numel() * 4 - self.x_all.data_ptr()
+            return lo // 4, hi // 4
+
+        def y_range(ls):
+            ps = [p for l in ls for p in span[l]]
+            lo = ps[0].y.data_ptr() - self.y_all.data_ptr()
+            hi = ps[-1].y.data_ptr() + ps[-1].y.numel() * 4 - self.y_all.data_ptr()
+            return lo // 4, hi // 4
+
+        h2d.wait_stream(cur)
+        d2h.wait_stream(cur)
+        x_ready = []
+        with torch.cuda.stream(h2d):
+            for ls in (layers[:1], layers[1:]):
+                if ls:
+                    a, b = x_range(ls)
+                    self.x_all[a:b].copy_(x_host[a:b], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(h2d)
+                    x_ready.append(e)
+        n = len(layers)
+        groups = [g for g in (layers[k * n // chunks:(k + 1) * n // chunks] for k in range(chunks)) if g]
+        for i, l in enumerate(layers):
+            if i < 2 and i < len(x_ready):
+                cur.wait_event(x_ready[i])
+            for p in span[l]:
+                if p.fused:
+                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=cur)
+                else:
+                    q8k_pack(p.x, p.xq, cur)
+                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, cur)
+            for g in groups:
+                if g[-1] == l:
+                    done = torch.cuda.Event()
+                    done.record(cur)
+                    d2h.wait_event(done)
+                    a, b = y_range(g)
+                    if g is groups[-1]:
+                        b = self.y_all.numel()  # through the last output's padding
+                    with torch.cuda.stream(d2h):
+                        y_host[a:b].copy_(self.y_all[a:b], non_blocking=True)
+        cur.wait_stream(h2d)
+        cur.wait_stream(d2h)
+
     def run_packs(self, stream=None) -> int:
         for p in self.projs:
             q8k_pack(p.x, p.xq, stream)
