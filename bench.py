@@ -147,6 +147,45 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def alu_roofline(q, step, batch: int, ms_per_launch: float, dp4a_rate: float, mma_rate: float) -> dict:
+    """The Q4_K mat-vec against the measured issue rate of the unit doing its multiply-adds:
+    dp4a (64 per 256-value block-row per vector) on the dp4a kernel, or mma.sync (one
+    m16n8k16, 4096 FLOP with the batch padded to 8, per block-row) on the tensor-core kernel."""
+    q4 = [p for p in step.projs if p.fmt == q.Q4_K]
+    block_rows = sum(p.rows * (p.K // 256) for p in q4) / len(q4)
+    info = q.launch_info(q.Q4_K, q4[0].rows, q4[0].K, batch)
+    tc = batch >= 5 and info["rows_per_stage"] == 16
+    if tc:
+        ops, peak, unit, op = block_rows * 4096.0, mma_rate, "TFLOP/s", "mma.sync.m16n8k16 f16->f32"
+    else:
+        ops, peak, unit, op = block_rows * 64.0 * batch, dp4a_rate, "Tdp4a/s", "dp4a"
+    achieved = ops / (ms_per_launch * 1e-3)
+    return {"bound": "alu", "kernel": "qmv_tc_kernel" if tc else "qmv_kernel", "op": op,
+            "achieved": achieved / 1e12, "peak": peak / 1e12, "unit": unit, "frac": achieved / peak,
+            "ops_per_launch": ops, "peak_kind": "measured (qmd_measure_alu, register-only kernels)"}
+
+
 def gpu_uuid(torch, dev_index: int):
     try:
         u = str(torch.cuda.get_device_properties(dev_index).uuid)
@@ -242,7 +281,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 dot / f32 epilogue",
         "data": "synthetic", "config": workload_config(args),
-        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": ncores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": ncores, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -366,6 +406,7 @@ def run_ours(args):
     q.lib()  # fails loudly if the CUDA library is missing
 
     step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=use_fused(args))
+    dp4a_rate, mma_rate = q.measure_alu()  # before the timed region
     nbytes = step.bytes()
     stream = torch.cuda.current_stream()
 
@@ -442,7 +483,12 @@ def run_ours(args):
         "config": workload_config(args),
         "pct_of_peak": {"of_" + peak_kind: gbs / world / peak, "of_nominal_8TBps": gbs / world / NOMINAL_HBM_GBS},
         "rows_per_s": world * rows_per_step / (ms_max * 1e-3),
+        "row_vectors_per_s": world * rows_per_step * args.batch / (ms_max * 1e-3),
         "bytes_per_step": nbytes,
+        "gbs_by_bytes": {"algorithmic": gbs,
+                         "weights_only": world * nbytes["weights"] / (ms_max * 1e-3) / 1e9,
+                         "matvec_only": world * nbytes["matvec"] / (ms_max * 1e-3) / 1e9,
+                         "pack_inclusive": world * (nbytes["matvec"] + nbytes["pack"]) / (ms_max * 1e-3) / 1e9},
         "roofline": {"bound": "hbm",
                      "kernel": "%s<Q4_K, batch %d, %s>" % ("qmv_tc_kernel" if args.batch >= 5 else "qmv_kernel", args.batch,
                                                             "fused pack" if q4_fused else "packed input"),
@@ -450,6 +496,7 @@ def run_ours(args):
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
                      "traffic": profiled_traffic("qmv_q4k"),
                      "algorithmic_bytes_per_launch": b4, "ms_per_launch": ms4},
+        "alu_roofline": alu_roofline(q, step, args.batch, ms4, dp4a_rate, mma_rate),
         "kernels": {
             "qmv_q4k": {"launches_per_step": nq4, "us_per_launch": ms4 * 1e3, "gbs": ach4},
             "qmv_q6k": {"launches_per_step": nq6, "us_per_launch": ms6 * 1e3, "gbs": b6 / (ms6 * 1e-3) / 1e9},
@@ -481,7 +528,8 @@ def run_ours(args):
                                 "sample": f"layers 0-{args.cpu_layers - 1} of 32, all four projections, batch "
                                           f"{args.batch}: oracle q8_K pack + mat-vec, rows split over {ncores} "
                                           f"threads, 4 passes, {tsecs:.1f} s wall",
-                                "single_thread": {"value": ob / secs / 1e9, "cores": 1, "seconds": secs}}
+                                "single_thread": {"value": ob / secs / 1e9, "cores": 1, "seconds": secs},
+                                "cpu_model": cpu_model()}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

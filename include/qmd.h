@@ -276,6 +276,15 @@ qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux,
                                   int32_t *sm, void *stream);
 
 /*
+ * qmd_measure_alu -- this device's issue rates for the two exact multiply-add paths of the
+ * mat-vec, for an ALU roofline beside the HBM one: dp4a instructions per second (each sums
+ * four int8 x int8 products into an int32; counted per thread) and f16 tensor FLOP/s through
+ * mma.sync.m16n8k16 with f32 accumulation.  Two register-only kernels of a few milliseconds
+ * on a private stream; the call waits for them.  Errors: NULL (either pointer), DEVICE, LAUNCH.
+ */
+qmd_status qmd_measure_alu(double *dp4a_per_s, double *mma_flop_per_s);
+
+/*
  * qmd_debug_wait_timeout -- launches one CTA that waits, with the given limit, on a
  * shared-memory barrier that nothing completes; the wait gives up, sets the device error
  * word and the kernel returns.  Used to test the bounded-wait path without hanging a GPU.

@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "qmd_qmatvec_launch_info": ([i32, i64, i64, i32, ip, ip, ip, ip, ip], i32),
             "qmd_debug_qmatvec_dump": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp, vp], i32),
             "qmd_debug_wait_timeout": ([u64, vp], i32),
+            "qmd_measure_alu": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], i32),
             "qmd_debug_set_plan": ([i32, i32, i32, i32], None),
             "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
             "qmd_version": ([], i32),
@@ -248,6 +249,13 @@ def debug_qmatvec_dump(fmt: int, W, W_aux, xq: Q8K, rows: int | None = None, str
     _check(lib().qmd_debug_qmatvec_dump(fmt, _ptr(W), _ptr(W_aux), xq.ptrs(), _ptr(y), rows, xq.K,
                                         xq.batch, _ptr(dots), _ptr(sm), _stream(stream)))
     return y, dots, sm
+
+
+def measure_alu() -> tuple[float, float]:
+    """qmd_measure_alu: (dp4a instructions/s, mma.sync f16 FLOP/s) measured on this device."""
+    d, m = ctypes.c_double(), ctypes.c_double()
+    _check(lib().qmd_measure_alu(ctypes.byref(d), ctypes.byref(m)))
+    return d.value, m.value
 
 
 def debug_wait_timeout(limit_ns: int, stream=None) -> None:

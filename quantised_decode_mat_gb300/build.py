@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqmd.so")
-UNITS = ("api", "pack", "rmsnorm", "qmv_q4k", "qmv_q5k", "qmv_q6k", "bind")
+UNITS = ("api", "pack", "rmsnorm", "qmv_q4k", "qmv_q5k", "qmv_q6k", "bind", "alu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"] + ARCH
 

@@ -202,3 +202,10 @@ def test_fused_entry_point_reaches_the_device_check(L):
     none = q.Q8KPtrs(None, None, None)
     assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, A, 16, 512, 1, None) == 9
     assert L.qmd_qmatvec_x(q.Q5_K, A, None, A, none, A, 16, 512, 8, None) == 9
+
+
+def test_measure_alu_refuses_null_pointers(L):
+    import ctypes
+    d = ctypes.c_double()
+    assert L.qmd_measure_alu(None, ctypes.byref(d)) == 1
+    assert L.qmd_measure_alu(ctypes.byref(d), None) == 1

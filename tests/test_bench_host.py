@@ -67,3 +67,8 @@ def test_traffic_figures_are_tied_to_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("qmv_q6k") is None
     f.write_text("source_hash: 0000\nqmv_q4k_dram_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("qmv_q4k") is None
+
+
+def test_cpu_model_is_a_name():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m.strip()
