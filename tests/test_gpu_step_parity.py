@@ -1,0 +1,78 @@
+"""The 7B-shaped decode step at full size, in the launch forms bench.py times (batch 1: the pack
+fused into the 4096-wide mat-vecs and a stand-alone pack for the 14336-wide down projection;
+batch 4: pack + mat-vec), against the oracle: q|k|v and o on every row, gate|up and down on the
+rows at every CTA boundary of their launch plus a random sample; two layers."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+import quantised_decode_mat_gb300 as q  # noqa: E402
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+TOL_SAME_ORDER = 1e-5
+TOL_F64 = 2e-3
+OFMT = {q.Q4_K: O.FMT_Q4_K, q.Q6_K_SPLIT: O.FMT_Q6_K}
+
+
+@pytest.fixture(scope="module", params=[1, 4], ids=["b1", "b4"])
+def step(request):
+    from quantised_decode_mat_gb300 import build as qbuild
+    from quantised_decode_mat_gb300 import step as qstep
+    qbuild.build()
+    q.lib()
+    q.debug_set_plan()
+    q.debug_set_launch_flags(0)
+    s = qstep.make_step(request.param, layers=2, device="cuda", keep_host_layers=(0, 1))
+    s.y_all.fill_(float("nan"))
+    s.run()
+    torch.cuda.synchronize()
+    q.get_device_error()
+    return s
+
+
+def _rows_to_check(p, batch):
+    if p.rows <= 6144:
+        return None
+    rng = np.random.default_rng(p.rows + 7 * batch + p.layer)
+    pick = set(rng.choice(p.rows, size=500, replace=False).tolist()) | {0, 1, p.rows - 2, p.rows - 1}
+    G = q.launch_info(p.fmt, p.rows, p.K, batch)["grid"]
+    for g in (G, 152, 304, 456, 608):  # the plan's grid and the grids the fused plans may take
+        pick |= {(p.rows * b) // g for b in range(g)} | {(p.rows * b) // g - 1 for b in range(1, g)}
+    return np.array(sorted(r for r in pick if 0 <= r < p.rows))
+
+
+def test_launch_forms_are_the_benched_ones(step):
+    from quantised_decode_mat_gb300.step import fuse_pack
+    for p in step.projs:
+        assert p.fused == fuse_pack(step.batch, p.K)
+    if step.batch == 1:
+        assert [p.fused for p in step.projs[:4]] == [True, True, True, False]
+
+
+@pytest.mark.parametrize("index", range(8), ids=[f"L{i // 4}-{n}" for i, n in
+                                                  enumerate(["qkv", "o", "gate_up", "down"] * 2)])
+def test_step_projection_matches_oracle(step, index):
+    from quantised_decode_mat_gb300 import step as qstep
+    p = step.projs[index]
+    Wg = step.host_weights[(p.layer, p.name)]
+    x = qstep.host_activation(step, p)
+    y = p.y.cpu().numpy()
+    idx = _rows_to_check(p, step.batch)
+    oqs, od, obs = O.q8k_pack(x)
+    W = Wg if idx is None else Wg[idx]
+    yg = y if idx is None else y[:, idx]
+    assert np.isfinite(yg).all(), "unwritten (NaN) outputs"
+    ref = O.qmatvec(OFMT[p.fmt], W, oqs, od, obs, O.ORDER_RUNS_OF_SIXTEEN)
+    assert O.rel_err(yg, ref).max() <= TOL_SAME_ORDER
+    assert np.count_nonzero(yg.view(np.uint32) != ref.view(np.uint32)) == 0
+    assert O.rel_err(yg, O.qmatvec_f64(OFMT[p.fmt], W, oqs, od)).max() <= TOL_F64
+    if not p.fused:  # the stand-alone pack's output, bit for bit
+        assert np.array_equal(p.xq.qs.cpu().numpy().reshape(oqs.shape), oqs)
+        assert np.array_equal(p.xq.d.cpu().numpy().reshape(od.shape).view(np.uint32), od.view(np.uint32))
+        assert np.array_equal(p.xq.bsums.cpu().numpy().reshape(obs.shape), obs)
