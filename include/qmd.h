@@ -156,8 +156,10 @@ qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, 
  *   xq     packed activations for `batch` vectors of length K (qs, bsums 16-byte aligned,
  *          d 4-byte aligned; bsums may be NULL for Q6_K_SPLIT, which does not read them)
  *   y      f32 [batch][rows], 4-byte aligned (written)
- * Limits: 1 <= batch <= 8; K <= 32768 for batch <= 2 and K <= 16384 for batch > 2
- * (QMD_ERR_SHAPE otherwise).
+ * Limits: 1 <= batch <= 8; any K up to 32768 for batch <= 2 and up to 16384 above; longer
+ * rows go to the tensor-core kernel, which takes them run by run when its per-run row sums
+ * (32 x (ceil(K / 4096) - 1) bytes for each row a multiprocessor handles) fit in shared memory
+ * (K = 32768: about 50,000 rows); QMD_ERR_SHAPE otherwise.
  * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, DEVICE, LAUNCH.
  * Device-side bounded waits that give up set a flag read by qmd_get_device_error.
  */
@@ -268,8 +270,8 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
  *         Q4_K, Q5_K: entry j < 8 is dot_j of sub-block j (entries 8..15 stay 0);
  *         Q6_K_SPLIT: entry s is dot'_s of group s.
  *   sm    int32 [batch][rows][nb][2]: the block's S and (Q4_K, Q5_K) M; M = 0 for Q6_K_SPLIT.
- * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm; this entry also
- * refuses K > 16384 (QMD_ERR_SHAPE).
+ * Both 16-byte aligned.  Errors as qmd_qmatvec, plus NULL for dots/sm; at batches of 1..4
+ * this entry also refuses K > 16384 (QMD_ERR_SHAPE).
  */
 qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,
                                   float *y, int64_t rows, int64_t K, int batch, int32_t *dots,
@@ -306,7 +308,9 @@ void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int 
  * qmd_debug_set_launch_flags -- test-only launch options for later launches: bit 0 launches
  * qmd_q8k_pack and qmd_qmatvec without programmatic dependent launch (plain stream order);
  * bit 1 computes batches of 5..8 vectors with the dp4a kernel even where the tensor-core
- * kernel would be chosen.  Results are the same either way.  Process-wide.
+ * kernel would be chosen; bit 2 computes every batch of 3..8 vectors with the tensor-core
+ * kernel where it fits (rows of more than 16 blocks run by run).  Results are the same either
+ * way.  Process-wide.
  */
 void qmd_debug_set_launch_flags(unsigned flags);
 

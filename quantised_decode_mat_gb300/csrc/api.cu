@@ -178,43 +178,56 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->row_bytes = row_bytes;
     pl->pre_bytes = pre_bytes;
     pl->row_stride = row_bytes;
-    // Tensor-core kernel: batches of 5..8 vectors, Q4_K / Q5_K rows of at most 16 blocks (below
-    // 5 vectors the dp4a kernel is as fast or faster).  One warp per block, each with its own
-    // ring of 16-row tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per
-    // warp) that fits.  A forced ring cap below 3 selects the dp4a kernel.
+    // Tensor-core kernel.  Chosen where it was measured faster -- Q4_K / Q5_K rows of at most 16
+    // blocks at 5..8 vectors (below 5 the dp4a kernel is as fast or faster; Q6_K's 14336-wide
+    // down projection took 30.6 us against 26.2 on dp4a at 8 vectors) -- and for rows the dp4a
+    // kernel cannot take (more than 128 blocks at one or two vectors, 64 above), which it walks
+    // run by run.  One warp per block of a run of 16 blocks, each with its own ring of 16-row
+    // tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per warp) that fits
+    // beside the run sums (and, fused, the packed activations).  A forced ring cap below 3
+    // selects the dp4a kernel, and so does a shape that does not fit.
     const int fst = g_force_stages.load();
-    if (batch >= TC_MIN_BATCH && nb <= 16 && fmt != QMD_Q6_K_SPLIT && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
+    pl->tc_rows = 0;
+    const bool tc_faster = batch >= TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
+    const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);
+    const bool tc_forced = (launch_flags() & LAUNCH_TC_ALL) && batch >= 3;
+    if ((tc_faster || dp4a_cannot || tc_forced) && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
         (fst <= 0 || fst >= 3)) {
-        const bool q5 = fmt == QMD_Q5_K;
+        const int RW = nb < TC_RUN ? nb : TC_RUN;
         const int64_t ntiles = (rows + TC_ROWS - 1) / TC_ROWS;
-        int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / nb > 0 ? 16 / nb : 1);
+        int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / RW > 0 ? 16 / RW : 1);
         if (cps > 8)
             cps = 8;
         int st = 0;
+        int64_t grid = 0, rows_pad = 0;
         for (; cps >= 1; --cps) {
+            grid = (int64_t)dev.sm_count * cps;
+            if (grid > ntiles)
+                grid = ntiles;
+            rows_pad = ((rows + grid - 1) / grid + TC_ROWS - 1) / TC_ROWS * TC_ROWS;
             int budget = dev.smem_per_sm / cps - 1024;
             if (budget > dev.smem_optin)
                 budget = dev.smem_optin;
-            for (st = 4; st >= 3; --st)
-                if ((fst <= 0 || st <= fst) &&
-                    qmv_tc_layout(st, q5, nb, batch, fused).total <= budget)
-                    break;
+            st = 0;
+            if (rows_pad <= (1 << 16))
+                for (st = 4; st >= 3; --st)
+                    if ((fst <= 0 || st <= fst) &&
+                        qmv_tc_layout(st, fmt, nb, batch, fused, (int)rows_pad).total <= budget)
+                        break;
             if (st >= 3)
                 break;
         }
         if (cps >= 1 && st >= 3) {  // otherwise the dp4a kernel below takes the call
-            int64_t grid = (int64_t)dev.sm_count * cps;
-            if (grid > ntiles)
-                grid = ntiles;
             pl->layout = 1;
             pl->grid = (int)grid;
             pl->stages = st;
-            pl->threads = 32 * nb;
-            pl->smem = qmv_tc_layout(st, q5, nb, batch, fused).total;
-            pl->WR = nb;
+            pl->threads = 32 * RW;
+            pl->smem = qmv_tc_layout(st, fmt, nb, batch, fused, (int)rows_pad).total;
+            pl->WR = RW;
             pl->RG = 1;
             pl->PR = TC_ROWS;
-            pl->stage_bytes = tc_slot_bytes(q5);
+            pl->stage_bytes = tc_slot_bytes(fmt);
+            pl->tc_rows = (int)rows_pad;
             return QMD_OK;
         }
     }

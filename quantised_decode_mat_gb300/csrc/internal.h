@@ -13,6 +13,7 @@ enum : unsigned {
     ERRBIT_QMV_WAIT = 1u,     // a mat-vec pipeline wait gave up
     ERRBIT_DEBUG_WAIT = 2u,   // the test-only wait kernel gave up (as intended)
     ERRBIT_DRAIN_WAIT = 4u,   // draining copies after a give-up also gave up
+    ERRBIT_PLAN = 8u,         // a launch got more rows per CTA than its shared memory was sized for
 };
 
 struct DeviceInfo {
@@ -34,7 +35,7 @@ uint64_t wait_limit_ns();
 // Test-only launch flags (bit 0: launch without programmatic dependent launch; bit 1: compute
 // batches of 5..8 vectors with the dp4a kernel even where the tensor-core kernel applies).
 unsigned launch_flags();
-enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u };
+enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u, LAUNCH_TC_ALL = 4u };
 
 // Record a CUDA error for qmd_last_error_detail and map it to a status.
 qmd_status fail(qmd_status st, const char *what, cudaError_t e);
@@ -64,6 +65,7 @@ struct QmvPlan {
     int grid, threads, smem, stages;
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;
+    int tc_rows;  // tensor-core kernel: rows per CTA rounded up to 16 (sizes the run sums)
 };
 
 // Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.

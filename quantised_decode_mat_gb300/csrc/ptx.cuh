@@ -1,5 +1,5 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a: shared-memory mbarriers, 1-D bulk async copies
-// (global -> this CTA's shared memory, no multicast), per-thread 16-byte async copies,
+// (global -> this CTA's shared memory, no multicast), per-thread 16- and 4-byte async copies,
 // programmatic dependent launch, and a bounded barrier wait that gives up instead of hanging.
 #pragma once
 
@@ -96,6 +96,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint6
 {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
                  : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared by one thread (through L1; both addresses 4-byte
+// aligned), tracked by the same commit groups.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

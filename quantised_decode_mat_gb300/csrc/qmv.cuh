@@ -55,6 +55,7 @@ struct QmvKParams {
     int64_t rows;
     int nb, WR, RG, stages, row_bytes, pre_bytes, stage_bytes, row_stride;
     int batch;
+    int tc_rows;          // tensor-core kernel: rows per CTA rounded up to 16
     int32_t *dbg_dots;
     int32_t *dbg_sm;
     const float *x;       // fused form: f32 activations [B][K], packed inside the kernel
@@ -750,6 +751,7 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     kp.pre_bytes = plan.pre_bytes;
     kp.stage_bytes = plan.stage_bytes;
     kp.row_stride = plan.row_stride;
+    kp.tc_rows = plan.tc_rows;
     kp.dbg_dots = a.dbg_dots;
     kp.dbg_sm = a.dbg_sm;
     kp.x = a.x;

@@ -1,6 +1,6 @@
 // qmv_q6k.cu -- Q6_K (split layout) instances of the decode mat-vec (batch 1..8, plus the
 // recording variant).
-#include "qmv.cuh"
+#include "qmv_tc.cuh"
 
 namespace qmd {
 
@@ -11,6 +11,8 @@ qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
     const qmd_status st = make_params(a, plan, kp, mode);
     if (st != QMD_OK)
         return st;
+    if (plan.layout == 1)
+        return launch_qmv_tc<QMD_Q6_K_SPLIT>(kp, plan, mode, s);
     return launch_qmv_slice<QMD_Q6_K_SPLIT>(kp, plan, a.batch, mode, s);
 }
 

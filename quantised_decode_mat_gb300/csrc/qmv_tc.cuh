@@ -1,5 +1,5 @@
-// qmv_tc.cuh -- the batched decode mat-vec (5..8 vectors) on the tensor cores, for Q4_K and Q5_K
-// rows of at most 16 blocks (K <= 4096).
+// qmv_tc.cuh -- the batched decode mat-vec (5..8 vectors) on the tensor cores, for Q4_K, Q5_K
+// and Q6_K (split) rows of any length.
 //
 // Same computation and the same bits as qmv_kernel (qmv.cuh): integer sub-block dots, the
 // per-block rank-one epilogue, the declared row order ("Language models on the device: the
@@ -10,63 +10,87 @@
 // weight codes by the same 16 values of all eight (zero-padded) vectors at once, and the
 // cross-lane sum over those 16 values happens inside the instruction.
 //
-// Exactness.  Every operand is a small integer held exactly in f16: a weight code n (0..15, or
-// 0..31 with Q5_K's fifth bit) enters as 1024 + n (the byte, under a 0x64 exponent byte), an
-// activation code as itself (|q| <= 127).  The accumulator starts at -1024 * (sum of the 32
-// codes of the sub-block), which is exactly -1024 x the q8_K sub-block sum, so after the
-// sub-block's two 16-value steps it holds dot_j = sum n * q exactly: every partial sum is an
-// integer below 2^24 in magnitude, whatever order the unit adds in.  dot_j leaves as an int32
+// Exactness.  Every operand is a small integer held exactly in f16: a weight code n (0..15, 0..31
+// with Q5_K's fifth bit, 0..63 for Q6_K) enters as 1024 + n (the byte, under a 0x64 exponent
+// byte), an activation code as itself (|q| <= 127).  The accumulator starts at -1024 x (the sum
+// of the activation codes the step covers) -- for Q6_K at -1056 x that sum, which also takes the
+// codes' -32 offset -- so the step leaves the exact integer dot: every partial sum is an integer
+// below 2^24 in magnitude, whatever order the unit adds in.  The dots leave as exact integers
 // and everything after (S, M, the f32 epilogue, the row sum) is the dp4a kernel's arithmetic.
 //
-// Value order inside a sub-block.  The MMA's k index can be any permutation of a sub-block's 32
-// values, as long as both operands use the same one.  Lane (g, t) = (lane / 4, lane % 4) takes,
-// of each 32-byte code chunk, the eight bytes 8t .. 8t+7 (one 8-byte shared load per row), so a
-// step u in {0, 1} covers bytes 8t + 4u .. 8t + 4u + 3 as the MMA's k = 2t, 2t+1, 2t+8, 2t+9.
+// Value order inside a step.  The MMA's k index can be any permutation of the step's 16 values,
+// as long as both operands use the same one.  Q4_K / Q5_K (32-value sub-blocks, two steps
+// each): lane (g, t) = (lane / 4, lane % 4) takes, of each 32-byte code chunk, the eight bytes
+// 8t .. 8t+7 (one 8-byte shared load per row), so step u in {0, 1} covers bytes 8t + 4u ..
+// 8t + 4u + 3 as the MMA's k = 2t, 2t+1, 2t+8, 2t+9.  Q6_K (16-value sub-blocks, one step
+// each): lane t takes values 4t .. 4t+3 of the sub-block, whose low nibbles and high bit pairs
+// sit in one 4-byte word of ql and one of qh.
 //
-// Work split and staging.  A CTA has one warp per block of the row (nb <= 16 warps); warp w
-// owns block w of every row.  Its lane (g, t) holds, for the whole kernel, the B fragments of
-// vector g over block w's 256 values (32 registers), and per 16-row tile computes the block
-// term of rows g and g+8 for vectors 2t and 2t+1.  Each warp streams its own column (16 rows x
-// one block per tile) through a private ring of STAGES slots with 16-byte cp.async copies, rows
-// padded to 160 (Q4_K) or 224 (Q5_K) bytes so that the fragment loads of 8 rows fall in
-// distinct banks (a 1-D bulk copy cannot pad rows, and the rows of a 16-block Q4_K tile are a
-// multiple of 128 bytes apart).  Warps never wait for each other to refill; they meet only to
-// sum a tile: each posts its block terms, and the last to arrive adds the nb terms of every
-// (row, vector) in the declared order and writes y.
+// Work split and staging.  A CTA has one warp per block of a run of 16 blocks (fewer for shorter
+// rows); warp w owns block 16r + w of every row in run r, and the CTA walks its rows' tiles of
+// 16 rows run by run.  At the start of a run a warp loads, for the whole run, the B fragments of
+// vector g over its block's 256 values (32 registers) and the block's per-vector constants, and
+// per 16-row tile computes the block term of rows g and g+8 for vectors 2t and 2t+1.  Each warp
+// streams its own column (16 rows x one block per tile, plus the rows' f16 scale for Q6_K)
+// through a private ring of STAGES slots with asynchronous copies, rows padded to 160 (Q4_K),
+// 224 (Q5_K) or 240 (Q6_K) bytes so that the fragment loads of 8 rows fall in distinct banks.
+// Warps never wait for each other to refill; they meet only to sum a tile: each posts its block
+// terms, and the last to arrive adds the run's terms of every (row, vector) in the declared
+// order (groups of four blocks, runs of four groups).  A run that is not the row's last leaves
+// its sums in shared memory; the last run's finisher adds the runs left to right and writes y.
 #pragma once
 
 #include "qmv.cuh"
 
 namespace qmd {
 
-constexpr int TC_ROWS = 16;  // rows per tile (the MMA's M)
-constexpr int TC_RED = 2;    // tiles whose block terms can be pending at once
+constexpr int TC_ROWS = 16;      // rows per tile (the MMA's M)
+constexpr int TC_RED = 2;        // tiles whose block terms can be pending at once
+constexpr int TC_RUN = 16;       // blocks per run (warps per CTA at most)
 constexpr int TC_MIN_BATCH = 5;  // smallest batch the plan gives to this kernel
 
-__host__ __device__ constexpr int tc_block_bytes(bool q5) { return q5 ? 176 : 144; }
-__host__ __device__ constexpr int tc_row_stride(bool q5) { return q5 ? 224 : 160; }
-__host__ __device__ constexpr int tc_slot_bytes(bool q5) { return TC_ROWS * tc_row_stride(q5); }
+__host__ __device__ constexpr int tc_block_bytes(int fmt)
+{
+    return fmt == QMD_Q6_K_SPLIT ? 208 : fmt == QMD_Q5_K ? 176 : 144;
+}
+__host__ __device__ constexpr int tc_row_stride(int fmt)
+{
+    return fmt == QMD_Q6_K_SPLIT ? 240 : fmt == QMD_Q5_K ? 224 : 160;
+}
+// a ring slot: 16 rows, and for Q6_K the 16 rows' 4-byte prefix words holding the scale d
+__host__ __device__ constexpr int tc_slot_bytes(int fmt)
+{
+    return TC_ROWS * tc_row_stride(fmt) + (fmt == QMD_Q6_K_SPLIT ? 64 : 0);
+}
+__host__ __device__ constexpr int tc_steps(int fmt) { return fmt == QMD_Q6_K_SPLIT ? 16 : 8; }
 
 struct TcLayout {
-    int red_off, bias_off, cnt_off, fin_off, acts_off, dx_off, bs_off, total;
+    int red_off, bias_off, cnt_off, fin_off, done_off, run_off, acts_off, dx_off, bs_off, total;
 };
 
-// Shared memory: warp rings [nb][stages][16 rows][row stride] | block terms f32
-// [TC_RED][nb][16 rows][8 vectors] | accumulator starts f32 [nb][8 sub-blocks][8 vectors] |
-// arrival counters u32 [TC_RED] | finished tile i32 [TC_RED] | fused form only: codes i8
-// [B][K], d f32 [B][nb], sums i16 [B][nb][8]
-__host__ __device__ inline TcLayout qmv_tc_layout(int stages, bool q5, int nb, int B, bool pack)
+// Shared memory: warp rings [RW][stages][slot] | block terms f32 [TC_RED][RW][16 rows][8 vectors]
+// | accumulator starts f32 [RW][steps][8 vectors] | arrival counters u32 [TC_RED] | finished
+// tile i32 [TC_RED] | finished runs per row tile i32 [rows_pad / 16] | earlier runs' sums f32
+// [runs - 1][rows_pad][8] | fused form only: codes i8 [B][K], d f32 [B][nb], sums i16
+// [B][nb][8].  RW = min(nb, 16) warps; rows_pad = the CTA's rows rounded up to 16.
+__host__ __device__ inline TcLayout qmv_tc_layout(int stages, int fmt, int nb, int B, bool pack, int rows_pad)
 {
+    const int RW = nb < TC_RUN ? nb : TC_RUN;
+    const int runs = (nb + TC_RUN - 1) / TC_RUN;
     TcLayout L;
-    int o = nb * stages * tc_slot_bytes(q5);
+    int o = RW * stages * tc_slot_bytes(fmt);
     L.red_off = o;
-    o += TC_RED * nb * TC_ROWS * 8 * 4;
+    o += TC_RED * RW * TC_ROWS * 8 * 4;
     L.bias_off = o;
-    o += nb * 8 * 8 * 4;
+    o += RW * tc_steps(fmt) * 8 * 4;
     L.cnt_off = o;
     o += TC_RED * 4;
     L.fin_off = o;
-    o = align_up(o + TC_RED * 4, 16);
+    o += TC_RED * 4;
+    L.done_off = o;
+    o = align_up(o + (rows_pad / TC_ROWS) * 4, 16);
+    L.run_off = o;
+    o += (runs - 1) * rows_pad * 8 * 4;
     L.acts_off = o;
     if (pack)
         o += B * nb * 256;
@@ -74,7 +98,7 @@ __host__ __device__ inline TcLayout qmv_tc_layout(int stages, bool q5, int nb, i
     if (pack)
         o = align_up(o + B * nb * 4, 16);
     L.bs_off = o;
-    if (pack)
+    if (pack && fmt != QMD_Q6_K_SPLIT)
         o += B * nb * 16;
     L.total = align_up(o, 16);
     return L;
@@ -106,6 +130,13 @@ __device__ __forceinline__ float byte_as_float(uint32_t w, uint32_t b)
     return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b)), 8388608.0f);
 }
 
+// Signed byte b (0..3) of w as an exact float: (byte ^ 0x80) is byte + 128 in 0..255 under the
+// exponent of 2^23, minus 2^23 + 128.
+__device__ __forceinline__ float sbyte_as_float(uint32_t w, uint32_t b)
+{
+    return __fsub_rn(__uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7440u | b)), 8388736.0f);
+}
+
 // Two signed bytes (bytes lo, lo+1 of w) as an exact f16 pair: (byte ^ 0x80) under a 0x64
 // exponent byte is 1024 + 128 + q, minus 1152.
 __device__ __forceinline__ uint32_t s8x2_to_f16x2(uint32_t w, uint32_t sel)
@@ -123,48 +154,71 @@ __device__ __forceinline__ int exact_small_int(float v)
     return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
 }
 
-// F is QMD_Q4_K or QMD_Q5_K; STAGES is the depth of each warp's ring.
-template <int F, int MODE, int STAGES>
+__device__ __forceinline__ uint32_t lds32(const void *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// F is QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT; STAGES is the depth of each warp's ring; MULTI
+// walks rows of more than 16 blocks run by run (without it the row is a single run and the
+// run bookkeeping compiles away).
+template <int F, int MODE, int STAGES, bool MULTI>
 __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
 {
+    constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
     constexpr bool Q5 = F == QMD_Q5_K;
     constexpr bool DUMP = MODE == QMV_DUMP;
     constexpr bool PACK = MODE == QMV_PACK;
-    constexpr int BLOCK_BYTES = tc_block_bytes(Q5);
-    constexpr int RSTRIDE = tc_row_stride(Q5);
-    constexpr int SLOT = tc_slot_bytes(Q5);
+    constexpr int BLOCK_BYTES = tc_block_bytes(F);
+    constexpr int RSTRIDE = tc_row_stride(F);
+    constexpr int SLOT = tc_slot_bytes(F);
     constexpr int CPR = BLOCK_BYTES / 16;  // 16-byte chunks per row of a block
+    constexpr int NSTEP = tc_steps(F);     // accumulator starts per block and vector
     constexpr int QS_OFF = Q5 ? 48 : 16;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = p.nb, B = p.batch;
+    const int RW = blockDim.x >> 5;  // warps: min(nb, 16)
+    const int runs = MULTI ? (nb + TC_RUN - 1) / TC_RUN : 1;
     const int g = lane >> 2, t = lane & 3;
-    const int blk = warp;  // this warp's block of every row
     const int64_t r0 = p.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = p.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
-    const int nch = (int)((r1 - r0 + TC_ROWS - 1) / TC_ROWS);
-    const TcLayout L = qmv_tc_layout(STAGES, Q5, nb, B, PACK);
+    const int nt = (int)((r1 - r0 + TC_ROWS - 1) / TC_ROWS);  // row tiles of this CTA
+    const int ntot = runs * nt;                                // tiles, run by run
+    const TcLayout L = qmv_tc_layout(STAGES, F, nb, B, PACK, p.tc_rows);
     uint8_t *ring = smem + (size_t)warp * STAGES * SLOT;
     float *s_red = reinterpret_cast<float *>(smem + L.red_off);
     unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + L.cnt_off);
     volatile int *s_fin = reinterpret_cast<volatile int *>(smem + L.fin_off);
+    volatile int *s_done = reinterpret_cast<volatile int *>(smem + L.done_off);
+    float *s_run = reinterpret_cast<float *>(smem + L.run_off);
     const uint64_t pol = policy_evict_first();
+    if (runs > 1 && nt * TC_ROWS > p.tc_rows) {  // more rows than the run-sum buffer was sized for
+        if (tid == 0)
+            atomicOr(p.err, ERRBIT_PLAN);
+        return;
+    }
 
-    // this warp's column of tile c (rows r0 + 16c ..) into its ring slot c % STAGES: lane l
-    // copies row l / 2, 16-byte chunks l % 2, l % 2 + 2, ...; every lane commits one group per
-    // tile index, empty past the last tile, so group counts stay aligned
+    // this warp's column of tile T (run T / nt, rows r0 + 16 (T % nt) ..) into ring slot
+    // T % STAGES: lane l copies row l / 2, 16-byte chunks l % 2, l % 2 + 2, ...; for Q6_K the
+    // even lanes also copy their row's aligned 4-byte prefix word holding the block's scale.
+    // Every lane commits one group per tile index, empty past its last tile, so group counts
+    // stay aligned.
     const int crow = lane >> 1, ccol = lane & 1;
-    const uint32_t cdst0 = smem_addr(ring) + crow * RSTRIDE + 16 * ccol;
-    const uint8_t *csrc0 = p.W + (r0 + crow) * p.row_bytes + blk * BLOCK_BYTES + 16 * ccol;
-    auto issue = [&](int c) {
-        if (c < nch && r0 + (int64_t)c * TC_ROWS + crow < r1) {
-            const uint32_t dst = cdst0 + (c % STAGES) * SLOT;
-            const uint8_t *src = csrc0 + (int64_t)c * TC_ROWS * p.row_bytes;
+    auto issue = [&](int T) {
+        if (T < ntot) {
+            const int r = MULTI ? T / nt : 0, c = MULTI ? T - r * nt : T;
+            const int b = r * TC_RUN + warp;
+            const int64_t row = r0 + (int64_t)c * TC_ROWS + crow;
+            if (b < nb && row < r1) {
+                const uint32_t slot = smem_addr(ring) + (T % STAGES) * SLOT;
+                const uint32_t dst = slot + crow * RSTRIDE + 16 * ccol;
+                const uint8_t *src = p.W + row * p.row_bytes + (int64_t)b * BLOCK_BYTES + 16 * ccol;
 #pragma unroll
-            for (int k = 0; k < (CPR + 1) / 2; ++k)
-                if (2 * k + ccol < CPR)
-                    cp_async_16(dst + 32 * k, src + 32 * k, pol);
+                for (int k = 0; k < (CPR + 1) / 2; ++k)
+                    if (2 * k + ccol < CPR)
+                        cp_async_16(dst + 32 * k, src + 32 * k, pol);
+                if (Q6 && ccol == 0)
+                    cp_async_4(slot + TC_ROWS * RSTRIDE + 4 * crow, p.Wpre + row * p.pre_bytes + 2 * (b & ~1));
+            }
         }
         cp_async_commit();
     };
@@ -173,9 +227,12 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
         s_cnt[tid] = 0;
         s_fin[tid] = tid - TC_RED;  // slot tid is free for tile tid
     }
+    if (runs > 1)
+        for (int i = tid; i < nt; i += blockDim.x)
+            s_done[i] = 0;
 #pragma unroll
-    for (int c = 0; c < STAGES; ++c)
-        issue(c);
+    for (int T = 0; T < STAGES; ++T)
+        issue(T);
     __syncthreads();
 
     pdl_launch_dependents();
@@ -192,22 +249,22 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
         float *dx = reinterpret_cast<float *>(smem + L.dx_off);
         int16_t *bs = reinterpret_cast<int16_t *>(smem + L.bs_off);
         const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
-        for (int b = warp; b < B * nb; b += nb) {
+        for (int b = warp; b < B * nb; b += RW) {
             const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
             const float4 xa = src[0], xb = src[1];
             const float v8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-            const Q8Block r = q8k_quantise_block(v8);
-            *reinterpret_cast<uint2 *>(acts + b * 256 + 8 * lane) = r.codes;
-            if ((lane & 3) == 0)
-                bs[b * 8 + (lane >> 2)] = (int16_t)r.sum4;
+            const Q8Block q = q8k_quantise_block(v8);
+            *reinterpret_cast<uint2 *>(acts + b * 256 + 8 * lane) = q.codes;
+            if (!Q6 && (lane & 3) == 0)
+                bs[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
             if (lane == 0)
-                dx[b] = r.d;
+                dx[b] = q.d;
             if (out) {
-                *reinterpret_cast<uint2 *>(p.xq_qs_out + (int64_t)b * 256 + 8 * lane) = r.codes;
+                *reinterpret_cast<uint2 *>(p.xq_qs_out + (int64_t)b * 256 + 8 * lane) = q.codes;
                 if ((lane & 3) == 0)
-                    p.xq_bs_out[b * 8 + (lane >> 2)] = (int16_t)r.sum4;
+                    p.xq_bs_out[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
                 if (lane == 0)
-                    p.xq_d_out[b] = r.d;
+                    p.xq_d_out[b] = q.d;
             }
         }
         __syncthreads();
@@ -216,186 +273,295 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
         b_src = bs;
     }
 
-    // ---- this lane's fixed operands: B fragments of vector g over block blk, and for vectors
-    // 2t, 2t+1 the block's scale, eight sub-block sums, and the accumulator start values -------
-    // k-step (j, u): the lane's four values of sub-block j are 32j + 8t + 4u .. +3 (the MMA's
-    // k = 2t, 2t+1, 2t+8, 2t+9), matching the A fragments built below.
-    uint32_t bfr[8][2][2];
-    {
-        const bool have = g < B;
-        const int8_t *xv = a_src + (int64_t)g * K + 256 * blk + 8 * t;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint32_t w = have ? *reinterpret_cast<const uint32_t *>(xv + 32 * j + 4 * u) : 0u;
-                bfr[j][u][0] = s8x2_to_f16x2(w, 0x4140u);  // values 8t + 4u, +1 (bytes 0, 1)
-                bfr[j][u][1] = s8x2_to_f16x2(w, 0x4342u);  // values +2, +3     (bytes 2, 3)
-            }
-    }
+    // this lane's operands for the current run, loaded at the run's first tile: B fragments of
+    // vector g over the warp's block, and for vectors 2t, 2t+1 the block's scale (and, Q4_K /
+    // Q5_K, its eight sub-block sums); the accumulator starts go to the warp's bias table
+    uint32_t bfr[32];
     float dxv[2];
-    int4 bsv[2];  // eight int16 sub-block sums of vectors 2t, 2t+1 (pairs per int)
-    // accumulator starts -1024 x sub-block sum, [sub-block j][vector], shared by the warp
-    float *bias = reinterpret_cast<float *>(smem + L.bias_off) + blk * 64;
+    int4 bsv[2];
+    float *bias = reinterpret_cast<float *>(smem + L.bias_off) + warp * NSTEP * 8;
+    auto load_run = [&](int blk) {
+        const bool have = g < B;
+        if (Q6) {
+            // step s = sub-block s: the lane's values 4t .. 4t+3, one word; the start is
+            // -1056 x the sub-block's 16 codes (the 1024 of the code encoding and the -32 offset)
+            const int8_t *xv = a_src + (int64_t)g * K + 256 * blk + 4 * t;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int v = 2 * t + e;
-        if (v < B) {
-            dxv[e] = d_src[v * nb + blk];
-            bsv[e] = *reinterpret_cast<const int4 *>(b_src + (v * nb + blk) * 8);
+            for (int s = 0; s < 16; ++s) {
+                const uint32_t w = have ? *reinterpret_cast<const uint32_t *>(xv + 16 * s) : 0u;
+                bfr[2 * s] = s8x2_to_f16x2(w, 0x4140u);
+                bfr[2 * s + 1] = s8x2_to_f16x2(w, 0x4342u);
+                int ps = __dp4a((int)w, 0x01010101, 0);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+                if (t == 0)
+                    bias[s * 8 + g] = -1056.0f * (float)ps;
+            }
         } else {
-            dxv[e] = 0.0f;
-            bsv[e] = make_int4(0, 0, 0, 0);
-        }
-        const int s8[8] = {(int)(int16_t)(bsv[e].x & 0xffff), bsv[e].x >> 16, (int)(int16_t)(bsv[e].y & 0xffff),
-                           bsv[e].y >> 16, (int)(int16_t)(bsv[e].z & 0xffff), bsv[e].z >> 16,
-                           (int)(int16_t)(bsv[e].w & 0xffff), bsv[e].w >> 16};
-        if (g == 0) {
+            // k-step (j, u): the lane's four values of sub-block j are 32j + 8t + 4u .. +3 (the
+            // MMA's k = 2t, 2t+1, 2t+8, 2t+9), matching the A fragments built below
+            const int8_t *xv = a_src + (int64_t)g * K + 256 * blk + 8 * t;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                bias[j * 8 + v] = -1024.0f * (float)s8[j];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t w = have ? *reinterpret_cast<const uint32_t *>(xv + 32 * j + 4 * u) : 0u;
+                    bfr[4 * j + 2 * u] = s8x2_to_f16x2(w, 0x4140u);      // values 8t + 4u, +1
+                    bfr[4 * j + 2 * u + 1] = s8x2_to_f16x2(w, 0x4342u);  // values +2, +3
+                }
         }
-    }
-    __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int v = 2 * t + e;
+            if (v < B) {
+                dxv[e] = d_src[v * nb + blk];
+                bsv[e] = Q6 ? make_int4(0, 0, 0, 0) : *reinterpret_cast<const int4 *>(b_src + (v * nb + blk) * 8);
+            } else {
+                dxv[e] = 0.0f;
+                bsv[e] = make_int4(0, 0, 0, 0);
+            }
+            if (!Q6) {  // -1024 x the q8_K sub-block sums
+                const int s8[8] = {(int)(int16_t)(bsv[e].x & 0xffff), bsv[e].x >> 16, (int)(int16_t)(bsv[e].y & 0xffff),
+                                   bsv[e].y >> 16, (int)(int16_t)(bsv[e].z & 0xffff), bsv[e].z >> 16,
+                                   (int)(int16_t)(bsv[e].w & 0xffff), bsv[e].w >> 16};
+                if (g == 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        bias[j * 8 + v] = -1024.0f * (float)s8[j];
+                }
+            }
+        }
+        __syncwarp();
+    };
 
     const unsigned long long wait_ns = p.wait_ns;
+    int run_nb = MULTI ? 0 : nb, blk = warp;
+    if (!MULTI)
+        load_run(warp);
 #pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-        cp_async_wait<STAGES - 1>();  // this lane's copies of tile c have landed
+    for (int T = 0; T < ntot; ++T) {
+        const int r = MULTI ? T / nt : 0, c = MULTI ? T - r * nt : T;
+        if (MULTI && c == 0) {
+            run_nb = min(TC_RUN, nb - r * TC_RUN);
+            if (warp >= run_nb)
+                break;  // only the last run can be short; this warp has no block in it
+            blk = r * TC_RUN + warp;
+            load_run(blk);
+        }
+        cp_async_wait<STAGES - 1>();  // this lane's copies of tile T have landed
         __syncwarp();                  // ... and every lane's are visible to the warp
         const int64_t rs = r0 + (int64_t)c * TC_ROWS;
         const int nr = (int)min((int64_t)TC_ROWS, r1 - rs);
 
         // rows g and g+8 of the tile (rows past nr hold stale bytes: computed, never stored)
-        const uint8_t *rowA = ring + (c % STAGES) * SLOT + g * RSTRIDE;
+        const uint8_t *slot = ring + (T % STAGES) * SLOT;
+        const uint8_t *rowA = slot + g * RSTRIDE;
         const uint8_t *rowB = rowA + 8 * RSTRIDE;
-        const uint4 hA = lds128(rowA), hB = lds128(rowB);
-        // six-bit scales of sub-blocks 0..3 and 4..7, one per byte
-        const uint32_t scA0 = hA.y & 0x3F3F3F3Fu, scA1 = (hA.w & 0x0F0F0F0Fu) | ((hA.y >> 2) & 0x30303030u);
-        const uint32_t scB0 = hB.y & 0x3F3F3F3Fu, scB1 = (hB.w & 0x0F0F0F0Fu) | ((hB.y >> 2) & 0x30303030u);
-        // Q5_K: the fifth bits of this lane's bytes 8t .. 8t+7 of every chunk (bit 2cq, 2cq+1)
-        uint2 qhA = make_uint2(0, 0), qhB = make_uint2(0, 0);
-        if (Q5) {
-            qhA = *reinterpret_cast<const uint2 *>(rowA + 16 + 8 * t);
-            qhB = *reinterpret_cast<const uint2 *>(rowB + 16 + 8 * t);
-        }
         int S[2][2] = {{0, 0}, {0, 0}};  // [row A/B][vector 2t / 2t+1]
-        // Q4_K: sum_j sc_j * dot_j in f32 over each half block (sub-blocks 0..3, 4..7): every
-        // product and partial sum is an integer of magnitude at most 4 * 63 * 15 * 127 * 32
-        // < 2^24, so the f32 fused multiply-adds are exact
-        float Sf[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half block: [row g v0, v1, g+8 v0, v1]
+        float term[2][2];
+        if constexpr (Q6) {
+            // 16 sub-blocks of 16 values; sum_s sc_s * dot_s in f32 banked to int32 every two
+            // sub-blocks: |sc| <= 128 and |dot| <= 16 * 32 * 127, so each partial is an integer
+            // below 2^24 and the fused multiply-adds are exact
+            const uint4 scA = lds128(rowA + 192), scB = lds128(rowB + 192);
+            float Sf[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // [row g v0, v1, g+8 v0, v1]
 #pragma unroll
-        for (int cq = 0; cq < 4; ++cq) {  // 32-byte code chunk cq: sub-blocks 2cq (low), 2cq+1 (high)
-            float dlo[4], dhi[4];
-            const float2 blo = *reinterpret_cast<const float2 *>(bias + (2 * cq) * 8 + 2 * t);
-            const float2 bhi = *reinterpret_cast<const float2 *>(bias + (2 * cq + 1) * 8 + 2 * t);
-            const uint2 cA = *reinterpret_cast<const uint2 *>(rowA + QS_OFF + 32 * cq + 8 * t);
-            const uint2 cB = *reinterpret_cast<const uint2 *>(rowB + QS_OFF + 32 * cq + 8 * t);
+            for (int h = 0; h < 2; ++h) {
+                // ql words (t6 & 1, half) at 64h + 16 (2 (t6 & 1) + half) + 4t; qh words (half)
+                uint32_t qlA[4], qlB[4], qhA[2], qhB[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint32_t wA = u ? cA.y : cA.x, wB = u ? cB.y : cB.x;
-                uint32_t loA = wA & 0x0F0F0F0Fu, loB = wB & 0x0F0F0F0Fu;
-                uint32_t hiA = (wA >> 4) & 0x0F0F0F0Fu, hiB = (wB >> 4) & 0x0F0F0F0Fu;
-                if (Q5) {
-                    const uint32_t qA = u ? qhA.y : qhA.x, qB = u ? qhB.y : qhB.x;
-                    const int rl = (2 * cq - 4) & 31, rh = (2 * cq - 3) & 31;
-                    loA |= __funnelshift_r(qA, qA, rl) & 0x10101010u;
-                    loB |= __funnelshift_r(qB, qB, rl) & 0x10101010u;
-                    hiA |= __funnelshift_r(qA, qA, rh) & 0x10101010u;
-                    hiB |= __funnelshift_r(qB, qB, rh) & 0x10101010u;
+                for (int i = 0; i < 4; ++i) {
+                    qlA[i] = lds32(rowA + 64 * h + 16 * i + 4 * t);
+                    qlB[i] = lds32(rowB + 64 * h + 16 * i + 4 * t);
                 }
-                // codes as f16 1024 + n: rows g (A) and g+8 (B), bytes 0, 1 then 2, 3
-                const uint32_t alo[4] = {__byte_perm(loA, 0x64u, 0x4140u), __byte_perm(loB, 0x64u, 0x4140u),
-                                         __byte_perm(loA, 0x64u, 0x4342u), __byte_perm(loB, 0x64u, 0x4342u)};
-                const uint32_t ahi[4] = {__byte_perm(hiA, 0x64u, 0x4140u), __byte_perm(hiB, 0x64u, 0x4140u),
-                                         __byte_perm(hiA, 0x64u, 0x4342u), __byte_perm(hiB, 0x64u, 0x4342u)};
-                if (u == 0) {
-                    mma_16816_c(dlo, alo, bfr[2 * cq][0][0], bfr[2 * cq][0][1], blo.x, blo.y, blo.x, blo.y);
-                    mma_16816_c(dhi, ahi, bfr[2 * cq + 1][0][0], bfr[2 * cq + 1][0][1], bhi.x, bhi.y, bhi.x, bhi.y);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    qhA[i] = lds32(rowA + 128 + 32 * h + 16 * i + 4 * t);
+                    qhB[i] = lds32(rowB + 128 + 32 * h + 16 * i + 4 * t);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int s = 8 * h + j, t6 = j >> 1, half = j & 1;
+                    const int qi = 2 * (t6 & 1) + half, nsh = 4 * (t6 >> 1), hsh = 2 * t6;
+                    // six-bit codes of the lane's four values, one per byte
+                    const uint32_t wA = ((qlA[qi] >> nsh) & 0x0F0F0F0Fu) | (((qhA[half] >> hsh) & 0x03030303u) << 4);
+                    const uint32_t wB = ((qlB[qi] >> nsh) & 0x0F0F0F0Fu) | (((qhB[half] >> hsh) & 0x03030303u) << 4);
+                    const uint32_t a[4] = {__byte_perm(wA, 0x64u, 0x4140u), __byte_perm(wB, 0x64u, 0x4140u),
+                                           __byte_perm(wA, 0x64u, 0x4342u), __byte_perm(wB, 0x64u, 0x4342u)};
+                    const float2 bb = *reinterpret_cast<const float2 *>(bias + s * 8 + 2 * t);
+                    float d[4];
+                    mma_16816_c(d, a, bfr[2 * s], bfr[2 * s + 1], bb.x, bb.y, bb.x, bb.y);
+                    // d holds the exact dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
+                    const uint32_t wsA = s < 4 ? scA.x : s < 8 ? scA.y : s < 12 ? scA.z : scA.w;
+                    const uint32_t wsB = s < 4 ? scB.x : s < 8 ? scB.y : s < 12 ? scB.z : scB.w;
+                    const float fA = sbyte_as_float(wsA, (uint32_t)(s & 3));
+                    const float fB = sbyte_as_float(wsB, (uint32_t)(s & 3));
+                    Sf[0] = __fmaf_rn(fA, d[0], Sf[0]);
+                    Sf[1] = __fmaf_rn(fA, d[1], Sf[1]);
+                    Sf[2] = __fmaf_rn(fB, d[2], Sf[2]);
+                    Sf[3] = __fmaf_rn(fB, d[3], Sf[3]);
+                    if (j & 1) {  // bank two sub-blocks as int32 (exact)
+                        S[0][0] += __float2int_rn(Sf[0]);
+                        S[0][1] += __float2int_rn(Sf[1]);
+                        S[1][0] += __float2int_rn(Sf[2]);
+                        S[1][1] += __float2int_rn(Sf[3]);
+                        Sf[0] = Sf[1] = Sf[2] = Sf[3] = 0.0f;
+                    }
+                    if (DUMP) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = g + 8 * (i >> 1), v = 2 * t + (i & 1);
+                            if (row < nr && v < B)
+                                p.dbg_dots[((v * p.rows + rs + row) * nb + blk) * 16 + s] = exact_small_int(d[i]);
+                        }
+                    }
+                }
+            }
+            // the block's f32 terms: dx * (d * S), d the row's f16 scale from the prefix word
+            const uint8_t *pre = slot + TC_ROWS * RSTRIDE;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = g + 8 * rr;
+                const uint32_t pw = lds32(pre + 4 * row);
+                const float d = __half2float(__ushort_as_half((unsigned short)((blk & 1) ? (pw >> 16) : (pw & 0xffffu))));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    term[rr][e] = __fmul_rn(dxv[e], __fmul_rn(d, __int2float_rn(S[rr][e])));
+                    if (DUMP && row < nr && 2 * t + e < B) {
+                        int32_t *sm = p.dbg_sm + (((2 * t + e) * p.rows + rs + row) * nb + blk) * 2;
+                        sm[0] = S[rr][e];
+                        sm[1] = 0;
+                    }
+                }
+            }
+        } else {
+            const uint4 hA = lds128(rowA), hB = lds128(rowB);
+            // six-bit scales of sub-blocks 0..3 and 4..7, one per byte
+            const uint32_t scA0 = hA.y & 0x3F3F3F3Fu, scA1 = (hA.w & 0x0F0F0F0Fu) | ((hA.y >> 2) & 0x30303030u);
+            const uint32_t scB0 = hB.y & 0x3F3F3F3Fu, scB1 = (hB.w & 0x0F0F0F0Fu) | ((hB.y >> 2) & 0x30303030u);
+            // Q5_K: the fifth bits of this lane's bytes 8t .. 8t+7 of every chunk (bit 2cq, 2cq+1)
+            uint2 qhA = make_uint2(0, 0), qhB = make_uint2(0, 0);
+            if (Q5) {
+                qhA = *reinterpret_cast<const uint2 *>(rowA + 16 + 8 * t);
+                qhB = *reinterpret_cast<const uint2 *>(rowB + 16 + 8 * t);
+            }
+            // Q4_K: sum_j sc_j * dot_j in f32 over each half block (sub-blocks 0..3, 4..7): every
+            // product and partial sum is an integer of magnitude at most 4 * 63 * 15 * 127 * 32
+            // < 2^24, so the f32 fused multiply-adds are exact
+            float Sf[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half block: [row g v0, v1, g+8 v0, v1]
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq) {  // 32-byte code chunk cq: sub-blocks 2cq (low), 2cq+1 (high)
+                float dlo[4], dhi[4];
+                const float2 blo = *reinterpret_cast<const float2 *>(bias + (2 * cq) * 8 + 2 * t);
+                const float2 bhi = *reinterpret_cast<const float2 *>(bias + (2 * cq + 1) * 8 + 2 * t);
+                const uint2 cA = *reinterpret_cast<const uint2 *>(rowA + QS_OFF + 32 * cq + 8 * t);
+                const uint2 cB = *reinterpret_cast<const uint2 *>(rowB + QS_OFF + 32 * cq + 8 * t);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t wA = u ? cA.y : cA.x, wB = u ? cB.y : cB.x;
+                    uint32_t loA = wA & 0x0F0F0F0Fu, loB = wB & 0x0F0F0F0Fu;
+                    uint32_t hiA = (wA >> 4) & 0x0F0F0F0Fu, hiB = (wB >> 4) & 0x0F0F0F0Fu;
+                    if (Q5) {
+                        const uint32_t qA = u ? qhA.y : qhA.x, qB = u ? qhB.y : qhB.x;
+                        const int rl = (2 * cq - 4) & 31, rh = (2 * cq - 3) & 31;
+                        loA |= __funnelshift_r(qA, qA, rl) & 0x10101010u;
+                        loB |= __funnelshift_r(qB, qB, rl) & 0x10101010u;
+                        hiA |= __funnelshift_r(qA, qA, rh) & 0x10101010u;
+                        hiB |= __funnelshift_r(qB, qB, rh) & 0x10101010u;
+                    }
+                    // codes as f16 1024 + n: rows g (A) and g+8 (B), bytes 0, 1 then 2, 3
+                    const uint32_t alo[4] = {__byte_perm(loA, 0x64u, 0x4140u), __byte_perm(loB, 0x64u, 0x4140u),
+                                             __byte_perm(loA, 0x64u, 0x4342u), __byte_perm(loB, 0x64u, 0x4342u)};
+                    const uint32_t ahi[4] = {__byte_perm(hiA, 0x64u, 0x4140u), __byte_perm(hiB, 0x64u, 0x4140u),
+                                             __byte_perm(hiA, 0x64u, 0x4342u), __byte_perm(hiB, 0x64u, 0x4342u)};
+                    if (u == 0) {
+                        mma_16816_c(dlo, alo, bfr[8 * cq], bfr[8 * cq + 1], blo.x, blo.y, blo.x, blo.y);
+                        mma_16816_c(dhi, ahi, bfr[8 * cq + 4], bfr[8 * cq + 5], bhi.x, bhi.y, bhi.x, bhi.y);
+                    } else {
+                        mma_16816(dlo, alo, bfr[8 * cq + 2], bfr[8 * cq + 3]);
+                        mma_16816(dhi, ahi, bfr[8 * cq + 6], bfr[8 * cq + 7]);
+                    }
+                }
+                // dlo, dhi hold the exact integer dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
+                const uint32_t wsA = cq < 2 ? scA0 : scA1, wsB = cq < 2 ? scB0 : scB1;
+                const uint32_t bl = 2 * (cq & 1), bh = bl + 1;
+                if (!Q5) {
+                    const float fAl = byte_as_float(wsA, bl), fAh = byte_as_float(wsA, bh);
+                    const float fBl = byte_as_float(wsB, bl), fBh = byte_as_float(wsB, bh);
+                    Sf[0] = __fmaf_rn(fAh, dhi[0], __fmaf_rn(fAl, dlo[0], Sf[0]));
+                    Sf[1] = __fmaf_rn(fAh, dhi[1], __fmaf_rn(fAl, dlo[1], Sf[1]));
+                    Sf[2] = __fmaf_rn(fBh, dhi[2], __fmaf_rn(fBl, dlo[2], Sf[2]));
+                    Sf[3] = __fmaf_rn(fBh, dhi[3], __fmaf_rn(fBl, dlo[3], Sf[3]));
+                    if (cq & 1) {  // a half block is complete: bank it as int32 (exact, below 2^24)
+                        S[0][0] += __float2int_rn(Sf[0]);
+                        S[0][1] += __float2int_rn(Sf[1]);
+                        S[1][0] += __float2int_rn(Sf[2]);
+                        S[1][1] += __float2int_rn(Sf[3]);
+                        Sf[0] = Sf[1] = Sf[2] = Sf[3] = 0.0f;
+                    }
                 } else {
-                    mma_16816(dlo, alo, bfr[2 * cq][1][0], bfr[2 * cq][1][1]);
-                    mma_16816(dhi, ahi, bfr[2 * cq + 1][1][0], bfr[2 * cq + 1][1][1]);
+                    const uint32_t sl = 0x4440u | bl, sh = 0x4440u | bh;
+                    const int sAl = (int)__byte_perm(wsA, 0u, sl), sAh = (int)__byte_perm(wsA, 0u, sh);
+                    const int sBl = (int)__byte_perm(wsB, 0u, sl), sBh = (int)__byte_perm(wsB, 0u, sh);
+                    S[0][0] += sAl * exact_small_int(dlo[0]) + sAh * exact_small_int(dhi[0]);
+                    S[0][1] += sAl * exact_small_int(dlo[1]) + sAh * exact_small_int(dhi[1]);
+                    S[1][0] += sBl * exact_small_int(dlo[2]) + sBh * exact_small_int(dhi[2]);
+                    S[1][1] += sBl * exact_small_int(dlo[3]) + sBh * exact_small_int(dhi[3]);
+                }
+                if (DUMP) {
+                    int il[4], ih[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        il[i] = exact_small_int(dlo[i]);
+                        ih[i] = exact_small_int(dhi[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = g + 8 * (i >> 1), v = 2 * t + (i & 1);
+                        if (row < nr && v < B) {
+                            int32_t *dd = p.dbg_dots + ((v * p.rows + rs + row) * nb + blk) * 16;
+                            dd[2 * cq] = il[i];
+                            dd[2 * cq + 1] = ih[i];
+                        }
+                    }
                 }
             }
-            // dlo, dhi hold the exact integer dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
-            const uint32_t wsA = cq < 2 ? scA0 : scA1, wsB = cq < 2 ? scB0 : scB1;
-            const uint32_t bl = 2 * (cq & 1), bh = bl + 1;
-            if (!Q5) {
-                const float fAl = byte_as_float(wsA, bl), fAh = byte_as_float(wsA, bh);
-                const float fBl = byte_as_float(wsB, bl), fBh = byte_as_float(wsB, bh);
-                Sf[0] = __fmaf_rn(fAh, dhi[0], __fmaf_rn(fAl, dlo[0], Sf[0]));
-                Sf[1] = __fmaf_rn(fAh, dhi[1], __fmaf_rn(fAl, dlo[1], Sf[1]));
-                Sf[2] = __fmaf_rn(fBh, dhi[2], __fmaf_rn(fBl, dlo[2], Sf[2]));
-                Sf[3] = __fmaf_rn(fBh, dhi[3], __fmaf_rn(fBl, dlo[3], Sf[3]));
-                if (cq & 1) {  // a half block is complete: bank it as int32 (exact, below 2^24)
-                    S[0][0] += __float2int_rn(Sf[0]);
-                    S[0][1] += __float2int_rn(Sf[1]);
-                    S[1][0] += __float2int_rn(Sf[2]);
-                    S[1][1] += __float2int_rn(Sf[3]);
-                    Sf[0] = Sf[1] = Sf[2] = Sf[3] = 0.0f;
-                }
-            } else {
-                const uint32_t sl = 0x4440u | bl, sh = 0x4440u | bh;
-                const int sAl = (int)__byte_perm(wsA, 0u, sl), sAh = (int)__byte_perm(wsA, 0u, sh);
-                const int sBl = (int)__byte_perm(wsB, 0u, sl), sBh = (int)__byte_perm(wsB, 0u, sh);
-                S[0][0] += sAl * exact_small_int(dlo[0]) + sAh * exact_small_int(dhi[0]);
-                S[0][1] += sAl * exact_small_int(dlo[1]) + sAh * exact_small_int(dhi[1]);
-                S[1][0] += sBl * exact_small_int(dlo[2]) + sBh * exact_small_int(dhi[2]);
-                S[1][1] += sBl * exact_small_int(dlo[3]) + sBh * exact_small_int(dhi[3]);
-            }
-            if (DUMP) {
-                int il[4], ih[4];
+
+            // ---- the block's f32 terms for (rows g, g+8) x (vectors 2t, 2t+1) ------------
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    il[i] = exact_small_int(dlo[i]);
-                    ih[i] = exact_small_int(dhi[i]);
-                }
+            for (int rr = 0; rr < 2; ++rr) {
+                const uint4 h = rr ? hB : hA;
+                const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                const uint32_t m0 = h.z & 0x3F3F3F3Fu;
+                const uint32_t m1 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+                const int row = g + 8 * rr;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = g + 8 * (i >> 1), v = 2 * t + (i & 1);
-                    if (row < nr && v < B) {
-                        int32_t *dd = p.dbg_dots + ((v * p.rows + rs + row) * nb + blk) * 16;
-                        dd[2 * cq] = il[i];
-                        dd[2 * cq + 1] = ih[i];
+                for (int e = 0; e < 2; ++e) {
+                    int M = __dp2a_lo(bsv[e].x, (int)m0, 0);
+                    M = __dp2a_hi(bsv[e].y, (int)m0, M);
+                    M = __dp2a_lo(bsv[e].z, (int)m1, M);
+                    M = __dp2a_hi(bsv[e].w, (int)m1, M);
+                    term[rr][e] = __fmul_rn(dxv[e], __fsub_rn(__fmul_rn(d, __int2float_rn(S[rr][e])),
+                                                              __fmul_rn(dmin, __int2float_rn(M))));
+                    if (DUMP && row < nr && 2 * t + e < B) {
+                        int32_t *sm = p.dbg_sm + (((2 * t + e) * p.rows + rs + row) * nb + blk) * 2;
+                        sm[0] = S[rr][e];
+                        sm[1] = M;
                     }
                 }
             }
         }
-
-        // ---- the block's f32 terms for (rows g, g+8) x (vectors 2t, 2t+1) ----------------
-        float term[2][2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const uint4 h = r ? hB : hA;
-            const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
-            const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-            const uint32_t m0 = h.z & 0x3F3F3F3Fu;
-            const uint32_t m1 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-            const int row = g + 8 * r;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                int M = __dp2a_lo(bsv[e].x, (int)m0, 0);
-                M = __dp2a_hi(bsv[e].y, (int)m0, M);
-                M = __dp2a_lo(bsv[e].z, (int)m1, M);
-                M = __dp2a_hi(bsv[e].w, (int)m1, M);
-                term[r][e] = __fmul_rn(dxv[e], __fsub_rn(__fmul_rn(d, __int2float_rn(S[r][e])),
-                                                         __fmul_rn(dmin, __int2float_rn(M))));
-                if (DUMP && row < nr && 2 * t + e < B) {
-                    int32_t *sm = p.dbg_sm + (((2 * t + e) * p.rows + rs + row) * nb + blk) * 2;
-                    sm[0] = S[r][e];
-                    sm[1] = M;
-                }
-            }
-        }
         __syncwarp();       // every lane is done with this ring slot
-        issue(c + STAGES);  // refill it with this warp's column of tile c + STAGES
+        issue(T + STAGES);  // refill it with this warp's column of tile T + STAGES
 
-        // ---- post the terms; the last warp to arrive adds every (row, vector)'s terms --------
-        const int rslot = c % TC_RED;
+        // ---- post the terms; the last warp to arrive adds the run's terms of every (row,
+        // vector) -------------------------------------------------------------------------------
+        const int rslot = T % TC_RED;
         int ok = 1;
         if (lane == 0) {  // the slot's previous tile must have been summed (bounded wait)
             const uint64_t t0 = globaltimer_ns();
-            while (s_fin[rslot] != c - TC_RED) {
+            while (s_fin[rslot] != T - TC_RED) {
                 if (globaltimer_ns() - t0 > wait_ns) {
                     ok = 0;
                     atomicOr(p.err, ERRBIT_QMV_WAIT);
@@ -407,21 +573,40 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
             cp_async_wait<0>();  // no copy may land after the warp is gone
             return;
         }
-        float *red = s_red + ((size_t)rslot * nb + blk) * TC_ROWS * 8;
+        float *red = s_red + ((size_t)rslot * RW + warp) * TC_ROWS * 8;
         *reinterpret_cast<float2 *>(red + g * 8 + 2 * t) = make_float2(term[0][0], term[0][1]);
         *reinterpret_cast<float2 *>(red + (g + 8) * 8 + 2 * t) = make_float2(term[1][0], term[1][1]);
         __syncwarp();
         unsigned last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&s_cnt[rslot], 1u) == (unsigned)(nb - 1);
+            last = atomicAdd(&s_cnt[rslot], 1u) == (unsigned)(run_nb - 1);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence_block();
-            // declared order: groups of four blocks (t0 + t1) + (t2 + t3), absent blocks +0; runs
-            // of four groups ((G0 + G1) + G2) + G3, absent groups +0 (one run: nb <= 16)
-            const float *base = s_red + (size_t)rslot * nb * TC_ROWS * 8;
+            const bool final_run = !MULTI || r == runs - 1;
+            if (MULTI && final_run && runs > 1) {  // the tile's earlier runs must have been summed (bounded)
+                int ok2 = 1;
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (s_done[c] != runs - 1) {
+                        if (globaltimer_ns() - t0 > wait_ns) {
+                            ok2 = 0;
+                            atomicOr(p.err, ERRBIT_QMV_WAIT);
+                            break;
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok2, 0)) {
+                    cp_async_wait<0>();
+                    return;
+                }
+                __threadfence_block();
+            }
+            // declared order: groups of four blocks (t0 + t1) + (t2 + t3), absent blocks +0; a
+            // run is ((G0 + G1) + G2) + G3, absent groups +0; the row adds its runs left to right
+            const float *base = s_red + (size_t)rslot * RW * TC_ROWS * 8;
             for (int o = lane; o < TC_ROWS * 8; o += 32) {
                 const int row = o >> 3, v = o & 7;
                 if (row < nr && v < B) {
@@ -431,40 +616,55 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
                         float x4[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            x4[i] = 4 * q4 + i < nb ? base[(4 * q4 + i) * TC_ROWS * 8 + o] : 0.0f;
+                            x4[i] = 4 * q4 + i < run_nb ? base[(4 * q4 + i) * TC_ROWS * 8 + o] : 0.0f;
                         const float G = __fadd_rn(__fadd_rn(x4[0], x4[1]), __fadd_rn(x4[2], x4[3]));
                         run = q4 == 0 ? G : __fadd_rn(run, G);
                     }
-                    p.y[(int64_t)v * p.rows + rs + row] = run;
+                    const int prow = c * TC_ROWS + row;  // the row within this CTA
+                    if (!final_run) {
+                        s_run[((size_t)r * p.tc_rows + prow) * 8 + v] = run;
+                    } else {
+                        float acc = run;
+                        if (MULTI && runs > 1) {
+                            acc = s_run[(size_t)prow * 8 + v];
+                            for (int rp = 1; rp < runs - 1; ++rp)
+                                acc = __fadd_rn(acc, s_run[((size_t)rp * p.tc_rows + prow) * 8 + v]);
+                            acc = __fadd_rn(acc, run);
+                        }
+                        p.y[(int64_t)v * p.rows + rs + row] = acc;
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) {
                 s_cnt[rslot] = 0;
                 __threadfence_block();
-                s_fin[rslot] = c;
+                if (MULTI && !final_run)  // finishers of one row tile's runs may overlap
+                    atomicAdd(const_cast<int *>(&s_done[c]), 1);
+                s_fin[rslot] = T;
             }
         }
     }
     cp_async_wait<0>();  // no copy may land after the CTA is gone
 }
 
-template <int F, int STAGES>
+template <int F, int STAGES, bool MULTI>
 qmd_status launch_tc_stages(const QmvKParams &kp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
-    return mode == QMV_PACK   ? launch_kernel<qmv_tc_kernel<F, QMV_PACK, STAGES>>(kp, plan, s)
-           : mode == QMV_DUMP ? launch_kernel<qmv_tc_kernel<F, QMV_DUMP, STAGES>>(kp, plan, s)
-                              : launch_kernel<qmv_tc_kernel<F, QMV_PLAIN, STAGES>>(kp, plan, s);
+    return mode == QMV_PACK   ? launch_kernel<qmv_tc_kernel<F, QMV_PACK, STAGES, MULTI>>(kp, plan, s)
+           : mode == QMV_DUMP ? launch_kernel<qmv_tc_kernel<F, QMV_DUMP, STAGES, MULTI>>(kp, plan, s)
+                              : launch_kernel<qmv_tc_kernel<F, QMV_PLAIN, STAGES, MULTI>>(kp, plan, s);
 }
 
 template <int F>
 qmd_status launch_qmv_tc(const QmvKParams &kp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
+    const bool multi = kp.nb > TC_RUN;
     switch (plan.stages) {
     case 3:
-        return launch_tc_stages<F, 3>(kp, plan, mode, s);
+        return multi ? launch_tc_stages<F, 3, true>(kp, plan, mode, s) : launch_tc_stages<F, 3, false>(kp, plan, mode, s);
     case 4:
-        return launch_tc_stages<F, 4>(kp, plan, mode, s);
+        return multi ? launch_tc_stages<F, 4, true>(kp, plan, mode, s) : launch_tc_stages<F, 4, false>(kp, plan, mode, s);
     }
     return QMD_ERR_SHAPE;
 }

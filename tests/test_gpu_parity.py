@@ -284,7 +284,7 @@ def test_bind_q6k_matches_oracle_split():
 def test_refused_calls_write_nothing():
     """Every buffer here is large enough for the largest shape passed, so a call that the host
     wrongly accepted could not read or write outside its buffers."""
-    rows, Kmax, Bmax = 16, 65536, 8
+    rows, Kmax, Bmax = 16, 1 << 20, 8
     W = torch.zeros(rows * (Kmax // 256) * 144, dtype=torch.uint8, device=DEV)
     xq = q.Q8K.empty(Bmax, Kmax, DEV)
     buf, y = poisoned_y(Bmax, rows)
@@ -292,13 +292,28 @@ def test_refused_calls_write_nothing():
     assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 500, 1, None) == 3
     assert L.qmd_qmatvec(q.Q4_K, W.data_ptr() + 8, None, xq.ptrs(), y.data_ptr(), rows, 512, 1, None) == 5
     assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 512, 9, None) == 4
-    # above the K limits (32768 at batch <= 2, 16384 above)
-    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, Kmax, 1, None) == 6
-    assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 32768, 3, None) == 6
+    # rows too long for either kernel: 4096 blocks (the tensor-core kernel's 255 earlier runs'
+    # sums do not fit beside its rings), and past the 2^20-block limit
+    for B in (1, 3, 8):
+        assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, Kmax, B, None) == 6
     assert L.qmd_qmatvec(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, 256 << 21, 1, None) == 6
     torch.cuda.synchronize()
     assert torch.isnan(y).all() and guard_intact(buf, Bmax, rows)
     q.get_device_error()
+
+
+@pytest.mark.parametrize("fmtname", ["q4k", "q6k"])
+@pytest.mark.parametrize("rows,K,batch", [(40, 65536, 1), (21, 32768, 3), (40, 20480, 4), (300, 36864, 2)])
+def test_long_rows_beyond_the_dp4a_limit(fmtname, rows, K, batch):
+    """Rows the dp4a kernel cannot take (more than 128 blocks at one or two vectors, 64 above)
+    run on the tensor-core kernel run by run, bit-identical to the same-order oracle."""
+    info = q.launch_info(QFMT[fmtname], rows, K, batch)
+    assert info["rows_per_stage"] == 16 and info["threads"] == 512
+    seed = rows + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    check_against_oracle(fmtname, Wg, x, y)
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
@@ -371,55 +386,90 @@ def test_fused_refusals():
 
 # ---- batches of 3..8 on the tensor cores: the same bits as the dp4a kernel -----------------------------
 DP4A_ONLY = 2  # launch flag: keep batches of 5..8 on the dp4a kernel
+TC_ALL = 4     # launch flag: every batch of 3..8 on the tensor-core kernel (long rows run by run)
 
 
-@pytest.mark.parametrize("fmtname", ["q4k", "q5k"])
+# rows of one run of at most 16 blocks, and longer rows walked run by run: 17 blocks (a run of
+# one block after a full one), one 16-row tile per CTA with 3 and 8 runs (the finishers of a
+# tile's runs overlap), the 14336-wide down projection
+TC_SHAPES = [(1000, 4096), (37, 256), (300, 2048), (17, 3840), (4099, 1280),
+             (77, 4352), (16, 12288), (200, 14336), (33, 8192), (5, 32768)]
+
+
+@pytest.mark.parametrize("fmtname", ["q4k", "q5k", "q6k"])
 @pytest.mark.parametrize("batch", [5, 6, 7, 8])
-@pytest.mark.parametrize("rows,K", [(1000, 4096), (37, 256), (300, 2048), (17, 3840), (4099, 1280)])
+@pytest.mark.parametrize("rows,K", TC_SHAPES)
 def test_tensor_core_path_equals_dp4a_path(fmtname, batch, rows, K):
     seed = 3 * rows + K + batch
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
     xq = gpu_pack(x)
-    info = q.launch_info(QFMT[fmtname], rows, K, batch)
-    assert info["threads"] == 32 * (K // 256) and info["rows_per_stage"] == 16  # the tensor-core plan
-    y_tc = run_matvec(fmtname, Wg, xq, rows, K, batch)
-    q.debug_set_launch_flags(DP4A_ONLY)
+    # the default plan: the tensor cores for Q4_K / Q5_K rows of at most 16 blocks and for rows
+    # the dp4a kernel cannot take, the dp4a kernel otherwise
+    default_tc = (fmtname != "q6k" and K <= 4096) or K > 16384
+    assert (q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16) == default_tc
+    q.debug_set_launch_flags(TC_ALL)
     try:
-        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] != 16
-        y_dp = run_matvec(fmtname, Wg, xq, rows, K, batch)
+        info = q.launch_info(QFMT[fmtname], rows, K, batch)
+        assert info["threads"] == 32 * min(K // 256, 16) and info["rows_per_stage"] == 16  # the tensor-core plan
+        y_tc = run_matvec(fmtname, Wg, xq, rows, K, batch)
     finally:
         q.debug_set_launch_flags(0)
-    assert np.array_equal(y_tc.view(np.uint32), y_dp.view(np.uint32))
+    if K <= 16384:  # the dp4a kernel's limit above two vectors
+        q.debug_set_launch_flags(DP4A_ONLY)
+        try:
+            assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] != 16
+            y_dp = run_matvec(fmtname, Wg, xq, rows, K, batch)
+        finally:
+            q.debug_set_launch_flags(0)
+        assert np.array_equal(y_tc.view(np.uint32), y_dp.view(np.uint32))
     idx = _sample_rows(rows, 96, seed)
     check_against_oracle(fmtname, Wg, x, y_tc, rows_idx=idx)
 
 
-@pytest.mark.parametrize("fmtname", ["q4k", "q5k"])
-def test_tensor_core_extreme_magnitudes(fmtname):
+@pytest.mark.parametrize("fmtname,K", [("q4k", 4096), ("q5k", 4096), ("q4k", 8192), ("q6k", 4096),
+                                       ("q6k", 14336)])
+def test_tensor_core_extreme_magnitudes(fmtname, K):
     """The largest codes and scales against activations of +-127: the accumulator's partial
-    sums reach their bound, and the integer dots must still be exact."""
-    rows, K, batch = 48, 4096, 8
+    sums reach their bound, and the integer dots must still be exact (Q6_K: scales -128 and
+    127, codes 63 and 0, so a two-sub-block sum of scaled dots reaches 2 x 128 x 16 x 32 x 127)."""
+    rows, batch = 48, 8
     Wg = synth.weights(fmtname, 77, rows, K).copy()
-    off = 48 if fmtname == "q5k" else 16
-    Wg[:, :, 4:16] = 0xFF                  # every scale and min 63
-    Wg[:, :, off:] = 0xFF                  # every nibble 15
-    if fmtname == "q5k":
-        Wg[:, :, 16:48] = 0xFF             # every fifth bit: codes 31
-    Wg[::2, :, off:] = 0x00                # even rows: codes 0 (only the min term)
+    if fmtname == "q6k":
+        Wg[:, :, 0:192] = 0xFF             # ql, qh: every code 63 (q - 32 = 31)
+        Wg[::2, :, 0:192] = 0x00           # even rows: every code 0 (q - 32 = -32)
+        Wg[:, :, 192:208] = 0x80           # every scale -128
+        Wg[1::4, :, 192:208] = 0x7F        # rows 1, 5, ...: every scale 127
+    else:
+        off = 48 if fmtname == "q5k" else 16
+        Wg[:, :, 4:16] = 0xFF              # every scale and min 63
+        Wg[:, :, off:] = 0xFF              # every nibble 15
+        if fmtname == "q5k":
+            Wg[:, :, 16:48] = 0xFF         # every fifth bit: codes 31
+        Wg[::2, :, off:] = 0x00            # even rows: codes 0 (only the min term)
     x = np.ones((batch, K), np.float32)
     x[1::2] = -1.0                         # +-1 everywhere: codes +-127
     x[2, ::3] = -1.0                       # mixed signs
     x[4] = synth.activations(78, 1, K)[0]
-    y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    q.debug_set_launch_flags(TC_ALL)
+    try:
+        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16  # the tensor-core plan
+        y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+        if fmtname == "q6k":
+            body, prefix = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+            yd, dots, sm = q.debug_qmatvec_dump(q.Q6_K_SPLIT, body, prefix, gpu_pack(x))
+        else:
+            yd, dots, sm = q.debug_qmatvec_dump(QFMT[fmtname], dev(Wg.reshape(rows, -1)), None, gpu_pack(x))
+        q.get_device_error()
+    finally:
+        q.debug_set_launch_flags(0)
     check_against_oracle(fmtname, Wg, x, y)
-    yd, dots, sm = q.debug_qmatvec_dump(QFMT[fmtname], dev(Wg.reshape(rows, -1)), None, gpu_pack(x))
-    q.get_device_error()
     oqs, _, _ = O.q8k_pack(x)
     dots = dots.cpu().numpy()
+    nsub = 16 if fmtname == "q6k" else 8
     for v in range(batch):
         for r in (0, 1, 2, 47):
-            assert np.array_equal(dots[v, r][:, :8], O.subdots(OFMT[fmtname], Wg[r], oqs[v]))
+            assert np.array_equal(dots[v, r][:, :nsub], O.subdots(OFMT[fmtname], Wg[r], oqs[v]))
 
 
 # ---- several host threads, each with its own stream: the same bits as one thread ---------------------
@@ -468,13 +518,14 @@ def test_concurrent_host_threads():
 
 
 # ---- census: every kernel variant the library can launch, value-checked --------------------------------
-CENSUS = [(f, b, fused, dp4a) for f in ("q4k", "q5k", "q6k") for b in range(1, 9) for fused in (False, True)
-          for dp4a in ((False, True) if (b >= 5 and f != "q6k") else (False,))]
+CENSUS = [(f, b, fused, flags) for f in ("q4k", "q5k", "q6k") for b in range(1, 9) for fused in (False, True)
+          for flags in ((0, DP4A_ONLY, TC_ALL) if b >= 5 else (0, TC_ALL) if b >= 3 else (0,))]
 
 
-@pytest.mark.parametrize("fmtname,batch,fused,dp4a_only", CENSUS,
-                         ids=[f"{f}-b{b}-{'fused' if fu else 'packed'}{'-dp4a' if d else ''}" for f, b, fu, d in CENSUS])
-def test_census_every_variant(fmtname, batch, fused, dp4a_only):
+@pytest.mark.parametrize("fmtname,batch,fused,flags", CENSUS,
+                         ids=[f"{f}-b{b}-{'fused' if fu else 'packed'}{['', '', '-dp4a', '', '-tc'][fl]}"
+                              for f, b, fu, fl in CENSUS])
+def test_census_every_variant(fmtname, batch, fused, flags):
     """Each (format, batch, fused or packed input, kernel layout) the plan can choose, on a small
     ragged case, bit-identical to the same-order oracle; plus the recording variant's dots."""
     rows, K = 45, 1024
@@ -486,7 +537,7 @@ def test_census_every_variant(fmtname, batch, fused, dp4a_only):
         W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
     else:
         W, Wa = dev(Wg.reshape(rows, -1)), None
-    q.debug_set_launch_flags(DP4A_ONLY if dp4a_only else 0)
+    q.debug_set_launch_flags(flags)
     try:
         buf, y = poisoned_y(batch, rows)
         if fused:
@@ -524,7 +575,7 @@ def _random_cases(n=24, seed=2024):
 
 @pytest.mark.parametrize("fmtname,rows,K,batch,fused,seed", _random_cases())
 def test_random_small_shapes(fmtname, rows, K, batch, fused, seed):
-    if batch > 2 and K > 16384:
+    if 2 < batch < 5 and K > 16384:
         pytest.skip("above the batch's K limit")
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
