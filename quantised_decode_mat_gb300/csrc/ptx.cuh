@@ -53,17 +53,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Wait for phase `parity` of the barrier to complete; give up after limit_ns.
+// try_wait with a suspend-time hint: the thread may sleep up to hint_ns in the barrier unit,
+// waking when the phase completes, instead of spinning on issue slots other warps could use.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete; give up after limit_ns.  (Spinning
+// without the hint took about 15 % of a batch-1 mat-vec's issued instructions.)
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i)
-        if (mbar_try_wait(bar, parity))
-            return true;
+    if (mbar_try_wait(bar, parity))
+        return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_hint(bar, parity, 2000u))
             return true;
         if (globaltimer_ns() - t0 > limit_ns)
             return false;
