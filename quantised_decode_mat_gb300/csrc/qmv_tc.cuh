@@ -1,5 +1,5 @@
-// qmv_tc.cuh -- the batched decode mat-vec (5..8 vectors) on the tensor cores, for Q4_K, Q5_K
-// and Q6_K (split) rows of any length.
+// qmv_tc.cuh -- the decode mat-vec on the tensor cores, for Q4_K, Q5_K and Q6_K (split) rows
+// of any length: batches of 5..8 vectors, and rows too long for the dp4a kernel at any batch.
 //
 // Same computation and the same bits as qmv_kernel (qmv.cuh): integer sub-block dots, the
 // per-block rank-one epilogue, the declared row order ("Language models on the device: the
@@ -47,7 +47,7 @@ namespace qmd {
 constexpr int TC_ROWS = 16;      // rows per tile (the MMA's M)
 constexpr int TC_RED = 2;        // tiles whose block terms can be pending at once
 constexpr int TC_RUN = 16;       // blocks per run (warps per CTA at most)
-constexpr int TC_MIN_BATCH = 5;  // smallest batch the plan gives to this kernel
+constexpr int TC_MIN_BATCH = 5;  // smallest batch the plan gives to this kernel for rows the dp4a kernel can take
 
 __host__ __device__ constexpr int tc_block_bytes(int fmt)
 {
