@@ -12,8 +12,9 @@
  *
  * Conventions for every call
  *  - All pointers to tensors are DEVICE pointers, owned by the caller, who also owns the
- *    stream.  The library allocates no device or host memory, keeps no per-call state, and
- *    never synchronises the stream (except qmd_get_device_error, which says so).
+ *    stream.  The library allocates no device or host memory on any compute call (only the
+ *    measurement helper qmd_measure_alu creates and frees its own scratch), keeps no per-call
+ *    state, and never synchronises the stream (except qmd_get_device_error, which says so).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls
  *    are asynchronous; buffers must stay live until the stream has passed the work.
  *  - Arguments are validated on the host before anything is launched.  A call that returns
@@ -25,9 +26,10 @@
  *  - Launch order: qmd_q8k_pack, qmd_rmsnorm_q8k_pack and qmd_qmatvec are launched as
  *    programmatic dependents of the preceding kernel in the stream.  Before waiting for that
  *    kernel to finish they read only weight buffers (W, W_aux; the norm gain g); everything
- *    else is read and written after it has finished.  Weights therefore must not be written by the kernel launched immediately
- *    before them in the same stream unless that kernel signals completion only by exiting
- *    (every kernel not written for programmatic launch does; so do this library's bind calls).
+ *    else is read and written after it has finished.  Weights therefore must not be written
+ *    by the kernel launched immediately before them in the same stream unless that kernel
+ *    signals completion only by exiting (every kernel not written for programmatic launch
+ *    does; so do this library's bind calls).
  */
 #ifndef QMD_H
 #define QMD_H
