@@ -226,11 +226,10 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     const uint32_t bar0 = smem_addr(smem + L.bar_off);
     const uint32_t ring0 = smem_addr(smem);
 
-    // Stream chunk c (rows r0 + c*TR ..) into stage c % stages.  The chunk's rows are one
+    // Stream chunk c (rows r0 + c*TR ..) into stage st = c % stages.  The chunk's rows are one
     // contiguous span of W, copied by as few bulk copies as possible (each issue costs the
     // issuing thread tens of nanoseconds), plus one copy of the rows' Q6_K prefix.
-    auto issue = [&](int c) {
-        const int st = c % p.stages;
+    auto issue = [&](int c, int st) {
         const int64_t rs = r0 + (int64_t)c * TR;
         const int nr = (int)min((int64_t)TR, r1 - rs);
         const uint32_t bar = bar0 + 8u * st;
@@ -257,7 +256,7 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     // the first stages, one per warp (issuing a bulk copy costs its thread tens of ns)
     for (int c = warp; c < min(p.stages, nch); c += NWT)
         if (lane == 0)
-            issue(c);
+            issue(c, c);
 
     pdl_launch_dependents();
     pdl_wait();  // activations come from earlier work in the stream
@@ -370,10 +369,13 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     }
 
     const unsigned long long wait_ns = p.wait_ns;
+    // this chunk's stage (c % stages) and barrier phase ((c / stages) & 1), stepped without a
+    // division: an integer division by the runtime ring depth on every chunk cost 4 % of the
+    // batch-1 kernel's instructions
+    int st = 0;
+    uint32_t parity = 0u;
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
-        const int st = c % p.stages;
-        const uint32_t parity = (uint32_t)(c / p.stages) & 1u;
         if (!mbar_wait_bounded(bar0 + 8u * st, parity, wait_ns)) {
             // A copy did not land in time: flag it, wait (bounded) for the copies that may
             // still be in flight so that none writes shared memory after the CTA exits, leave.
@@ -581,8 +583,12 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
             if (lane == 0) {
                 s_cnt[st] = 0;
                 if (c + p.stages < nch)
-                    issue(c + p.stages);  // every warp of the CTA is done with this stage
+                    issue(c + p.stages, st);  // every warp of the CTA is done with this stage
             }
+        }
+        if (++st == p.stages) {
+            st = 0;
+            parity ^= 1u;
         }
     }
 }
