@@ -639,7 +639,9 @@ qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t
         }
     }
     // Persistent grid: no more CTAs than can be resident at once (rows are split by gridDim).
-    int grid = plan.grid < cap ? plan.grid : cap;
+    // The tensor-core kernel keeps its planned grid, which sized its per-CTA run sums; its
+    // CTAs never wait for one another, so any that do not fit at once run later.
+    int grid = (plan.grid < cap || plan.tc_rows > 0) ? plan.grid : cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)plan.threads);

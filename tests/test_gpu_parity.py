@@ -316,6 +316,24 @@ def test_long_rows_beyond_the_dp4a_limit(fmtname, rows, K, batch):
     check_against_oracle(fmtname, Wg, x, y)
 
 
+@pytest.mark.parametrize("cps", [1, 3, 8])
+def test_long_rows_with_forced_ctas_per_sm(cps):
+    """A forced CTAs-per-SM count can ask for more resident CTAs than fit; the run-by-run
+    tensor-core kernel keeps its planned grid (its run sums are sized for it), and the CTAs that
+    do not fit at once run later."""
+    fmtname, rows, K, batch = "q4k", 700, 20480, 3
+    seed = 91 + cps
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    q.debug_set_plan(0, 0, 0, cps)
+    try:
+        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16
+        y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    finally:
+        q.debug_set_plan()
+    check_against_oracle(fmtname, Wg, x, y)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     q.debug_wait_timeout(2_000_000)  # 2 ms
     with pytest.raises(q.QmdError, match="QMD_ERR_DEVICE_TIMEOUT"):
