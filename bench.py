@@ -457,6 +457,27 @@ def run_ours(args):
     msr = time_graph(torch, gr, reps, stream) / len(rms)
     br = sum(4 * p.x.numel() * 3 + 4 * 4096 + p.xq.batch * (4096 + 16 * 4 + 16 * 16) for p in rms) / len(rms)
 
+    # the same normalised inputs feeding their mat-vecs: RMSNorm + pack, then the mat-vec (two
+    # launches), against qmd_qmatvec_rmsnorm_x (one launch); h written to its own buffer in both
+    hbuf = [torch.empty_like(p.x) for p in rms]
+
+    def run_norm_two():
+        for p, r, h in zip(rms, resid, hbuf):
+            q.rmsnorm_q8k_pack(p.x, r, gain, 1e-6, h_out=h, out=p.xq)
+            q.qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows)
+
+    def run_norm_one():
+        for p, r, h in zip(rms, resid, hbuf):
+            q.qmatvec_rmsnorm_x(p.fmt, p.W, p.W_aux, p.x, r, gain, 1e-6, h_out=h, y=p.y, rows=p.rows)
+
+    gn2 = step.capture(run_norm_two)
+    gn1 = step.capture(run_norm_one)
+    gn2.replay()
+    gn1.replay()
+    msn2 = time_graph(torch, gn2, reps, stream) / len(rms)
+    msn1 = time_graph(torch, gn1, reps, stream) / len(rms)
+    bn = sum(p.weight_bytes + 4 * p.x.numel() * 3 + 4 * 4096 + 4 * p.xq.batch * p.rows for p in rms) / len(rms)
+
     # end to end: inputs from pinned host memory in, outputs to pinned host memory out, every step
     x_host = torch.empty(step.x_all.shape, dtype=step.x_all.dtype, pin_memory=True)
     y_host = torch.empty(step.y_all.shape, dtype=step.y_all.dtype, pin_memory=True)
@@ -507,6 +528,11 @@ def run_ours(args):
                                  "note": "RMSNorm + residual add + pack of a 4096-wide input (x, residual in "
                                          "place, gain read; codes, scales, sums written), timed as a chain of "
                                          "its launches beside the step"},
+            "qmv_rmsnorm": {"launches_per_step": 0, "us_per_launch": msn1 * 1e3, "gbs": bn / (msn1 * 1e-3) / 1e9,
+                            "two_launch_us": msn2 * 1e3, "two_launch_gbs": bn / (msn2 * 1e-3) / 1e9,
+                            "note": "residual add + RMSNorm + pack + mat-vec in one launch (qmd_qmatvec_rmsnorm_x) "
+                                    "on the 4096-wide projections (q|k|v, gate|up), against RMSNorm-pack then "
+                                    "mat-vec; bytes = weights + x, residual, h + gain + y; chains beside the step"},
         },
         "e2e": {"value": world * nbytes["algorithmic"] / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": step.x_all.numel() * 4, "d2h_bytes_per_step": step.y_all.numel() * 4,
@@ -514,7 +540,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": step.launches * args.steps,
     }
-    del g, g4, g6, gp, ge, gr
+    del g, g4, g6, gp, ge, gr, gn1, gn2
     if rank == 0 and not args.no_configs:
         line["configs"] = time_configs(torch, q, torch.device(f"cuda:{local_rank}"), peak)
     if rank == 0 and args.cpu_layers > 0:

@@ -59,7 +59,8 @@ typedef enum qmd_status {
     QMD_ERR_LAUNCH = 7,                /* the CUDA runtime refused the launch (see qmd_last_error_detail) */
     QMD_ERR_DEVICE_TIMEOUT = 8,        /* a bounded wait inside a kernel gave up (qmd_get_device_error) */
     QMD_ERR_DEVICE = 9,                /* no usable CUDA device, or it is not an sm_103 part */
-    QMD_ERR_VALUE = 10                 /* a scalar argument is out of its range (e.g. eps < 0 or not finite) */
+    QMD_ERR_VALUE = 10                 /* a scalar argument is out of its range (e.g. eps < 0 or not finite),
+                                          or buffers that must not overlap do */
 } qmd_status;
 
 /* Weight formats, named by their GGUF type ids. */
@@ -184,6 +185,30 @@ qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_co
  */
 qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
                          float *y, int64_t rows, int64_t K, int batch, void *stream);
+
+/*
+ * qmd_qmatvec_rmsnorm_x -- the residual add, the RMSNorm, the q8_K pack and the mat-vec in one
+ * launch: y is exactly qmd_qmatvec(fmt, W, W_aux, qmd_rmsnorm_q8k_pack(x, r, g, eps), ...),
+ * with the same bits -- the same h, the same sum-of-squares order, the same codes ("Language
+ * models on the device: the cajeta-llm kernels", §2.6 the normalisation and residual kernels
+ * ahead of the device quantiser of §1 and the decode mat-vecs, here one launch).  Each CTA
+ * forms h and its sum of squares itself, so the normalised vector never goes to memory and a
+ * dependent launch leaves the stream.
+ *   x, r, g, eps  as qmd_rmsnorm_q8k_pack (r may be NULL)
+ *   h_out   f32 [batch][K], 16-byte aligned, receives h (written by one CTA); or NULL.  Unlike
+ *           qmd_rmsnorm_q8k_pack it must NOT overlap x, r or g, since every CTA still reads x
+ *           and r while it is written (QMD_ERR_VALUE).
+ *   xq_out  optional, as qmd_qmatvec_x: the packed codes of the normalised vector
+ * Other arguments as qmd_qmatvec.  Limits: the dp4a kernel's (every K up to 32768 at batch
+ * <= 2 and 16384 above) with the packed codes in shared memory, as qmd_qmatvec_x; longer rows
+ * give QMD_ERR_SHAPE (pack with qmd_rmsnorm_q8k_pack and call qmd_qmatvec instead).
+ * Errors: NULL (W, x, g, y, a partial xq_out, or W_aux for Q6_K_SPLIT), FORMAT,
+ * K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, VALUE (eps, or h_out overlapping x, r or g),
+ * SHAPE, DEVICE, LAUNCH.
+ */
+qmd_status qmd_qmatvec_rmsnorm_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, const float *r,
+                                 const float *g, float eps, float *h_out, qmd_q8k xq_out, float *y, int64_t rows,
+                                 int64_t K, int batch, void *stream);
 
 /*
  * qmd_q6k_prefix_stride -- entries (f16) per row of the Q6_K scale prefix: nb rounded up to

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             "qmd_rmsnorm_q8k_pack": ([vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, i64, i32, vp], i32),
             "qmd_qmatvec": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_qmatvec_x": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
+            "qmd_qmatvec_rmsnorm_x": ([i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, vp, i64, i64, i32, vp],
+                                      i32),
             "qmd_q6k_prefix_stride": ([i64], i64),
             "qmd_q6k_split_bytes": ([i64, i64, sizep, sizep], i32),
             "qmd_bind_q6k": ([vp, vp, vp, i64, i64, vp], i32),
@@ -180,6 +182,22 @@ def qmatvec_x(fmt: int, W, W_aux, x, y=None, rows: int | None = None, xq_out: Q8
     out = xq_out.ptrs() if xq_out is not None else Q8KPtrs(None, None, None)
     _check(lib().qmd_qmatvec_x(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
                                _stream(stream)))
+    return y
+
+
+def qmatvec_rmsnorm_x(fmt: int, W, W_aux, x, r, g, eps: float, h_out=None, y=None, rows: int | None = None,
+                      xq_out: Q8K | None = None, stream=None):
+    """qmd_qmatvec_rmsnorm_x: y f32 [batch, rows] = W (fmt) x rmsnorm_q8k_pack(x, r, g, eps), in one
+    launch.  x, r (may be None), h_out (optional; must not overlap x, r or g) f32 [batch, K];
+    g f32 [K]."""
+    import torch
+    rows = W.shape[0] if rows is None else rows
+    batch, K = x.shape
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    out = xq_out.ptrs() if xq_out is not None else Q8KPtrs(None, None, None)
+    _check(lib().qmd_qmatvec_rmsnorm_x(fmt, _ptr(W), _ptr(W_aux), _ptr(x), _ptr(r), _ptr(g), float(eps),
+                                       _ptr(h_out), out, _ptr(y), rows, K, batch, _stream(stream)))
     return y
 
 

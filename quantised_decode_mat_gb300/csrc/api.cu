@@ -112,10 +112,10 @@ static int default_rows_per_stage(bool q6, int batch)
 // stage, mode); if the lookup fails, the launch bound's worst case.
 static int kernel_regs(int fmt, int batch, int PR, int mode)
 {
-    static std::atomic<int> cache[3][QMD_MAX_BATCH + 1][4][3];
+    static std::atomic<int> cache[3][QMD_MAX_BATCH + 1][4][4];
     const int fi = fmt == QMD_Q6_K_SPLIT ? 2 : fmt == QMD_Q5_K ? 1 : 0;
     const int pi = PR >= 8 ? 3 : PR >= 4 ? 2 : PR >= 2 ? 1 : 0;
-    if (batch < 1 || batch > QMD_MAX_BATCH || mode < 0 || mode > 2)
+    if (batch < 1 || batch > QMD_MAX_BATCH || mode < 0 || mode > 3)
         return 65536 / qmv_max_threads(batch, PR, mode);
     std::atomic<int> &slot = cache[fi][batch][pi][mode];
     int r = slot.load();
@@ -172,7 +172,8 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
 qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
 {
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
-    const bool fused = mode == QMV_PACK;
+    const bool norm = mode == QMV_NORM;
+    const bool fused = mode == QMV_PACK || norm;  // the CTAs pack the activations themselves
     const int row_bytes = nb * (q6 ? 208 : fmt == QMD_Q5_K ? 176 : 144);
     const int pre_bytes = q6 ? align_up(nb, 8) * 2 : 0;
     pl->row_bytes = row_bytes;
@@ -185,13 +186,14 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // run by run.  One warp per block of a run of 16 blocks, each with its own ring of 16-row
     // tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per warp) that fits
     // beside the run sums (and, fused, the packed activations).  A forced ring cap below 3
-    // selects the dp4a kernel, and so does a shape that does not fit.
+    // selects the dp4a kernel, and so does a shape that does not fit.  The RMSNorm form exists
+    // only in the dp4a kernel.
     const int fst = g_force_stages.load();
     pl->tc_rows = 0;
     const bool tc_faster = batch >= TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
     const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);
     const bool tc_forced = (launch_flags() & LAUNCH_TC_ALL) && batch >= 3;
-    if ((tc_faster || dp4a_cannot || tc_forced) && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
+    if (!norm && (tc_faster || dp4a_cannot || tc_forced) && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
         (fst <= 0 || fst >= 3)) {
         const int RW = nb < TC_RUN ? nb : TC_RUN;
         const int64_t ntiles = (rows + TC_ROWS - 1) / TC_ROWS;
@@ -301,6 +303,11 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         RG = max_threads / (WR * 32);
     if (RG < 1)
         RG = 1;
+    // The RMSNorm form sums the squares with the first 256 threads of each CTA.
+    if (norm && RG * WR < 8)
+        RG = (8 + WR - 1) / WR;
+    if (norm && RG * WR * 32 > max_threads)
+        return QMD_ERR_SHAPE;
     const int TR = RG * PR;
     const int64_t sb64 = (int64_t)TR * (row_bytes + pre_bytes);
     if (sb64 > dev.smem_optin)
@@ -311,7 +318,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         cps = 32 / (RG * WR) > 0 ? 32 / (RG * WR) : 1;
     if (cps > 8)
         cps = 8;
-    const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused, slots).total + 64;
+    const int fixed = qmv_smem_layout(0, stage_bytes, RG, WR, batch, nb, q6, fused, slots, norm).total + 64;
     // Ring depth: up to 8 stages, but 2 for two to four vectors -- bulk copies in flight together
     // share the SM's bandwidth, so a deeper ring delays its first stage, and the dot products,
     // with little headroom over the copies, never catch up (measured on the 7B shapes).
@@ -320,7 +327,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         return QMD_ERR_SHAPE;
     pl->layout = 0;
     pl->threads = RG * WR * 32;
-    pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused, slots).total;
+    pl->smem = qmv_smem_layout(pl->stages, stage_bytes, RG, WR, batch, nb, q6, fused, slots, norm).total;
     pl->WR = WR;
     pl->RG = RG;
     pl->PR = PR;
@@ -362,9 +369,24 @@ qmd_status check_k(int64_t K)
     return QMD_OK;
 }
 
+// Do [a, a + na) and [b, b + nb) bytes overlap?
+inline bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return a && b && pa < pb + nb && pb < pa + na;
+}
+
+// The RMSNorm form's extra arguments; g == NULL selects the other forms.
+struct NormArgs {
+    const float *r = nullptr;
+    const float *g = nullptr;
+    float eps = 0.0f;
+    float *h_out = nullptr;
+};
+
 qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                           int64_t rows, int64_t K, int batch, int32_t *dots, int32_t *sm, bool dump,
-                          const float *x, qmd_q8k xq_out, void *stream)
+                          const float *x, qmd_q8k xq_out, void *stream, const NormArgs &na = NormArgs())
 {
     if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
         return QMD_ERR_FORMAT;
@@ -389,13 +411,24 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
         (!fused && (!aligned(xq.qs, 16) || (!q6 && !aligned(xq.bsums, 16)) || !aligned(xq.d, 4))) ||
         (fused && !aligned(x, 16)) ||
         (fused && want_out && (!aligned(xq_out.qs, 16) || !aligned(xq_out.bsums, 16) || !aligned(xq_out.d, 4))) ||
-        (dump && (!aligned(dots, 16) || !aligned(sm, 16))))
+        (dump && (!aligned(dots, 16) || !aligned(sm, 16))) ||
+        (na.g && (!aligned(na.g, 16) || (na.r && !aligned(na.r, 16)) || (na.h_out && !aligned(na.h_out, 16)))))
         return QMD_ERR_MISALIGNED;
+    if (na.g) {
+        if (!(na.eps >= 0.0f) || !(na.eps <= 3.4028234663852886e38f))  // rejects NaN, negatives and +inf
+            return QMD_ERR_VALUE;
+        // h is written by one CTA while every CTA still reads x and r: they must not share bytes
+        const size_t vb = (size_t)batch * (size_t)K * sizeof(float);
+        if (overlaps(na.h_out, vb, x, vb) || overlaps(na.h_out, vb, na.r, vb) ||
+            overlaps(na.h_out, vb, na.g, (size_t)K * sizeof(float)))
+            return QMD_ERR_VALUE;
+    }
     DeviceInfo dev;
     if ((st = current_device(&dev)) != QMD_OK)
         return st;
     QmvPlan plan;
-    if ((st = qmv_plan(fmt, rows, nb, batch, dev, &plan, fused ? QMV_PACK : dump ? QMV_DUMP : QMV_PLAIN)) != QMD_OK)
+    const int mode = na.g ? QMV_NORM : fused ? QMV_PACK : dump ? QMV_DUMP : QMV_PLAIN;
+    if ((st = qmv_plan(fmt, rows, nb, batch, dev, &plan, mode)) != QMD_OK)
         return st;
     QmvArgs a;
     a.fmt = fmt;
@@ -414,6 +447,10 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
     a.xq_qs_out = fused && want_out ? xq_out.qs : nullptr;
     a.xq_d_out = fused && want_out ? xq_out.d : nullptr;
     a.xq_bs_out = fused && want_out ? xq_out.bsums : nullptr;
+    a.r = na.r;
+    a.g = na.g;
+    a.eps = na.eps;
+    a.h_out = na.h_out;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return q6 ? launch_qmv_q6k(a, plan, s) : fmt == QMD_Q5_K ? launch_qmv_q5k(a, plan, s) : launch_qmv_q4k(a, plan, s);
 }
@@ -476,6 +513,21 @@ qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const fl
         return QMD_ERR_NULL;
     const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
     return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream);
+}
+
+qmd_status qmd_qmatvec_rmsnorm_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, const float *r,
+                                 const float *g, float eps, float *h_out, qmd_q8k xq_out, float *y, int64_t rows,
+                                 int64_t K, int batch, void *stream)
+{
+    if (!x || !g)
+        return QMD_ERR_NULL;
+    const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
+    NormArgs na;
+    na.r = r;
+    na.g = g;
+    na.eps = eps;
+    na.h_out = h_out;
+    return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream, na);
 }
 
 qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq,

@@ -13,7 +13,7 @@ enum : unsigned {
     ERRBIT_QMV_WAIT = 1u,     // a mat-vec pipeline wait gave up
     ERRBIT_DEBUG_WAIT = 2u,   // the test-only wait kernel gave up (as intended)
     ERRBIT_DRAIN_WAIT = 4u,   // draining copies after a give-up also gave up
-    ERRBIT_PLAN = 8u,         // a launch got more rows per CTA than its shared memory was sized for
+    ERRBIT_PLAN = 8u,         // a launch whose geometry its plan does not allow (rows per CTA, threads)
 };
 
 struct DeviceInfo {
@@ -58,6 +58,10 @@ struct QmvArgs {
     int8_t *xq_qs_out;   // fused form: optional copy of the packed activations
     float *xq_d_out;
     int16_t *xq_bs_out;
+    const float *r = nullptr;  // RMSNorm form: optional residual
+    const float *g = nullptr;  // non-NULL selects the RMSNorm form (packs RMSNorm(x + r) * g)
+    float *h_out = nullptr;    // RMSNorm form: optional h = x + r, written by CTA 0
+    float eps = 0.0f;
 };
 
 struct QmvPlan {

@@ -13,6 +13,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Bytes of dynamic shared memory this CTA was launched with (PTX special register).
+__device__ __forceinline__ uint32_t dynamic_smem_bytes()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

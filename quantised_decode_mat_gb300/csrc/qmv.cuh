@@ -62,26 +62,31 @@ struct QmvKParams {
     int8_t *xq_qs_out;    // fused form, optional: the packed activations, written by CTA 0
     float *xq_d_out;
     int16_t *xq_bs_out;
+    const float *r;       // RMSNorm form: optional residual [B][K] (h = x + r, else h = x)
+    const float *g;       // RMSNorm form: gain [K]
+    float *h_out;         // RMSNorm form, optional: h, written by CTA 0
+    float eps;            // RMSNorm form
     unsigned *err;
     unsigned long long wait_ns;
 };
 
-// Kernel variants: plain; recording the integer arithmetic; packing f32 activations itself.
-enum QmvMode { QMV_PLAIN = 0, QMV_DUMP = 1, QMV_PACK = 2 };
+// Kernel variants: plain; recording the integer arithmetic; packing f32 activations itself;
+// packing the RMSNorm of x (+ a residual) itself.
+enum QmvMode { QMV_PLAIN = 0, QMV_DUMP = 1, QMV_PACK = 2, QMV_NORM = 3 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 struct SmemLayout {
-    int red_off, cnt_off, bar_off, dx_off, bs_off, acts_off, total;
+    int red_off, cnt_off, bar_off, dx_off, bs_off, acts_off, norm_off, total;
 };
 
 // Shared memory: ring [stages][stage_bytes] | red f32 [stages][RG][WR][slots] | counters u32
 // [stages] | mbarriers u64 [stages] | dx f32 [B][nb] | Q4_K bsums i16 [B][nb][8] | fused form:
-// the packed codes i8 [B][K].  slots: 8, or 16 when a stage has more than 8 (row, vector)
-// pairs per warp.
+// the packed codes i8 [B][K] | RMSNorm form: warp sums of squares f32 [B][8] and 1/rms f32 [B].
+// slots: 8, or 16 when a stage has more than 8 (row, vector) pairs per warp.
 __host__ __device__ inline SmemLayout qmv_smem_layout(int stages, int stage_bytes, int RG, int WR,
                                                       int B, int nb, bool q6, bool pack = false,
-                                                      int slots = 8)
+                                                      int slots = 8, bool norm = false)
 {
     SmemLayout L;
     int o = stages * stage_bytes;
@@ -100,6 +105,9 @@ __host__ __device__ inline SmemLayout qmv_smem_layout(int stages, int stage_byte
     L.acts_off = o;
     if (pack)
         o += B * nb * 256;
+    L.norm_off = o;
+    if (norm)
+        o += B * 9 * 4;
     L.total = align_up(o, 16);
     return L;
 }
@@ -196,7 +204,8 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
     constexpr bool Q5 = F == QMD_Q5_K;
     constexpr bool DUMP = MODE == QMV_DUMP;
-    constexpr bool PACK = MODE == QMV_PACK;
+    constexpr bool NORM = MODE == QMV_NORM;
+    constexpr bool PACK = MODE == QMV_PACK || NORM;  // both pack their activations themselves
     constexpr int P = PR * B;                                               // (row, vector) slots
     static_assert(P >= 1 && P <= 16, "PR x B must be at most 16");
     constexpr int PP = P > 8 ? 16 : P > 4 ? 8 : P > 2 ? 4 : P > 1 ? 2 : 1;  // padded to a power of two
@@ -218,13 +227,20 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     const int64_t r0 = p.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = p.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
     const int nch = (int)((r1 - r0 + TR - 1) / TR);
-    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, RG, WR, B, nb, Q6, PACK, SL);
+    const SmemLayout L = qmv_smem_layout(p.stages, p.stage_bytes, RG, WR, B, nb, Q6, PACK, SL, NORM);
     float *s_red = reinterpret_cast<float *>(smem + L.red_off);
     unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + L.cnt_off);
     const float *s_dx = reinterpret_cast<const float *>(smem + L.dx_off);
     const int16_t *s_bs = reinterpret_cast<const int16_t *>(smem + L.bs_off);
     const uint32_t bar0 = smem_addr(smem + L.bar_off);
     const uint32_t ring0 = smem_addr(smem);
+    // A launch whose plan does not fit the kernel: the RMSNorm form's sum of squares takes 256
+    // threads, and the layout must lie inside the dynamic shared memory the launch was given.
+    if ((NORM && NWT < 8) || (uint32_t)L.total > dynamic_smem_bytes()) {
+        if (tid == 0)
+            atomicOr(p.err, ERRBIT_PLAN);
+        return;
+    }
 
     // Stream chunk c (rows r0 + c*TR ..) into stage st = c % stages.  The chunk's rows are one
     // contiguous span of W, copied by as few bulk copies as possible (each issue costs the
@@ -276,7 +292,58 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
         float *dx = reinterpret_cast<float *>(smem + L.dx_off);
         int16_t *bs = reinterpret_cast<int16_t *>(smem + L.bs_off);
         const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
-        constexpr int QB = 4;  // blocks per warp whose loads are in flight together
+        float *s_inv = reinterpret_cast<float *>(smem + L.norm_off) + B * 8;  // RMSNorm form: 1/rms
+        if (NORM) {
+            // RMSNorm of h = x (+ r), each f32 operation rounded alone, the sum of squares in
+            // the order the stand-alone RMSNorm pack declares (so the codes are the same): thread
+            // t of the first 256 adds the squares of elements t, t + 256, ... left to right; each
+            // warp combines its partials by xor-shuffles 16, 8, 4, 2, 1; the eight warp totals
+            // are added left to right.  CTA 0 writes h when asked.
+            float *s_part = reinterpret_cast<float *>(smem + L.norm_off);
+            for (int v = 0; v < B; ++v) {
+                if (tid < 256) {
+                    const float *xv = p.x + v * K;
+                    const float *rv = p.r ? p.r + v * K : nullptr;
+                    float *hv = (p.h_out && blockIdx.x == 0) ? p.h_out + v * K : nullptr;
+                    float acc = 0.0f;
+                    constexpr int U = 8;  // loads in flight per thread per round (registers: 1024-thread bound)
+                    for (int64_t i0 = tid; i0 < K; i0 += (int64_t)U * 256) {
+                        float xu[U], ru[U];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int64_t i = i0 + (int64_t)u * 256;
+                            xu[u] = i < K ? xv[i] : 0.0f;
+                            ru[u] = (rv && i < K) ? rv[i] : 0.0f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int64_t i = i0 + (int64_t)u * 256;
+                            if (i < K) {
+                                const float h = rv ? __fadd_rn(xu[u], ru[u]) : xu[u];
+                                if (hv)
+                                    hv[i] = h;
+                                acc = __fadd_rn(acc, __fmul_rn(h, h));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+                    if (lane == 0)
+                        s_part[v * 8 + warp] = acc;
+                }
+            }
+            __syncthreads();
+            if (tid < B) {
+                float total = s_part[tid * 8];
+                for (int w = 1; w < 8; ++w)
+                    total = __fadd_rn(total, s_part[tid * 8 + w]);
+                const float ms = __fdiv_rn(total, (float)K);
+                s_inv[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+            }
+            __syncthreads();
+        }
+        constexpr int QB = NORM ? 1 : 4;  // blocks per warp whose loads are in flight together
         for (int b0 = warp; b0 < B * nb; b0 += QB * NWT) {
             float4 xa[QB], xb[QB];
 #pragma unroll
@@ -286,6 +353,26 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
                     const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
                     xa[u] = src[0];
                     xb[u] = src[1];
+                    if (NORM) {  // n = (h * (1/rms)) * g with h = x (+ r), as the RMSNorm pack does
+                        const int v = b / nb, blk_g = b - v * nb;
+                        float4 ra = make_float4(0.f, 0.f, 0.f, 0.f), rb = ra;
+                        if (p.r) {
+                            const float4 *rsrc = reinterpret_cast<const float4 *>(p.r + (int64_t)b * 256 + 8 * lane);
+                            ra = rsrc[0];
+                            rb = rsrc[1];
+                        }
+                        const float4 *gsrc = reinterpret_cast<const float4 *>(p.g + blk_g * 256 + 8 * lane);
+                        const float4 ga = gsrc[0], gb = gsrc[1];
+                        const float inv = s_inv[v];
+                        auto nrm = [&](float x, float r, float gg) {
+                            const float h = p.r ? __fadd_rn(x, r) : x;
+                            return __fmul_rn(__fmul_rn(h, inv), gg);
+                        };
+                        xa[u] = make_float4(nrm(xa[u].x, ra.x, ga.x), nrm(xa[u].y, ra.y, ga.y), nrm(xa[u].z, ra.z, ga.z),
+                                            nrm(xa[u].w, ra.w, ga.w));
+                        xb[u] = make_float4(nrm(xb[u].x, rb.x, gb.x), nrm(xb[u].y, rb.y, gb.y), nrm(xb[u].z, rb.z, gb.z),
+                                            nrm(xb[u].w, rb.w, gb.w));
+                    }
                 }
             }
 #pragma unroll
@@ -723,6 +810,7 @@ int qmv_slice_regs(int batch, int PR, int mode)
 #define QMD_CASE(BB)                                                                                 \
     case BB:                                                                                         \
         return mode == QMV_PACK   ? instance_regs<F, BB, QMV_PACK>(PR)                               \
+               : mode == QMV_NORM ? instance_regs<F, BB, QMV_NORM>(PR)                               \
                : mode == QMV_DUMP ? instance_regs<F, BB, QMV_DUMP>(PR)                               \
                                   : instance_regs<F, BB, QMV_PLAIN>(PR);
     switch (batch) {
@@ -766,11 +854,15 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     kp.xq_qs_out = a.xq_qs_out;
     kp.xq_d_out = a.xq_d_out;
     kp.xq_bs_out = a.xq_bs_out;
+    kp.r = a.r;
+    kp.g = a.g;
+    kp.h_out = a.h_out;
+    kp.eps = a.eps;
     kp.err = device_error_word();
     kp.wait_ns = wait_limit_ns();
     if (kp.err == nullptr)
         return QMD_ERR_DEVICE;
-    mode = a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;
+    mode = a.g != nullptr ? QMV_NORM : a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;
     return QMD_OK;
 }
 
@@ -780,6 +872,7 @@ qmd_status launch_qmv_slice(const QmvKParams &kp, const QmvPlan &plan, int batch
 #define QMD_CASE(BB)                                                                                 \
     case BB:                                                                                         \
         return mode == QMV_PACK   ? launch_rows<F, BB, QMV_PACK>(kp, plan, s)                        \
+               : mode == QMV_NORM ? launch_rows<F, BB, QMV_NORM>(kp, plan, s)                        \
                : mode == QMV_DUMP ? launch_rows<F, BB, QMV_DUMP>(kp, plan, s)                        \
                                   : launch_rows<F, BB, QMV_PLAIN>(kp, plan, s);
     switch (batch) {

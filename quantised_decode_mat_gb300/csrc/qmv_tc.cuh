@@ -660,6 +660,8 @@ template <int F>
 qmd_status launch_qmv_tc(const QmvKParams &kp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
     const bool multi = kp.nb > TC_RUN;
+    if (mode == QMV_NORM)  // the RMSNorm form exists only in the dp4a kernel
+        return QMD_ERR_SHAPE;
     switch (plan.stages) {
     case 3:
         return multi ? launch_tc_stages<F, 3, true>(kp, plan, mode, s) : launch_tc_stages<F, 3, false>(kp, plan, mode, s);

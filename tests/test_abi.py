@@ -209,3 +209,35 @@ def test_measure_alu_refuses_null_pointers(L):
     d = ctypes.c_double()
     assert L.qmd_measure_alu(None, ctypes.byref(d)) == 1
     assert L.qmd_measure_alu(ctypes.byref(d), None) == 1
+
+
+def st_norm_mv(L, fmt=q.Q4_K, W=A, Wa=None, x=A, r=None, g=A, eps=1e-6, h=None, xq=None, y=A, rows=16, K=512,
+               batch=2):
+    return L.qmd_qmatvec_rmsnorm_x(fmt, W, Wa, x, r, g, ctypes.c_float(eps), h, xq or q.Q8KPtrs(None, None, None),
+                                   y, rows, K, batch, None)
+
+
+FAR = A + (1 << 20)  # a buffer that overlaps none of the others (2 x 512 f32 = 4 KB each)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(g=None), 1), (dict(W=None), 1), (dict(y=None), 1),
+    (dict(fmt=q.Q6_K_SPLIT), 1), (dict(xq=q.Q8KPtrs(A, None, None)), 1), (dict(fmt=7), 2),
+    (dict(K=300), 3), (dict(batch=0), 4), (dict(batch=9), 4), (dict(rows=0), 6),
+    (dict(x=A + 4), 5), (dict(r=A + 8), 5), (dict(g=A + 12), 5), (dict(h=FAR + 4), 5),
+    (dict(eps=-1e-3), 10), (dict(eps=float("nan")), 10), (dict(eps=float("inf")), 10),
+    # h is written by one CTA while the others still read x and r: no overlap allowed
+    (dict(h=A), 10), (dict(h=A + 4096 - 16), 10), (dict(r=FAR, h=FAR + 16), 10), (dict(h=A - 4096 + 16), 10),
+])
+def test_rmsnorm_matvec_refusals(L, kw, status):
+    assert st_norm_mv(L, **kw) == status
+
+
+def test_rmsnorm_matvec_valid_arguments_reach_the_device_check(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    assert st_norm_mv(L) == 9
+    assert st_norm_mv(L, r=FAR, h=FAR + 4096, eps=0.0) == 9
+    assert st_norm_mv(L, h=A + 4096) == 9  # adjacent, not overlapping
+    assert st_norm_mv(L, fmt=q.Q6_K_SPLIT, Wa=A, batch=8) == 9
