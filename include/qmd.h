@@ -164,7 +164,8 @@ qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, 
  * (32 x (ceil(K / 4096) - 1) bytes for each row a multiprocessor handles) fit in shared memory
  * (K = 32768: about 50,000 rows); QMD_ERR_SHAPE otherwise.
  * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, DEVICE, LAUNCH.
- * Device-side bounded waits that give up set a flag read by qmd_get_device_error.
+ * Device-side bounded waits that give up, and a CTA that finds its launch geometry does not match
+ * its plan (it then returns without touching memory), set a flag read by qmd_get_device_error.
  */
 qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                        int64_t rows, int64_t K, int batch, void *stream);
