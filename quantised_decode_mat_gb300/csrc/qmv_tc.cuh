@@ -156,6 +156,16 @@ __device__ __forceinline__ int exact_small_int(float v)
 
 __device__ __forceinline__ uint32_t lds32(const void *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
+// component-wise f32 addition, each rounded alone
+__device__ __forceinline__ float4 add4(float4 a, float4 b)
+{
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+// A warp that finds its term slot still unsummed sleeps this long between polls, leaving the
+// issue slots to the warps doing dot products (measured: polling without a sleep took a fifth
+// of the kernel's instructions at batch 8).
+constexpr unsigned SPIN_NS = 32;
+
 // F is QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT; STAGES is the depth of each warp's ring; MULTI
 // walks rows of more than 16 blocks run by run (without it the row is a single run and the
 // run bookkeeping compiles away).
@@ -559,10 +569,12 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
         // vector) -------------------------------------------------------------------------------
         const int rslot = T % TC_RED;
         int ok = 1;
-        if (lane == 0) {  // the slot's previous tile must have been summed (bounded wait)
+        if (lane == 0 && s_fin[rslot] != T - TC_RED) {  // the slot's previous tile must have been summed
+            // (bounded wait; the clock is read every 16th poll)
             const uint64_t t0 = globaltimer_ns();
-            while (s_fin[rslot] != T - TC_RED) {
-                if (globaltimer_ns() - t0 > wait_ns) {
+            for (unsigned n = 1; s_fin[rslot] != T - TC_RED; ++n) {
+                __nanosleep(SPIN_NS);
+                if ((n & 15) == 0 && globaltimer_ns() - t0 > wait_ns) {
                     ok = 0;
                     atomicOr(p.err, ERRBIT_QMV_WAIT);
                     break;
@@ -607,31 +619,38 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
             // declared order: groups of four blocks (t0 + t1) + (t2 + t3), absent blocks +0; a
             // run is ((G0 + G1) + G2) + G3, absent groups +0; the row adds its runs left to right
             const float *base = s_red + (size_t)rslot * RW * TC_ROWS * 8;
-            for (int o = lane; o < TC_ROWS * 8; o += 32) {
-                const int row = o >> 3, v = o & 7;
-                if (row < nr && v < B) {
-                    float run = 0.0f;
+            {  // lane: row lane / 2, vectors 4 (lane % 2) .. +3, added component by component
+                const int row = lane >> 1, v0 = 4 * (lane & 1);
+                if (row < nr && v0 < B) {
+                    const int o = row * 8 + v0;
+                    float4 run = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        float x4[4];
+                        float4 x4[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            x4[i] = 4 * q4 + i < run_nb ? base[(4 * q4 + i) * TC_ROWS * 8 + o] : 0.0f;
-                        const float G = __fadd_rn(__fadd_rn(x4[0], x4[1]), __fadd_rn(x4[2], x4[3]));
-                        run = q4 == 0 ? G : __fadd_rn(run, G);
+                            x4[i] = 4 * q4 + i < run_nb ? *reinterpret_cast<const float4 *>(base + (4 * q4 + i) * TC_ROWS * 8 + o)
+                                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        const float4 G = add4(add4(x4[0], x4[1]), add4(x4[2], x4[3]));
+                        run = q4 == 0 ? G : add4(run, G);
                     }
                     const int prow = c * TC_ROWS + row;  // the row within this CTA
                     if (!final_run) {
-                        s_run[((size_t)r * p.tc_rows + prow) * 8 + v] = run;
+                        *reinterpret_cast<float4 *>(s_run + ((size_t)r * p.tc_rows + prow) * 8 + v0) = run;
                     } else {
-                        float acc = run;
+                        float4 acc = run;
                         if (MULTI && runs > 1) {
-                            acc = s_run[(size_t)prow * 8 + v];
+                            acc = *reinterpret_cast<const float4 *>(s_run + (size_t)prow * 8 + v0);
                             for (int rp = 1; rp < runs - 1; ++rp)
-                                acc = __fadd_rn(acc, s_run[((size_t)rp * p.tc_rows + prow) * 8 + v]);
-                            acc = __fadd_rn(acc, run);
+                                acc = add4(acc, *reinterpret_cast<const float4 *>(s_run + ((size_t)rp * p.tc_rows + prow) * 8 + v0));
+                            acc = add4(acc, run);
                         }
-                        p.y[(int64_t)v * p.rows + rs + row] = acc;
+                        float *yv = p.y + (int64_t)v0 * p.rows + rs + row;
+                        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (v0 + i < B)
+                                yv[(int64_t)i * p.rows] = a4[i];
                     }
                 }
             }
