@@ -112,6 +112,26 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// 2-D tiled tensor copy (TMA) global -> this CTA's shared memory: the box the tensor map
+// describes, starting at element coordinates (x, y), completing the box's bytes on the barrier.
+// x times the element size must be a multiple of 16 bytes; dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk / tensor copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared by one thread (no L1 allocation, L2 policy as
 // given); completion is tracked per thread by commit groups.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t policy)

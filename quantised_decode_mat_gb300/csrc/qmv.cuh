@@ -683,8 +683,8 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
 // Launch one kernel instance with the plan's shape: opt in to its shared memory, cap the grid
 // at what is resident at once (a persistent grid; rows are split by gridDim), and launch it as
 // a programmatic dependent of the previous kernel in the stream.
-template <auto Kern>
-qmd_status launch_kernel(const QmvKParams &kp, const QmvPlan &plan, cudaStream_t s)
+template <auto Kern, typename Params>
+qmd_status launch_kernel(const Params &kp, const QmvPlan &plan, cudaStream_t s)
 {
     auto kern = Kern;
     int dev = 0;

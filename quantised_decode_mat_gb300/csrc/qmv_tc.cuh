@@ -31,14 +31,21 @@
 // 16 rows run by run.  At the start of a run a warp loads, for the whole run, the B fragments of
 // vector g over its block's 256 values (32 registers) and the block's per-vector constants, and
 // per 16-row tile computes the block term of rows g and g+8 for vectors 2t and 2t+1.  Each warp
-// streams its own column (16 rows x one block per tile, plus the rows' f16 scale for Q6_K)
-// through a private ring of STAGES slots with asynchronous copies, rows padded to 160 (Q4_K),
-// 224 (Q5_K) or 240 (Q6_K) bytes so that the fragment loads of 8 rows fall in distinct banks.
+// streams its own column (16 rows x one block per tile, plus the rows' f16 scales for Q6_K)
+// through a private ring of STAGES slots: one tensor copy (TMA) per tile and operand, issued by
+// lane 0 and completing on the slot's mbarrier.  The rows land dense (144, 176 or 208 bytes
+// apart), which keeps every fragment load at its minimum number of shared-memory wavefronts:
+// the eight rows g of a load start 4, 12 or 20 banks apart.  CTAs take whole 16-row tiles.
 // Warps never wait for each other to refill; they meet only to sum a tile: each posts its block
 // terms, and the last to arrive adds the run's terms of every (row, vector) in the declared
 // order (groups of four blocks, runs of four groups).  A run that is not the row's last leaves
 // its sums in shared memory; the last run's finisher adds the runs left to right and writes y.
 #pragma once
+
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "qmv.cuh"
 
@@ -53,22 +60,20 @@ __host__ __device__ constexpr int tc_block_bytes(int fmt)
 {
     return fmt == QMD_Q6_K_SPLIT ? 208 : fmt == QMD_Q5_K ? 176 : 144;
 }
-__host__ __device__ constexpr int tc_row_stride(int fmt)
-{
-    return fmt == QMD_Q6_K_SPLIT ? 240 : fmt == QMD_Q5_K ? 224 : 160;
-}
-// a ring slot: 16 rows, and for Q6_K the 16 rows' 4-byte prefix words holding the scale d
+// a ring slot: the 16 rows of one block, dense as the tensor copy writes them, and for Q6_K the
+// rows' 16-byte prefix chunks (eight f16 scales, the block's among them); a multiple of 128 bytes
 __host__ __device__ constexpr int tc_slot_bytes(int fmt)
 {
-    return TC_ROWS * tc_row_stride(fmt) + (fmt == QMD_Q6_K_SPLIT ? 64 : 0);
+    return TC_ROWS * tc_block_bytes(fmt) + (fmt == QMD_Q6_K_SPLIT ? TC_ROWS * 16 : 0);
 }
 __host__ __device__ constexpr int tc_steps(int fmt) { return fmt == QMD_Q6_K_SPLIT ? 16 : 8; }
 
 struct TcLayout {
-    int red_off, bias_off, cnt_off, fin_off, done_off, run_off, acts_off, dx_off, bs_off, total;
+    int bar_off, red_off, bias_off, cnt_off, fin_off, done_off, run_off, acts_off, dx_off, bs_off, total;
 };
 
-// Shared memory: warp rings [RW][stages][slot] | block terms f32 [TC_RED][RW][16 rows][8 vectors]
+// Shared memory: warp rings [RW][stages][slot] | ring barriers u64 [RW][stages] | block terms f32
+// [TC_RED][RW][16 rows][8 vectors]
 // | accumulator starts f32 [RW][steps][8 vectors] | arrival counters u32 [TC_RED] | finished
 // tile i32 [TC_RED] | finished runs per row tile i32 [rows_pad / 16] | earlier runs' sums f32
 // [runs - 1][rows_pad][8] | fused form only: codes i8 [B][K], d f32 [B][nb], sums i16
@@ -79,6 +84,8 @@ __host__ __device__ inline TcLayout qmv_tc_layout(int stages, int fmt, int nb, i
     const int runs = (nb + TC_RUN - 1) / TC_RUN;
     TcLayout L;
     int o = RW * stages * tc_slot_bytes(fmt);
+    L.bar_off = o;
+    o = align_up(o + RW * stages * 8, 16);
     L.red_off = o;
     o += TC_RED * RW * TC_ROWS * 8 * 4;
     L.bias_off = o;
@@ -166,20 +173,27 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b)
 // of the kernel's instructions at batch 8).
 constexpr unsigned SPIN_NS = 32;
 
+// The kernel's parameters: the common ones and the tensor maps its copies read through.
+struct TcParams {
+    QmvKParams k;
+    CUtensorMap wmap;    // W as u8 [rows][row_bytes], box: one block's bytes x 16 rows
+    CUtensorMap premap;  // Q6_K prefix as u16 [rows][prefix stride], box: 8 scales x 16 rows
+};
+
 // F is QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT; STAGES is the depth of each warp's ring; MULTI
 // walks rows of more than 16 blocks run by run (without it the row is a single run and the
 // run bookkeeping compiles away).
 template <int F, int MODE, int STAGES, bool MULTI>
-__global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
+__global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ TcParams tp)
 {
+    const QmvKParams &p = tp.k;
     constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
     constexpr bool Q5 = F == QMD_Q5_K;
     constexpr bool DUMP = MODE == QMV_DUMP;
     constexpr bool PACK = MODE == QMV_PACK;
     constexpr int BLOCK_BYTES = tc_block_bytes(F);
-    constexpr int RSTRIDE = tc_row_stride(F);
+    constexpr int RSTRIDE = BLOCK_BYTES;  // rows of a slot
     constexpr int SLOT = tc_slot_bytes(F);
-    constexpr int CPR = BLOCK_BYTES / 16;  // 16-byte chunks per row of a block
     constexpr int NSTEP = tc_steps(F);     // accumulator starts per block and vector
     constexpr int QS_OFF = Q5 ? 48 : 16;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -189,10 +203,13 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
     const int RW = blockDim.x >> 5;  // warps: min(nb, 16)
     const int runs = MULTI ? (nb + TC_RUN - 1) / TC_RUN : 1;
     const int g = lane >> 2, t = lane & 3;
-    const int64_t r0 = p.rows * (int64_t)blockIdx.x / gridDim.x;
-    const int64_t r1 = p.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
-    const int nt = (int)((r1 - r0 + TC_ROWS - 1) / TC_ROWS);  // row tiles of this CTA
-    const int ntot = runs * nt;                                // tiles, run by run
+    // rows are split in whole 16-row tiles, so only the matrix's last tile is partial (its
+    // missing rows arrive as zeros from the tensor copy) and no tile is read by two CTAs
+    const int64_t tiles = (p.rows + TC_ROWS - 1) / TC_ROWS;
+    const int64_t tb0 = tiles * blockIdx.x / gridDim.x, tb1 = tiles * (blockIdx.x + 1) / gridDim.x;
+    const int64_t r0 = tb0 * TC_ROWS, r1 = min(p.rows, tb1 * TC_ROWS);
+    const int nt = (int)(tb1 - tb0);  // row tiles of this CTA
+    const int ntot = runs * nt;       // tiles, run by run
     const TcLayout L = qmv_tc_layout(STAGES, F, nb, B, PACK, p.tc_rows);
     uint8_t *ring = smem + (size_t)warp * STAGES * SLOT;
     float *s_red = reinterpret_cast<float *>(smem + L.red_off);
@@ -208,29 +225,32 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
     }
 
     // this warp's column of tile T (run T / nt, rows r0 + 16 (T % nt) ..) into ring slot
-    // T % STAGES: lane l copies row l / 2, 16-byte chunks l % 2, l % 2 + 2, ...; for Q6_K the
-    // even lanes also copy their row's aligned 4-byte prefix word holding the block's scale.
-    // Every lane commits one group per tile index, empty past its last tile, so group counts
-    // stay aligned.
-    const int crow = lane >> 1, ccol = lane & 1;
+    // T % STAGES: one tensor copy of the 16 rows' block and, for Q6_K, one of the rows' 16-byte
+    // prefix chunks holding the block's scale, both completing on the slot's barrier.  Issued
+    // by lane 0; a warp copies only the tiles of runs in which it has a block.
+    const uint32_t ring0 = smem_addr(ring);
+    const uint32_t bar0 = smem_addr(smem + L.bar_off) + 8u * (uint32_t)(warp * STAGES);
+    auto copies = [&](int T) { return T < ntot && (MULTI ? T / nt : 0) * TC_RUN + warp < nb; };
     auto issue = [&](int T) {
-        if (T < ntot) {
+        if (copies(T)) {
             const int r = MULTI ? T / nt : 0, c = MULTI ? T - r * nt : T;
             const int b = r * TC_RUN + warp;
-            const int64_t row = r0 + (int64_t)c * TC_ROWS + crow;
-            if (b < nb && row < r1) {
-                const uint32_t slot = smem_addr(ring) + (T % STAGES) * SLOT;
-                const uint32_t dst = slot + crow * RSTRIDE + 16 * ccol;
-                const uint8_t *src = p.W + row * p.row_bytes + (int64_t)b * BLOCK_BYTES + 16 * ccol;
-#pragma unroll
-                for (int k = 0; k < (CPR + 1) / 2; ++k)
-                    if (2 * k + ccol < CPR)
-                        cp_async_16(dst + 32 * k, src + 32 * k, pol);
-                if (Q6 && ccol == 0)
-                    cp_async_4(slot + TC_ROWS * RSTRIDE + 4 * crow, p.Wpre + row * p.pre_bytes + 2 * (b & ~1));
-            }
+            const uint32_t st = (uint32_t)(T % STAGES);
+            const uint32_t bar = bar0 + 8u * st, dst = ring0 + st * SLOT;
+            const int y = (int)(r0 + (int64_t)c * TC_ROWS);
+            mbar_arrive_expect_tx(bar, SLOT);
+            tma_load_2d(dst, &tp.wmap, b * BLOCK_BYTES, y, bar, pol);
+            if (Q6)
+                tma_load_2d(dst + TC_ROWS * BLOCK_BYTES, &tp.premap, b & ~7, y, bar, pol);
         }
-        cp_async_commit();
+    };
+    const unsigned long long wait_ns = p.wait_ns;
+    // wait (bounded) for this warp's copies of tiles T0 .. T0 + STAGES - 1 still in flight, so
+    // that none lands after the warp has gone
+    auto drain = [&](int T0) {
+        for (int u = T0; u < T0 + STAGES; ++u)
+            if (copies(u))
+                (void)mbar_wait_bounded(bar0 + 8u * (uint32_t)(u % STAGES), (uint32_t)(u / STAGES) & 1u, wait_ns);
     };
 
     if (tid < TC_RED) {
@@ -240,9 +260,14 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
     if (runs > 1)
         for (int i = tid; i < nt; i += blockDim.x)
             s_done[i] = 0;
+    if (lane == 0) {
+        for (int i = 0; i < STAGES; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_barrier_init();
 #pragma unroll
-    for (int T = 0; T < STAGES; ++T)
-        issue(T);
+        for (int T = 0; T < STAGES; ++T)
+            issue(T);
+    }
     __syncthreads();
 
     pdl_launch_dependents();
@@ -344,7 +369,6 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
         __syncwarp();
     };
 
-    const unsigned long long wait_ns = p.wait_ns;
     int run_nb = MULTI ? 0 : nb, blk = warp;
     if (!MULTI)
         load_run(warp);
@@ -358,12 +382,18 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
             blk = r * TC_RUN + warp;
             load_run(blk);
         }
-        cp_async_wait<STAGES - 1>();  // this lane's copies of tile T have landed
-        __syncwarp();                  // ... and every lane's are visible to the warp
+        // tile T's copies have landed (bounded; the decision is the warp's)
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8u * (uint32_t)(T % STAGES), (uint32_t)(T / STAGES) & 1u,
+                                                       wait_ns))) {
+            if (lane == 0)
+                atomicOr(p.err, ERRBIT_QMV_WAIT);
+            drain(T);
+            return;
+        }
         const int64_t rs = r0 + (int64_t)c * TC_ROWS;
         const int nr = (int)min((int64_t)TC_ROWS, r1 - rs);
 
-        // rows g and g+8 of the tile (rows past nr hold stale bytes: computed, never stored)
+        // rows g and g+8 of the tile (rows past nr hold zeros: computed, never stored)
         const uint8_t *slot = ring + (T % STAGES) * SLOT;
         const uint8_t *rowA = slot + g * RSTRIDE;
         const uint8_t *rowB = rowA + 8 * RSTRIDE;
@@ -427,13 +457,13 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
                     }
                 }
             }
-            // the block's f32 terms: dx * (d * S), d the row's f16 scale from the prefix word
-            const uint8_t *pre = slot + TC_ROWS * RSTRIDE;
+            // the block's f32 terms: dx * (d * S), d the row's f16 scale from its prefix chunk
+            const uint8_t *pre = slot + TC_ROWS * BLOCK_BYTES;
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int row = g + 8 * rr;
-                const uint32_t pw = lds32(pre + 4 * row);
-                const float d = __half2float(__ushort_as_half((unsigned short)((blk & 1) ? (pw >> 16) : (pw & 0xffffu))));
+                const unsigned short hb = *reinterpret_cast<const unsigned short *>(pre + 16 * row + 2 * (blk & 7));
+                const float d = __half2float(__ushort_as_half(hb));
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     term[rr][e] = __fmul_rn(dxv[e], __fmul_rn(d, __int2float_rn(S[rr][e])));
@@ -562,8 +592,11 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
                 }
             }
         }
-        __syncwarp();       // every lane is done with this ring slot
-        issue(T + STAGES);  // refill it with this warp's column of tile T + STAGES
+        __syncwarp();  // every lane is done with this ring slot
+        if (lane == 0) {
+            fence_proxy_async_smem();  // the warp's reads of the slot before the copy's writes
+            issue(T + STAGES);         // refill it with this warp's column of tile T + STAGES
+        }
 
         // ---- post the terms; the last warp to arrive adds the run's terms of every (row,
         // vector) -------------------------------------------------------------------------------
@@ -582,7 +615,7 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
             }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            cp_async_wait<0>();  // no copy may land after the warp is gone
+            drain(T + 1);  // no copy may land after the warp is gone
             return;
         }
         float *red = s_red + ((size_t)rslot * RW + warp) * TC_ROWS * 8;
@@ -611,7 +644,7 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok2, 0)) {
-                    cp_async_wait<0>();
+                    drain(T + 1);
                     return;
                 }
                 __threadfence_block();
@@ -664,15 +697,68 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const QmvKParams p)
             }
         }
     }
-    cp_async_wait<0>();  // no copy may land after the CTA is gone
+    // every tile a warp copies it also consumes, so no copy is in flight here
 }
 
 template <int F, int STAGES, bool MULTI>
-qmd_status launch_tc_stages(const QmvKParams &kp, const QmvPlan &plan, int mode, cudaStream_t s)
+qmd_status launch_tc_stages(const TcParams &tp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
-    return mode == QMV_PACK   ? launch_kernel<qmv_tc_kernel<F, QMV_PACK, STAGES, MULTI>>(kp, plan, s)
-           : mode == QMV_DUMP ? launch_kernel<qmv_tc_kernel<F, QMV_DUMP, STAGES, MULTI>>(kp, plan, s)
-                              : launch_kernel<qmv_tc_kernel<F, QMV_PLAIN, STAGES, MULTI>>(kp, plan, s);
+    return mode == QMV_PACK   ? launch_kernel<qmv_tc_kernel<F, QMV_PACK, STAGES, MULTI>>(tp, plan, s)
+           : mode == QMV_DUMP ? launch_kernel<qmv_tc_kernel<F, QMV_DUMP, STAGES, MULTI>>(tp, plan, s)
+                              : launch_kernel<qmv_tc_kernel<F, QMV_PLAIN, STAGES, MULTI>>(tp, plan, s);
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link to the driver
+// library); NULL if this driver does not provide it.
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                       const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                       CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+inline TensorMapEncodeFn tensor_map_encoder()
+{
+    static TensorMapEncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<TensorMapEncodeFn>(f);
+    });
+    return fn;
+}
+
+// Tensor maps of one call: W as bytes [rows][row_bytes] in boxes of one block x 16 rows (rows
+// past the end read as zeros), and for Q6_K the prefix as u16 [rows][prefix stride] in boxes of
+// 8 entries x 16 rows.  Row pitches are multiples of 16 bytes (144, 176 and 208 are; the prefix
+// stride is a multiple of 8 entries), bases 16-byte aligned (checked by the caller).
+template <int F>
+qmd_status tc_tensor_maps(const QmvKParams &kp, TcParams &tp)
+{
+    const TensorMapEncodeFn enc = tensor_map_encoder();
+    if (!enc)
+        return fail(QMD_ERR_LAUNCH, "cuTensorMapEncodeTiled entry point", cudaErrorNotSupported);
+    std::memset(&tp.wmap, 0, sizeof tp.wmap);
+    std::memset(&tp.premap, 0, sizeof tp.premap);
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t wdim[2] = {(cuuint64_t)kp.row_bytes, (cuuint64_t)kp.rows};
+    const cuuint64_t wstr[1] = {(cuuint64_t)kp.row_bytes};
+    const cuuint32_t wbox[2] = {(cuuint32_t)tc_block_bytes(F), (cuuint32_t)TC_ROWS};
+    if (enc(&tp.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(kp.W), wdim, wstr, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return fail(QMD_ERR_LAUNCH, "tensor map of the weights", cudaErrorInvalidValue);
+    if (F == QMD_Q6_K_SPLIT) {
+        const cuuint64_t pdim[2] = {(cuuint64_t)(kp.pre_bytes / 2), (cuuint64_t)kp.rows};
+        const cuuint64_t pstr[1] = {(cuuint64_t)kp.pre_bytes};
+        const cuuint32_t pbox[2] = {8, (cuuint32_t)TC_ROWS};
+        if (enc(&tp.premap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t *>(kp.Wpre), pdim, pstr, pbox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(QMD_ERR_LAUNCH, "tensor map of the Q6_K prefix", cudaErrorInvalidValue);
+    }
+    return QMD_OK;
 }
 
 template <int F>
@@ -681,11 +767,16 @@ qmd_status launch_qmv_tc(const QmvKParams &kp, const QmvPlan &plan, int mode, cu
     const bool multi = kp.nb > TC_RUN;
     if (mode == QMV_NORM)  // the RMSNorm form exists only in the dp4a kernel
         return QMD_ERR_SHAPE;
+    TcParams tp;
+    tp.k = kp;
+    const qmd_status st = tc_tensor_maps<F>(kp, tp);
+    if (st != QMD_OK)
+        return st;
     switch (plan.stages) {
     case 3:
-        return multi ? launch_tc_stages<F, 3, true>(kp, plan, mode, s) : launch_tc_stages<F, 3, false>(kp, plan, mode, s);
+        return multi ? launch_tc_stages<F, 3, true>(tp, plan, mode, s) : launch_tc_stages<F, 3, false>(tp, plan, mode, s);
     case 4:
-        return multi ? launch_tc_stages<F, 4, true>(kp, plan, mode, s) : launch_tc_stages<F, 4, false>(kp, plan, mode, s);
+        return multi ? launch_tc_stages<F, 4, true>(tp, plan, mode, s) : launch_tc_stages<F, 4, false>(tp, plan, mode, s);
     }
     return QMD_ERR_SHAPE;
 }
