@@ -442,9 +442,9 @@ def run_ours(args):
     b6 = sum(per(p) for p in step.projs if p.fmt == q.Q6_K_SPLIT) / nq6
     bp = nbytes["pack"] / len(step.projs)
 
-    # RMSNorm + residual + pack (qmd_rmsnorm_q8k_pack) on the inputs of the 4096-wide projections
-    # (q|k|v and gate|up read a normalised residual stream in a decode step), a chain of launches
-    rms = [p for p in step.projs if p.K == 4096]
+    # RMSNorm + residual + pack (qmd_rmsnorm_q8k_pack) on the inputs of q|k|v and gate|up (the two
+    # projections that read a normalised residual stream in a decode step), a chain of launches
+    rms = [p for p in step.projs if p.name in ("qkv", "gate_up")]
     gain = torch.full((4096,), 1.0, dtype=torch.float32, device=stream.device)
     resid = [torch.zeros_like(p.x) for p in rms]
 

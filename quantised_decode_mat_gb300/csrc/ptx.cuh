@@ -1,6 +1,6 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a: shared-memory mbarriers, 1-D bulk async copies
-// (global -> this CTA's shared memory, no multicast), per-thread 16- and 4-byte async copies,
-// programmatic dependent launch, and a bounded barrier wait that gives up instead of hanging.
+// and 2-D tiled tensor copies (global -> this CTA's shared memory, no multicast), programmatic
+// dependent launch, and a bounded barrier wait that gives up instead of hanging.
 #pragma once
 
 #include <cstdint>
@@ -130,30 +130,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 16-byte asynchronous copy global -> shared by one thread (no L1 allocation, L2 policy as
-// given); completion is tracked per thread by commit groups.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t policy)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-                 : "memory");
-}
-
-// 4-byte asynchronous copy global -> shared by one thread (through L1; both addresses 4-byte
-// aligned), tracked by the same commit groups.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's committed groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Programmatic dependent launch: let the next kernel in the stream be scheduled, and wait
