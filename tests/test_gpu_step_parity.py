@@ -1,7 +1,8 @@
 """The 7B-shaped decode step at full size, in the launch forms bench.py times (batch 1: the pack
 fused into the 4096-wide mat-vecs and a stand-alone pack for the 14336-wide down projection;
-batch 4: pack + mat-vec), against the oracle: q|k|v and o on every row, gate|up and down on the
-rows at every CTA boundary of their launch plus a random sample; two layers."""
+batches 4 and 8: pack + mat-vec, the 4096-wide ones on the tensor cores at batch 8), against the
+oracle: q|k|v and o on every row, gate|up and down on the rows at every CTA boundary of their
+launch plus a random sample; two layers."""
 import numpy as np
 import pytest
 
@@ -20,7 +21,7 @@ TOL_F64 = 2e-3
 OFMT = {q.Q4_K: O.FMT_Q4_K, q.Q6_K_SPLIT: O.FMT_Q6_K}
 
 
-@pytest.fixture(scope="module", params=[1, 4], ids=["b1", "b4"])
+@pytest.fixture(scope="module", params=[1, 4, 8], ids=["b1", "b4", "b8"])
 def step(request):
     from quantised_decode_mat_gb300 import build as qbuild
     from quantised_decode_mat_gb300 import step as qstep
@@ -42,8 +43,11 @@ def _rows_to_check(p, batch):
     rng = np.random.default_rng(p.rows + 7 * batch + p.layer)
     pick = set(rng.choice(p.rows, size=500, replace=False).tolist()) | {0, 1, p.rows - 2, p.rows - 1}
     G = q.launch_info(p.fmt, p.rows, p.K, batch)["grid"]
+    tiles = (p.rows + 15) // 16
     for g in (G, 152, 304, 456, 608):  # the plan's grid and the grids the fused plans may take
         pick |= {(p.rows * b) // g for b in range(g)} | {(p.rows * b) // g - 1 for b in range(1, g)}
+        # the tensor-core kernel splits whole 16-row tiles
+        pick |= {16 * ((tiles * b) // g) for b in range(g)} | {16 * ((tiles * b) // g) - 1 for b in range(1, g)}
     return np.array(sorted(r for r in pick if 0 <= r < p.rows))
 
 
