@@ -180,8 +180,8 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->pre_bytes = pre_bytes;
     pl->row_stride = row_bytes;
     // Tensor-core kernel.  Chosen where it was measured faster -- Q4_K / Q5_K rows of at most 16
-    // blocks at 5..8 vectors (below 5 the dp4a kernel is as fast or faster; Q6_K's 14336-wide
-    // down projection took 30.6 us against 26.2 on dp4a at 8 vectors) -- and for rows the dp4a
+    // blocks at 5..8 vectors (below 5 the dp4a kernel is faster; Q6_K's 14336-wide down
+    // projection takes 26.9 us against 26.2 on dp4a at 8 vectors) -- and for rows the dp4a
     // kernel cannot take (more than 128 blocks at one or two vectors, 64 above), which it walks
     // run by run.  One warp per block of a run of 16 blocks, each with its own ring of 16-row
     // tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per warp) that fits
