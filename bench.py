@@ -515,7 +515,8 @@ def run_ours(args):
                                                             "fused pack" if q4_fused else "packed input"),
                      "achieved": ach4, "peak": peak,
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
-                     "traffic": profiled_traffic("qmv_q4k"),
+                     # the committed capture is of the batch-1 fused-pack launches only
+                     "traffic": profiled_traffic("qmv_q4k") if args.batch == 1 and q4_fused else None,
                      "algorithmic_bytes_per_launch": b4, "ms_per_launch": ms4},
         "alu_roofline": alu_roofline(q, step, args.batch, ms4, dp4a_rate, mma_rate),
         "kernels": {
