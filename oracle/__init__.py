@@ -76,11 +76,12 @@ def lib():
             L.oracle_rmsnorm_q8k_pack.argtypes = [p, p, p, ctypes.c_float, i64, p, p, p, p, p]
             for name in ("oracle_q4k_fields", "oracle_q4k_dequant", "oracle_q6k_fields",
                          "oracle_q6k_dequant", "oracle_q8k_pack", "oracle_q4k_subdots",
-                         "oracle_q6k_subdots", "oracle_block_terms", "oracle_qmatvec",
+                         "oracle_q6k_subdots", "oracle_block_terms",
                          "oracle_q5k_fields", "oracle_q5k_dequant", "oracle_q5k_subdots",
                          "oracle_qmatvec_f64", "oracle_q6k_split", "oracle_rmsnorm",
                          "oracle_rmsnorm_q8k_pack"):
                 getattr(L, name).restype = None
+            L.oracle_qmatvec.restype = ctypes.c_int  # 0, or non-zero for a refused call
             _lib = L
     return _lib
 
@@ -206,7 +207,9 @@ def qmatvec(fmt: int, W: np.ndarray, qs: np.ndarray, xd: np.ndarray, bsums: np.n
     xd = _c(xd, np.float32).reshape(batch, nb)
     bsums = _c(bsums, np.int16).reshape(batch, nb, 8)
     y = np.zeros((batch, rows), np.float32)
-    lib().oracle_qmatvec(fmt, _ptr(W), _ptr(qs), _ptr(xd), _ptr(bsums), rows, K, batch, order, _ptr(y))
+    rc = lib().oracle_qmatvec(fmt, _ptr(W), _ptr(qs), _ptr(xd), _ptr(bsums), rows, K, batch, order, _ptr(y))
+    if rc != 0:
+        raise RuntimeError(f"oracle_qmatvec refused the call (status {rc}, K={K}, batch={batch})")
     return y
 
 

@@ -49,6 +49,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define QK 256
@@ -344,17 +345,20 @@ void oracle_block_terms(int fmt, const uint8_t *row, const int8_t *qs, const flo
  *          This is the order the GPU path declares for its reduction (for rows of at most 16
  *          blocks it equals order 1); the oracle states it independently.
  * W is canonical GGUF blocks [rows][K/256][144, 176 or 210]; the packed vectors are batch-major:
- * qs [batch][K], xd [batch][K/256], bsums [batch][K/256][8]; y is [batch][rows].          */
-#define MAX_NB 4096
-void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd,
-                    const int16_t *bsums, int64_t rows, int64_t K, int batch, int order,
-                    float *y)
+ * qs [batch][K], xd [batch][K/256], bsums [batch][K/256][8]; y is [batch][rows].
+ * Returns 0, or non-zero (and writes nothing) for a shape it is not defined on or when the
+ * per-row scratch cannot be allocated; any row length is accepted.                          */
+int oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd,
+                   const int16_t *bsums, int64_t rows, int64_t K, int batch, int order,
+                   float *y)
 {
     int64_t nb = K / QK;
     int64_t bb = fmt == FMT_Q4_K ? Q4K_BYTES : fmt == FMT_Q5_K ? Q5K_BYTES : Q6K_BYTES;
-    float terms[MAX_NB];
-    if (nb > MAX_NB)
-        return;
+    if (nb < 1 || K % QK != 0 || rows < 0 || batch < 1)
+        return 1; /* not a shape the mat-vec is defined on: nothing written */
+    float *terms = (float *)malloc((size_t)nb * sizeof(float));
+    if (!terms)
+        return 2; /* out of memory: nothing written */
     for (int v = 0; v < batch; ++v) {
         for (int64_t r = 0; r < rows; ++r) {
             oracle_block_terms(fmt, W + r * nb * bb, qs + v * K, xd + v * nb,
@@ -391,6 +395,8 @@ void oracle_qmatvec(int fmt, const uint8_t *W, const int8_t *qs, const float *xd
             y[v * rows + r] = acc;
         }
     }
+    free(terms);
+    return 0;
 }
 
 /* ---- brute force: dequantise W and x_hat = dx * q8 to f64 and sum in f64. ------------- */

@@ -636,3 +636,28 @@ def test_q5k_subdots_and_epilogue_brute_force():
             w = np.concatenate([O.dequant(O.FMT_Q5_K, W[r, b]) for b in range(3)])
             xh = np.repeat(xd[v].astype(np.float64), 256) * qs[v].astype(np.float64)
             assert np.isclose(y64[v, r], float(np.dot(w, xh)), rtol=1e-12, atol=1e-12)
+
+
+def test_long_rows_are_computed_not_skipped():
+    """Rows of more than 4096 blocks (K = 1,048,832 here) are computed like any other: the
+    same-order result sits within the f32 summation bound of the f64 brute force, so the
+    output cannot be the untouched zero buffer."""
+    K = 4097 * 256
+    W = synth.weights("q4k", 11, 2, K)
+    x = synth.activations(11, 1, K)
+    qs, xd, bs = O.q8k_pack(x)
+    y = O.qmatvec(O.FMT_Q4_K, W, qs, xd, bs, O.ORDER_RUNS_OF_SIXTEEN)
+    ref = O.qmatvec_f64(O.FMT_Q4_K, W, qs, xd)
+    for r in range(2):
+        t = O.block_terms(O.FMT_Q4_K, W[r], qs[0], xd[0], bs[0]).astype(np.float64)
+        bound = 4 * 4097 * 2.0 ** -24 * np.abs(t).sum() + 64 * 2.0 ** -24 * abs(ref[0, r])
+        assert y[0, r] != 0.0
+        assert abs(float(y[0, r]) - ref[0, r]) <= bound
+
+
+def test_refused_shape_raises():
+    """A call the mat-vec is not defined on raises instead of returning a zero buffer."""
+    W = np.zeros((1, 0), np.uint8)  # one row of K = 0
+    qs = np.zeros((1, 0), np.int8)
+    with pytest.raises(RuntimeError, match="refused"):
+        O.qmatvec(O.FMT_Q4_K, W, qs, np.zeros((1, 0), np.float32), np.zeros((1, 0, 8), np.int16))
