@@ -49,15 +49,19 @@ class Q8KPtrs(ctypes.Structure):
 _lib = None
 
 
-def lib() -> ctypes.CDLL:
-    """Load libqmd.so (raises if it has not been built)."""
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """Load libqmd.so (raises if it has not been built).  `path` loads another build of the same
+    library instead (the traced build, libqmd_trace.so); it must come before the first load."""
     global _lib
+    if _lib is not None and path is not None and path != _lib._name:
+        raise RuntimeError(f"{_lib._name} is already loaded")
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
+        path = path or LIB_PATH
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
                 "or `python -m quantised_decode_mat_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         i64, i32, vp, u64 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64
         ip = ctypes.POINTER(ctypes.c_int)
         sizep = ctypes.POINTER(ctypes.c_size_t)
@@ -85,6 +89,9 @@ def lib() -> ctypes.CDLL:
             "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
             "qmd_version": ([], i32),
         }
+        if hasattr(L, "qmd_debug_trace"):  # the traced build (include/qmd_trace.h)
+            sigs["qmd_debug_trace"] = ([vp, i64], i32)
+            sigs["qmd_debug_trace_launches"] = ([vp, vp, i64], i64)
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
             f.argtypes = args

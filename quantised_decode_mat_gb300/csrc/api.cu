@@ -9,12 +9,13 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
 #include "internal.h"
 #include "ptx.cuh"
-#include "qmv_tc.cuh"
+#include "qmv_rl.cuh"
 
 namespace qmd {
 
@@ -95,6 +96,27 @@ unsigned *device_error_word()
     return addr[dev].load(std::memory_order_acquire);
 }
 
+#ifdef QMD_TRACE
+// Traced build: one caller-owned device buffer of stamp records; each launch takes the next
+// `ctas` records and logs (first record, CTAs) on the host, in launch (or capture) order.
+static std::mutex g_trace_mu;
+static unsigned long long *g_trace_buf = nullptr;
+static int64_t g_trace_cap = 0, g_trace_used = 0;
+static std::vector<int64_t> g_trace_log;
+
+unsigned long long *trace_reserve(int ctas)
+{
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (!g_trace_buf || ctas < 1 || g_trace_used + ctas > g_trace_cap)
+        return nullptr;
+    unsigned long long *p = g_trace_buf + g_trace_used * QMD_TRACE_FIELDS;
+    g_trace_log.push_back(g_trace_used);
+    g_trace_log.push_back(ctas);
+    g_trace_used += ctas;
+    return p;
+}
+#endif
+
 // Rows per row group per stage: 8 at one or two vectors, 4 at three or four, 2 above (16 (row,
 // vector) slots per warp from two vectors up; measured on the 7B shapes with the CTA counts
 // chosen below).
@@ -169,6 +191,55 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
     return false;
 }
 
+// Row-lane kernel (qmv_rl.cuh): one CTA per SM (more when forced), a ring for as many warps as
+// the CTA has 4-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
+// has steps) that fits beside the activations, and up to 16 warps to pack them.  false if
+// nothing fits (very long rows).
+static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
+{
+    const int64_t tiles = (rows + RL_ROWS - 1) / RL_ROWS;
+    const int nsteps = (nb + RL_BLOCKS - 1) / RL_BLOCKS;
+    const int cps = g_force_cps.load() > 0 ? g_force_cps.load() : 1;
+    int64_t grid = (int64_t)dev.sm_count * cps;
+    if (grid > tiles)
+        grid = tiles;
+    const int64_t per_cta = (tiles + grid - 1) / grid;
+    int W = g_force_rg.load() > 0 ? g_force_rg.load() : (int)(per_cta < RL_MAX_WARPS ? per_cta : RL_MAX_WARPS);
+    if (W > RL_MAX_WARPS)
+        W = RL_MAX_WARPS;
+    if (W < 1)
+        W = 1;
+    int budget = dev.smem_per_sm / cps - 1024;
+    if (budget > dev.smem_optin)
+        budget = dev.smem_optin;
+    const int64_t steps = (per_cta + W - 1) / W * nsteps;  // most steps a warp has
+    int S = g_force_stages.load() > 0 ? g_force_stages.load() : 4;
+    if (S > steps)
+        S = (int)steps;
+    for (; S >= 1; --S)
+        if (qmv_rl_layout(fmt, W, S, batch, nb).total <= budget)
+            break;
+    if (S < 1)
+        return false;
+    // every warp of the CTA packs (or loads) the activations: at least as many warps as blocks to
+    // pack, up to 16, even where fewer warps have tiles
+    int NW = W;
+    const int64_t blocks = (int64_t)batch * nb;
+    const int want = (int)(blocks < RL_MAX_WARPS ? blocks : RL_MAX_WARPS);
+    if (g_force_rg.load() <= 0 && NW < want)
+        NW = want;
+    pl->layout = 2;
+    pl->grid = (int)grid;
+    pl->threads = 32 * NW;
+    pl->smem = qmv_rl_layout(fmt, W, S, batch, nb).total;
+    pl->stages = S;
+    pl->WR = W;
+    pl->RG = 1;
+    pl->PR = RL_ROWS;
+    pl->stage_bytes = rl_slot_bytes(fmt);
+    return true;
+}
+
 qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
 {
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
@@ -190,6 +261,12 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // only in the dp4a kernel.
     const int fst = g_force_stages.load();
     pl->tc_rows = 0;
+    // One or two vectors: the row-lane kernel, unless a test flag asks for another kernel (three
+    // and four on it too when a flag asks).
+    const bool rl_batch = batch <= RL_DEFAULT_BATCH || ((launch_flags() & LAUNCH_RL) && batch <= RL_MAX_BATCH);
+    if (mode != QMV_NORM && rl_batch && !(launch_flags() & (LAUNCH_SLICE | LAUNCH_TC_ALL)) &&
+        rl_plan(fmt, rows, nb, batch, dev, pl))
+        return QMD_OK;
     const bool tc_faster = batch >= TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
     const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);
     const bool tc_forced = (launch_flags() & LAUNCH_TC_ALL) && batch >= 3;
@@ -689,6 +766,33 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)
 }
 
 void qmd_debug_set_launch_flags(unsigned flags) { g_launch_flags.store(flags); }
+
+#ifdef QMD_TRACE
+qmd_status qmd_debug_trace(void *buf, int64_t records)
+{
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (buf && (!aligned(buf, 8) || records < 0))
+        return QMD_ERR_VALUE;
+    g_trace_buf = static_cast<unsigned long long *>(buf);
+    g_trace_cap = buf ? records : 0;
+    g_trace_used = 0;
+    g_trace_log.clear();
+    return QMD_OK;
+}
+
+int64_t qmd_debug_trace_launches(int64_t *first, int32_t *ctas, int64_t max)
+{
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    const int64_t n = (int64_t)g_trace_log.size() / 2;
+    for (int64_t i = 0; i < n && i < max; ++i) {
+        if (first)
+            first[i] = g_trace_log[2 * i];
+        if (ctas)
+            ctas[i] = (int32_t)g_trace_log[2 * i + 1];
+    }
+    return n;
+}
+#endif
 
 int qmd_version(void) { return 100; }
 

@@ -33,9 +33,17 @@ unsigned *device_error_word();
 uint64_t wait_limit_ns();
 
 // Test-only launch flags (bit 0: launch without programmatic dependent launch; bit 1: compute
-// batches of 5..8 vectors with the dp4a kernel even where the tensor-core kernel applies).
+// batches of 5..8 vectors with the dp4a kernel even where the tensor-core kernel applies; bit 2:
+// the tensor-core kernel for every batch of 3..8; bit 3: the dp4a slice kernel instead of the
+// row-lane kernel; bit 4: the row-lane kernel for batches of 3 and 4 as well).
 unsigned launch_flags();
-enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u, LAUNCH_TC_ALL = 4u };
+enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u, LAUNCH_TC_ALL = 4u, LAUNCH_SLICE = 8u, LAUNCH_RL = 16u };
+
+#ifdef QMD_TRACE
+// Traced build: the stamp records for the next launch of `ctas` CTAs (QMD_TRACE_FIELDS each), or
+// NULL when no trace buffer is set or it is full.
+unsigned long long *trace_reserve(int ctas);
+#endif
 
 // Record a CUDA error for qmd_last_error_detail and map it to a status.
 qmd_status fail(qmd_status st, const char *what, cudaError_t e);
@@ -65,7 +73,7 @@ struct QmvArgs {
 };
 
 struct QmvPlan {
-    int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh)
+    int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh); 2: row-lane kernel (qmv_rl.cuh)
     int grid, threads, smem, stages;
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;

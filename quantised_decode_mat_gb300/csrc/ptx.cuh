@@ -54,6 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// Index of the multiprocessor this thread runs on.
+__device__ __forceinline__ uint32_t smid()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
@@ -122,6 +130,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// 3-D tiled tensor copy (TMA) global -> this CTA's shared memory: the box the tensor map
+// describes, starting at element coordinates (x, y, z), completing the box's bytes on the
+// barrier.  x times the element size must be a multiple of 16 bytes; dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -16,6 +16,7 @@ namespace qmd {
 
 struct Q8Block {
     uint2 codes;  // this lane's 8 codes, packed little-endian
+    int sum2;     // the sum of the 16 codes of lanes 2s, 2s+1 (valid in both)
     int sum4;     // the lane's sub-block sum (valid in lanes 4j, for sub-block j)
     float d;      // the block scale (valid in every lane)
 };
@@ -47,6 +48,7 @@ __device__ __forceinline__ Q8Block q8k_quantise_block(const float (&v)[8])
     out.codes.y = (q[4] & 255) | ((q[5] & 255) << 8) | ((q[6] & 255) << 16) | ((uint32_t)(q[7] & 255) << 24);
     // sub-block j = lanes 4j .. 4j+3
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    out.sum2 = sum;
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     out.sum4 = sum;
     out.d = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);

@@ -68,7 +68,27 @@ struct QmvKParams {
     float eps;            // RMSNorm form
     unsigned *err;
     unsigned long long wait_ns;
+#ifdef QMD_TRACE
+    unsigned long long *trace;  // traced build: QMD_TRACE_FIELDS time stamps per CTA, or NULL
+#endif
 };
+
+// Traced build only (compiled with -DQMD_TRACE): per-CTA global-timer stamps of the phases of a
+// launch, for the per-phase breakdown of a decode step.  Fields: 0 entry, 1 first weight copies
+// requested, 2 dependency wait released, 3 activations ready, 4 first stage landed, 5 the last
+// stage's rows written, 6 exit (the latest warp), 7 SM id | CTA << 16 | grid << 32 | kind << 48.
+constexpr int QMD_TRACE_FIELDS = 8;
+#ifdef QMD_TRACE
+#define QMD_STAMP(P, I)                                                                            \
+    do {                                                                                           \
+        if ((P).trace)                                                                             \
+            (P).trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS + (I)] = globaltimer_ns();             \
+    } while (0)
+#else
+#define QMD_STAMP(P, I) \
+    do {                \
+    } while (0)
+#endif
 
 // Kernel variants: plain; recording the integer arithmetic; packing f32 activations itself;
 // packing the RMSNorm of x (+ a residual) itself.
@@ -234,6 +254,14 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     const int16_t *s_bs = reinterpret_cast<const int16_t *>(smem + L.bs_off);
     const uint32_t bar0 = smem_addr(smem + L.bar_off);
     const uint32_t ring0 = smem_addr(smem);
+#ifdef QMD_TRACE
+    if (tid == 0 && p.trace) {
+        p.trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS] = globaltimer_ns();
+        p.trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS + 7] =
+            (unsigned long long)smid() | ((unsigned long long)blockIdx.x << 16) |
+            ((unsigned long long)gridDim.x << 32) | ((unsigned long long)(PACK ? 1 : 2) << 48);
+    }
+#endif
     // A launch whose plan does not fit the kernel: the RMSNorm form's sum of squares takes 256
     // threads, and the layout must lie inside the dynamic shared memory the launch was given.
     if ((NORM && NWT < 8) || (uint32_t)L.total > dynamic_smem_bytes()) {
@@ -273,9 +301,13 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     for (int c = warp; c < min(p.stages, nch); c += NWT)
         if (lane == 0)
             issue(c, c);
+    if (tid == 0)
+        QMD_STAMP(p, 1);
 
     pdl_launch_dependents();
     pdl_wait();  // activations come from earlier work in the stream
+    if (tid == 0)
+        QMD_STAMP(p, 2);
 
     // ---- this thread's activation slice, for all B vectors (fixed for every row) ----------
     const int64_t K = (int64_t)nb * 256;
@@ -429,6 +461,8 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
         }
     }
     __syncthreads();
+    if (tid == 0)
+        QMD_STAMP(p, 3);
 
     // lane constants for reading a block's scales and codes
     const bool hiw = (k >> 1) >= 2;  // Q4_K: sub-blocks 4..7 use the split 6-bit fields
@@ -478,6 +512,8 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
             __syncwarp();
             return;
         }
+        if (c == 0 && tid == 0)
+            QMD_STAMP(p, 4);
         const uint8_t *stage = smem + (size_t)st * p.stage_bytes;
         const int64_t rs = r0 + (int64_t)c * TR;
         const int nr = (int)min((int64_t)TR, r1 - rs);
@@ -671,6 +707,8 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
                 s_cnt[st] = 0;
                 if (c + p.stages < nch)
                     issue(c + p.stages, st);  // every warp of the CTA is done with this stage
+                if (c == nch - 1)
+                    QMD_STAMP(p, 5);
             }
         }
         if (++st == p.stages) {
@@ -678,6 +716,10 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
             parity ^= 1u;
         }
     }
+#ifdef QMD_TRACE
+    if (lane == 0 && p.trace)
+        atomicMax(p.trace + (size_t)blockIdx.x * QMD_TRACE_FIELDS + 6, globaltimer_ns());
+#endif
 }
 
 // Launch one kernel instance with the plan's shape: opt in to its shared memory, cap the grid
@@ -860,6 +902,9 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     kp.eps = a.eps;
     kp.err = device_error_word();
     kp.wait_ns = wait_limit_ns();
+#ifdef QMD_TRACE
+    kp.trace = trace_reserve(plan.grid);
+#endif
     if (kp.err == nullptr)
         return QMD_ERR_DEVICE;
     mode = a.g != nullptr ? QMV_NORM : a.x != nullptr ? QMV_PACK : a.dbg_dots != nullptr ? QMV_DUMP : QMV_PLAIN;

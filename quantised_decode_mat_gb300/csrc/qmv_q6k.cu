@@ -1,6 +1,6 @@
 // qmv_q6k.cu -- Q6_K (split layout) instances of the decode mat-vec (batch 1..8, plus the
 // recording variant).
-#include "qmv_tc.cuh"
+#include "qmv_rl.cuh"
 
 namespace qmd {
 
@@ -13,6 +13,8 @@ qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
         return st;
     if (plan.layout == 1)
         return launch_qmv_tc<QMD_Q6_K_SPLIT>(kp, plan, mode, s);
+    if (plan.layout == 2)
+        return launch_qmv_rl<QMD_Q6_K_SPLIT>(kp, plan, mode, a.batch, s);
     return launch_qmv_slice<QMD_Q6_K_SPLIT>(kp, plan, a.batch, mode, s);
 }
 

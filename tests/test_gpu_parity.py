@@ -15,6 +15,7 @@ torch = pytest.importorskip("torch")
 import oracle as O  # noqa: E402
 import quantised_decode_mat_gb300 as q  # noqa: E402
 from quantised_decode_mat_gb300 import synth  # noqa: E402
+from tests.oracle_rows import oracle_rows_threaded  # noqa: E402
 
 pytestmark = [
     pytest.mark.gpu,
@@ -77,18 +78,21 @@ OFMT = {"q4k": O.FMT_Q4_K, "q5k": O.FMT_Q5_K, "q6k": O.FMT_Q6_K}
 QFMT = {"q4k": q.Q4_K, "q5k": q.Q5_K, "q6k": q.Q6_K_SPLIT}
 
 
-def check_against_oracle(fmtname, Wg, x, y, rows_idx=None, exact=True):
-    """y [B, R] from the GPU vs oracle on the same W (canonical) and x; rows_idx samples rows."""
+def check_against_oracle(fmtname, Wg, x, y, rows_idx=None, exact=True, f64_idx=None):
+    """y [B, R] from the GPU vs oracle on the same W (canonical) and x; rows_idx samples rows
+    (default: every row); f64_idx limits the f64 brute force to a sample of those."""
     oqs, od, obs = O.q8k_pack(x)
     W = Wg if rows_idx is None else Wg[rows_idx]
     yg = y if rows_idx is None else y[:, rows_idx]
-    ref = O.qmatvec(OFMT[fmtname], W, oqs, od, obs, O.ORDER_RUNS_OF_SIXTEEN)
+    ref = oracle_rows_threaded(OFMT[fmtname], W, oqs, od, obs, O.ORDER_RUNS_OF_SIXTEEN)
     assert np.isfinite(yg).all(), "unwritten (NaN) outputs"
     err = O.rel_err(yg, ref)
     assert err.max() <= TOL_SAME_ORDER, f"same-order rel err {err.max():.3g}"
     if exact:
         diff = np.count_nonzero(yg.view(np.uint32) != ref.view(np.uint32))
         assert diff == 0, f"{diff} outputs differ in bits from the same-order oracle"
+    if f64_idx is not None:
+        W, yg = W[f64_idx], yg[:, f64_idx]
     ref64 = O.qmatvec_f64(OFMT[fmtname], W, oqs, od)
     assert O.rel_err(yg, ref64).max() <= TOL_F64
 
@@ -179,18 +183,15 @@ def _sample_rows(rows, n, seed):
 
 
 @pytest.mark.parametrize("batch", [1, 2, 4, 8])
-def test_config3_gate_up_sampled(batch):
+def test_config3_gate_up_every_row(batch):
+    """The fused gate|up shape (28672 x 4096) at each of its batches, every output bit-identical to
+    the same-order oracle (threaded over rows); the f64 brute force on a sample of rows."""
     c = synth.CONFIGS[3]
     Wg = synth.weights(c["fmt"], c["seed"], c["rows"], c["K"])
     x = synth.activations(c["seed"], batch, c["K"])
     y = run_matvec(c["fmt"], Wg, gpu_pack(x), c["rows"], c["K"], batch)
     assert np.isfinite(y).all()
-    # rows at every CTA boundary of the launch, plus a random sample
-    info = q.launch_info(q.Q4_K, c["rows"], c["K"], batch)
-    G = info["grid"]
-    bounds = {(c["rows"] * b) // G for b in range(G)} | {(c["rows"] * b) // G - 1 for b in range(1, G)}
-    idx = np.array(sorted(set(_sample_rows(c["rows"], 600, batch).tolist()) | bounds))
-    check_against_oracle(c["fmt"], Wg, x, y, rows_idx=idx)
+    check_against_oracle(c["fmt"], Wg, x, y, f64_idx=_sample_rows(c["rows"], 400, batch))
 
 
 SWEEP = [
@@ -224,15 +225,21 @@ def test_sweep_shapes(fmtname, rows, K, batch):
                                                   ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2),
                                                   ("q6k", 90, 14336, 1), ("q5k", 1500, 4096, 1),
                                                   ("q5k", 300, 3072, 4), ("q4k", 900, 4096, 6)])
-def test_pipeline_plans(plan, fmtname, rows, K, batch):
-    """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits."""
+@pytest.mark.parametrize("flags", [0, 8, 16], ids=["default", "slice", "rowlane"])
+def test_pipeline_plans(plan, fmtname, rows, K, batch, flags):
+    """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits.  For
+    the row-lane kernel (batches 1 and 2 by default, 3 and 4 with flag 16) the plan's row groups
+    are its warps per CTA and its stages the slots of each warp's ring; flag 8 runs the dp4a
+    slice kernel instead."""
     q.debug_set_plan(*plan)
+    q.debug_set_launch_flags(flags)
     try:
         Wg = synth.weights(fmtname, 5, rows, K)
         x = synth.activations(5, batch, K)
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
     finally:
         q.debug_set_plan()
+        q.debug_set_launch_flags(0)
     check_against_oracle(fmtname, Wg, x, y)
 
 
@@ -305,15 +312,27 @@ def test_refused_calls_write_nothing():
 @pytest.mark.parametrize("fmtname", ["q4k", "q6k"])
 @pytest.mark.parametrize("rows,K,batch", [(40, 65536, 1), (21, 32768, 3), (40, 20480, 4), (300, 36864, 2)])
 def test_long_rows_beyond_the_dp4a_limit(fmtname, rows, K, batch):
-    """Rows the dp4a kernel cannot take (more than 128 blocks at one or two vectors, 64 above)
-    run on the tensor-core kernel run by run, bit-identical to the same-order oracle."""
-    info = q.launch_info(QFMT[fmtname], rows, K, batch)
-    assert info["rows_per_stage"] == 16 and info["threads"] == 512
+    """Rows the dp4a slice kernel cannot take (more than 128 blocks at one or two vectors, 64
+    above) run on the row-lane kernel, whose warps walk any row length step by step (the default
+    at one or two vectors, flag 16 at three or four), or on the tensor-core kernel run by run
+    (the default at three or four vectors, flag 8 below).  All bit-identical to the same-order
+    oracle."""
+    assert (q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == RL_ROWS) == (batch <= 2)
     seed = rows + K + batch
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
-    y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
+    xq = gpu_pack(x)
+    y = run_matvec(fmtname, Wg, xq, rows, K, batch)
     check_against_oracle(fmtname, Wg, x, y)
+    for flags, rps in ((SLICE, 16), (RL, RL_ROWS)):
+        q.debug_set_launch_flags(flags)
+        try:
+            info = q.launch_info(QFMT[fmtname], rows, K, batch)
+            assert info["rows_per_stage"] == rps and (rps != 16 or info["threads"] == 512)
+            y2 = run_matvec(fmtname, Wg, xq, rows, K, batch)
+        finally:
+            q.debug_set_launch_flags(0)
+        assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
 @pytest.mark.parametrize("cps", [1, 3, 8])
@@ -326,11 +345,13 @@ def test_long_rows_with_forced_ctas_per_sm(cps):
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
     q.debug_set_plan(0, 0, 0, cps)
+    q.debug_set_launch_flags(SLICE)  # the tensor-core kernel, not the row-lane one
     try:
         assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
     finally:
         q.debug_set_plan()
+        q.debug_set_launch_flags(0)
     check_against_oracle(fmtname, Wg, x, y)
 
 
@@ -405,6 +426,9 @@ def test_fused_refusals():
 # ---- batches of 3..8 on the tensor cores: the same bits as the dp4a kernel -----------------------------
 DP4A_ONLY = 2  # launch flag: keep batches of 5..8 on the dp4a kernel
 TC_ALL = 4     # launch flag: every batch of 3..8 on the tensor-core kernel (long rows run by run)
+SLICE = 8      # launch flag: the dp4a slice kernel instead of the row-lane one
+RL = 16        # launch flag: the row-lane kernel for batches of 3 and 4 as well
+RL_ROWS = 4    # rows per tile of the row-lane kernel (its launch_info rows_per_stage)
 
 
 # rows of one run of at most 16 blocks, and longer rows walked run by run: 17 blocks (a run of
@@ -537,12 +561,12 @@ def test_concurrent_host_threads():
 
 # ---- census: every kernel variant the library can launch, value-checked --------------------------------
 CENSUS = [(f, b, fused, flags) for f in ("q4k", "q5k", "q6k") for b in range(1, 9) for fused in (False, True)
-          for flags in ((0, DP4A_ONLY, TC_ALL) if b >= 5 else (0, TC_ALL) if b >= 3 else (0,))]
+          for flags in ((0, DP4A_ONLY, TC_ALL) if b >= 5 else (0, TC_ALL, RL) if b >= 3 else (0, SLICE))]
+_FLAG_ID = {0: "", DP4A_ONLY: "-dp4a", TC_ALL: "-tc", SLICE: "-slice", RL: "-rowlane"}
 
 
 @pytest.mark.parametrize("fmtname,batch,fused,flags", CENSUS,
-                         ids=[f"{f}-b{b}-{'fused' if fu else 'packed'}{['', '', '-dp4a', '', '-tc'][fl]}"
-                              for f, b, fu, fl in CENSUS])
+                         ids=[f"{f}-b{b}-{'fused' if fu else 'packed'}{_FLAG_ID[fl]}" for f, b, fu, fl in CENSUS])
 def test_census_every_variant(fmtname, batch, fused, flags):
     """Each (format, batch, fused or packed input, kernel layout) the plan can choose, on a small
     ragged case, bit-identical to the same-order oracle; plus the recording variant's dots."""
