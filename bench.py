@@ -316,6 +316,9 @@ def workload_config(args):
     layers = getattr(args, "layers", synth.STEP_LAYERS)
     return {"workload": f"decode_step_7b_q4k_q6k_{layers}layers_b{args.batch}",
             "launch": launch_form(args),
+            "schedule": ("rows split evenly over the SMs" if getattr(args, "no_workspace", False) else
+                         "rows split evenly, the last quarter of each 1-2 vector launch handed out to warps as "
+                         "they free up (scheduling workspace)"),
             "layers": layers,
             "projections": [f"{n}:{f}:{r}x{k}" for (n, f, r, k) in synth.STEP_PROJECTIONS],
             "batch": args.batch,
@@ -405,7 +408,8 @@ def run_ours(args):
     from quantised_decode_mat_gb300 import step as qstep
     q.lib()  # fails loudly if the CUDA library is missing
 
-    step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=use_fused(args))
+    step = qstep.make_step(args.batch, layers=args.layers, device=f"cuda:{local_rank}", fused=use_fused(args),
+                           workspace=not getattr(args, "no_workspace", False))
     dp4a_rate, mma_rate = q.measure_alu()  # before the timed region
     nbytes = step.bytes()
     stream = torch.cuda.current_stream()
@@ -579,6 +583,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=32,
                     help="decoder layers in the step (32 for the 7B-shaped step; fewer only for profiling "
                          "captures, which must stay small)")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="run the mat-vecs without a scheduling workspace (every row split evenly over the SMs)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config mat-vec timings (configs 0-3) reported beside the step")
     ap.add_argument("--cpu-layers", type=int, default=8,

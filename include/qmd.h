@@ -47,6 +47,7 @@ extern "C" {
 #define QMD_Q5K_BLOCK_BYTES 176
 #define QMD_Q6K_BLOCK_BYTES 210
 #define QMD_Q6K_BODY_BYTES 208
+#define QMD_WORKSPACE_BYTES 4096 /* scheduling workspace of qmd_qmatvec_ws / qmd_qmatvec_x_ws */
 
 typedef enum qmd_status {
     QMD_OK = 0,
@@ -188,6 +189,27 @@ qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const fl
                          float *y, int64_t rows, int64_t K, int batch, void *stream);
 
 /*
+ * qmd_qmatvec_ws, qmd_qmatvec_x_ws -- qmd_qmatvec and qmd_qmatvec_x with a scheduling workspace:
+ * the same results, bit for bit.  With one or two vectors (the row-lane kernel) the first three
+ * quarters of the rows are split evenly over the multiprocessors as usual, and the last quarter
+ * is handed to warps four rows at a time, in the order they ask for more work, so that a
+ * multiprocessor that runs slow does not set the end of the launch.  Other plans (three or more
+ * vectors) ignore the workspace.  This is a scheduling choice of this implementation; the pages
+ * have no counterpart.
+ *   workspace  device, QMD_WORKSPACE_BYTES bytes, 16-byte aligned, owned by the caller.  Zero it
+ *              once; every call that completes leaves it zeroed again.  Calls ordered in one stream
+ *              may share one workspace; calls that may run at the same time on the GPU (other
+ *              streams, concurrent graphs) need their own.  After a call reports
+ *              QMD_ERR_DEVICE_TIMEOUT (qmd_get_device_error) zero the workspace again.
+ * Other arguments, limits and errors as qmd_qmatvec / qmd_qmatvec_x; in addition NULL (no
+ * workspace) and MISALIGNED (workspace).
+ */
+qmd_status qmd_qmatvec_ws(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
+                          int64_t rows, int64_t K, int batch, void *workspace, void *stream);
+qmd_status qmd_qmatvec_x_ws(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                            float *y, int64_t rows, int64_t K, int batch, void *workspace, void *stream);
+
+/*
  * qmd_qmatvec_rmsnorm_x -- the residual add, the RMSNorm, the q8_K pack and the mat-vec in one
  * launch: y is exactly qmd_qmatvec(fmt, W, W_aux, qmd_rmsnorm_q8k_pack(x, r, g, eps), ...),
  * with the same bits -- the same h, the same sum-of-squares order, the same codes ("Language
@@ -327,6 +349,7 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream);
  * per stage (1..8, rounded down to 1, 2, 4 or 8, then halved until rows x batch <= 16), a
  * cap on pipeline stages (a cap below 3 keeps batches of 5..8 off the tensor-core kernel), and
  * CTAs per multiprocessor (1..8); 0 keeps the default of each.
+ * For the row-lane kernel, row groups are its warps with a ring and stages the slots of each ring.
  * Results do not depend on the plan; tests use this to drive the stage ring through many
  * wrap-arounds on small inputs.  Process-wide.
  */
@@ -337,10 +360,19 @@ void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int 
  * qmd_q8k_pack and qmd_qmatvec without programmatic dependent launch (plain stream order);
  * bit 1 computes batches of 5..8 vectors with the dp4a kernel even where the tensor-core
  * kernel would be chosen; bit 2 computes every batch of 3..8 vectors with the tensor-core
- * kernel where it fits (rows of more than 16 blocks run by run).  Results are the same either
- * way.  Process-wide.
+ * kernel where it fits (rows of more than 16 blocks run by run); bit 3 keeps one and two vectors
+ * off the row-lane kernel (the dp4a slice kernel, or the tensor-core kernel for rows the slice
+ * kernel cannot take); bit 4 puts three and four vectors on the row-lane kernel as well.  Results
+ * are the same either way.  Process-wide.
  */
 void qmd_debug_set_launch_flags(unsigned flags);
+
+/*
+ * qmd_debug_set_dynamic_tiles -- test-only: the share, per mille (0..1000), of a row-lane launch's
+ * 4-row tiles that qmd_qmatvec_ws hands out by claims (the rest split evenly); any other value
+ * restores the default.  Results do not depend on it.  Process-wide.
+ */
+void qmd_debug_set_dynamic_tiles(int per_mille);
 
 /* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
 int qmd_version(void);

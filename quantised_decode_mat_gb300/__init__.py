@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "libqmd.so")
 
 QMD_QK = 256
 QMD_MAX_BATCH = 8
+QMD_WORKSPACE_BYTES = 4096
 Q4_K = 12
 Q5_K = 13
 Q6_K_SPLIT = 14
@@ -70,6 +71,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_rmsnorm_q8k_pack": ([vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, i64, i32, vp], i32),
             "qmd_qmatvec": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_qmatvec_x": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
+            "qmd_qmatvec_ws": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp], i32),
+            "qmd_qmatvec_x_ws": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp], i32),
             "qmd_qmatvec_rmsnorm_x": ([i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, vp, i64, i64, i32, vp],
                                       i32),
             "qmd_q6k_prefix_stride": ([i64], i64),
@@ -87,6 +90,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_measure_alu": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], i32),
             "qmd_debug_set_plan": ([i32, i32, i32, i32], None),
             "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
+            "qmd_debug_set_dynamic_tiles": ([i32], None),
             "qmd_version": ([], i32),
         }
         if hasattr(L, "qmd_debug_trace"):  # the traced build (include/qmd_trace.h)
@@ -165,30 +169,46 @@ def rmsnorm_q8k_pack(x, r, g, eps: float, h_out=None, out: Q8K | None = None, st
     return out
 
 
-def qmatvec(fmt: int, W, W_aux, xq: Q8K, y=None, rows: int | None = None, stream=None):
-    """qmd_qmatvec: y f32 [batch, rows] = W (fmt) x xq.  W is the uint8 weight tensor whose first
-    dimension is rows; W_aux the Q6_K prefix (None for Q4_K)."""
+def workspace(device="cuda"):
+    """A zeroed scheduling workspace for qmatvec / qmatvec_x (QMD_WORKSPACE_BYTES on `device`).
+    Calls ordered in one stream may share it; concurrent calls need their own."""
+    import torch
+    return torch.zeros(QMD_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device)
+
+
+def qmatvec(fmt: int, W, W_aux, xq: Q8K, y=None, rows: int | None = None, stream=None, workspace=None):
+    """qmd_qmatvec (qmd_qmatvec_ws with a workspace): y f32 [batch, rows] = W (fmt) x xq.  W is the
+    uint8 weight tensor whose first dimension is rows; W_aux the Q6_K prefix (None for Q4_K)."""
     import torch
     rows = W.shape[0] if rows is None else rows
     if y is None:
         y = torch.empty((xq.batch, rows), dtype=torch.float32, device=xq.qs.device)
-    _check(lib().qmd_qmatvec(fmt, _ptr(W), _ptr(W_aux), xq.ptrs(), _ptr(y), rows, xq.K, xq.batch,
-                             _stream(stream)))
+    if workspace is None:
+        _check(lib().qmd_qmatvec(fmt, _ptr(W), _ptr(W_aux), xq.ptrs(), _ptr(y), rows, xq.K, xq.batch,
+                                 _stream(stream)))
+    else:
+        _check(lib().qmd_qmatvec_ws(fmt, _ptr(W), _ptr(W_aux), xq.ptrs(), _ptr(y), rows, xq.K, xq.batch,
+                                    _ptr(workspace), _stream(stream)))
     return y
 
 
 def qmatvec_x(fmt: int, W, W_aux, x, y=None, rows: int | None = None, xq_out: Q8K | None = None,
-              stream=None):
-    """qmd_qmatvec_x: y f32 [batch, rows] = W (fmt) x q8k_pack(x), packing inside the kernel.
-    x: f32 [batch, K].  xq_out: optional Q8K that receives the packed activations."""
+              stream=None, workspace=None):
+    """qmd_qmatvec_x (qmd_qmatvec_x_ws with a workspace): y f32 [batch, rows] = W (fmt) x
+    q8k_pack(x), packing inside the kernel.  x: f32 [batch, K].  xq_out: optional Q8K that
+    receives the packed activations."""
     import torch
     rows = W.shape[0] if rows is None else rows
     batch, K = x.shape
     if y is None:
         y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
     out = xq_out.ptrs() if xq_out is not None else Q8KPtrs(None, None, None)
-    _check(lib().qmd_qmatvec_x(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
-                               _stream(stream)))
+    if workspace is None:
+        _check(lib().qmd_qmatvec_x(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
+                                   _stream(stream)))
+    else:
+        _check(lib().qmd_qmatvec_x_ws(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
+                                      _ptr(workspace), _stream(stream)))
     return y
 
 
@@ -293,6 +313,10 @@ def debug_set_plan(row_groups: int = 0, rows_per_stage: int = 0, max_stages: int
 
 def debug_set_launch_flags(flags: int = 0) -> None:
     lib().qmd_debug_set_launch_flags(int(flags))
+
+
+def debug_set_dynamic_tiles(per_mille: int = -1) -> None:
+    lib().qmd_debug_set_dynamic_tiles(int(per_mille))
 
 
 def version() -> int:

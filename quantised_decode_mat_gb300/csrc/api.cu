@@ -26,6 +26,16 @@ static __device__ unsigned int g_error_word;
 static thread_local char g_detail[320];
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 static std::atomic<int> g_force_rg{0}, g_force_rows{0}, g_force_stages{0}, g_force_cps{0};
+// Per mille of a row-lane launch's tiles handed out by claims when a workspace is given
+// (measured on the 7B shapes; qmd_debug_set_dynamic_tiles overrides it).
+static constexpr int DYN_PERMILLE = 250;
+static std::atomic<int> g_dyn_permille{-1};
+
+int64_t dynamic_tiles(int64_t tiles)
+{
+    const int pm = g_dyn_permille.load() >= 0 ? g_dyn_permille.load() : DYN_PERMILLE;
+    return tiles * pm / 1000;
+}
 
 qmd_status fail(qmd_status st, const char *what, cudaError_t e)
 {
@@ -193,8 +203,8 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
 
 // Row-lane kernel (qmv_rl.cuh): one CTA per SM (more when forced), a ring for as many warps as
 // the CTA has 4-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
-// has steps) that fits beside the activations, and up to 16 warps to pack them.  false if
-// nothing fits (very long rows).
+// has steps) that fits beside the activations, up to 16 warps to pack them, and one more warp
+// that requests the rings' first fills.  false if nothing fits (very long rows).
 static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
 {
     const int64_t tiles = (rows + RL_ROWS - 1) / RL_ROWS;
@@ -204,9 +214,10 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (grid > tiles)
         grid = tiles;
     const int64_t per_cta = (tiles + grid - 1) / grid;
-    int W = g_force_rg.load() > 0 ? g_force_rg.load() : (int)(per_cta < RL_MAX_WARPS ? per_cta : RL_MAX_WARPS);
-    if (W > RL_MAX_WARPS)
-        W = RL_MAX_WARPS;
+    const int wmax = rl_max_warps(batch);
+    int W = g_force_rg.load() > 0 ? g_force_rg.load() : (int)(per_cta < wmax ? per_cta : wmax);
+    if (W > wmax)
+        W = wmax;
     if (W < 1)
         W = 1;
     int budget = dev.smem_per_sm / cps - 1024;
@@ -225,18 +236,22 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // pack, up to 16, even where fewer warps have tiles
     int NW = W;
     const int64_t blocks = (int64_t)batch * nb;
-    const int want = (int)(blocks < RL_MAX_WARPS ? blocks : RL_MAX_WARPS);
+    const int want = (int)(blocks < wmax ? blocks : wmax);
     if (g_force_rg.load() <= 0 && NW < want)
         NW = want;
     pl->layout = 2;
     pl->grid = (int)grid;
-    pl->threads = 32 * NW;
+    pl->threads = 32 * (NW + 1);  // plus the warp that requests the first ring fills
     pl->smem = qmv_rl_layout(fmt, W, S, batch, nb).total;
     pl->stages = S;
     pl->WR = W;
     pl->RG = 1;
     pl->PR = RL_ROWS;
     pl->stage_bytes = rl_slot_bytes(fmt);
+    // ring slots per warp requested before the dependency wait (the rest right after it); a
+    // forced rows-per-stage value stands for this count here
+    const int pre = g_force_rows.load() > 0 ? g_force_rows.load() : RL_PRE_STEPS;
+    pl->pre_steps = pre < S ? pre : S;
     return true;
 }
 
@@ -463,7 +478,8 @@ struct NormArgs {
 
 qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y,
                           int64_t rows, int64_t K, int batch, int32_t *dots, int32_t *sm, bool dump,
-                          const float *x, qmd_q8k xq_out, void *stream, const NormArgs &na = NormArgs())
+                          const float *x, qmd_q8k xq_out, void *stream, const NormArgs &na = NormArgs(),
+                          void *workspace = nullptr)
 {
     if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
         return QMD_ERR_FORMAT;
@@ -489,7 +505,8 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
         (fused && !aligned(x, 16)) ||
         (fused && want_out && (!aligned(xq_out.qs, 16) || !aligned(xq_out.bsums, 16) || !aligned(xq_out.d, 4))) ||
         (dump && (!aligned(dots, 16) || !aligned(sm, 16))) ||
-        (na.g && (!aligned(na.g, 16) || (na.r && !aligned(na.r, 16)) || (na.h_out && !aligned(na.h_out, 16)))))
+        (na.g && (!aligned(na.g, 16) || (na.r && !aligned(na.r, 16)) || (na.h_out && !aligned(na.h_out, 16)))) ||
+        (workspace && !aligned(workspace, 16)))
         return QMD_ERR_MISALIGNED;
     if (na.g) {
         if (!(na.eps >= 0.0f) || !(na.eps <= 3.4028234663852886e38f))  // rejects NaN, negatives and +inf
@@ -528,6 +545,7 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
     a.g = na.g;
     a.eps = na.eps;
     a.h_out = na.h_out;
+    a.ws = static_cast<unsigned *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return q6 ? launch_qmv_q6k(a, plan, s) : fmt == QMD_Q5_K ? launch_qmv_q5k(a, plan, s) : launch_qmv_q4k(a, plan, s);
 }
@@ -590,6 +608,26 @@ qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const fl
         return QMD_ERR_NULL;
     const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
     return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream);
+}
+
+qmd_status qmd_qmatvec_ws(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_const xq, float *y, int64_t rows,
+                          int64_t K, int batch, void *workspace, void *stream)
+{
+    if (!workspace)
+        return QMD_ERR_NULL;
+    const qmd_q8k none = {nullptr, nullptr, nullptr};
+    return qmatvec_common(fmt, W, W_aux, xq, y, rows, K, batch, nullptr, nullptr, false, nullptr, none, stream,
+                          NormArgs(), workspace);
+}
+
+qmd_status qmd_qmatvec_x_ws(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                            float *y, int64_t rows, int64_t K, int batch, void *workspace, void *stream)
+{
+    if (!x || !workspace)
+        return QMD_ERR_NULL;
+    const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
+    return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream,
+                          NormArgs(), workspace);
 }
 
 qmd_status qmd_qmatvec_rmsnorm_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, const float *r,
@@ -766,6 +804,11 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)
 }
 
 void qmd_debug_set_launch_flags(unsigned flags) { g_launch_flags.store(flags); }
+
+void qmd_debug_set_dynamic_tiles(int per_mille)
+{
+    g_dyn_permille.store(per_mille >= 0 && per_mille <= 1000 ? per_mille : -1);
+}
 
 #ifdef QMD_TRACE
 qmd_status qmd_debug_trace(void *buf, int64_t records)

@@ -70,7 +70,11 @@ struct QmvArgs {
     const float *g = nullptr;  // non-NULL selects the RMSNorm form (packs RMSNorm(x + r) * g)
     float *h_out = nullptr;    // RMSNorm form: optional h = x + r, written by CTA 0
     float eps = 0.0f;
+    unsigned *ws = nullptr;    // optional scheduling workspace (row-lane kernel)
 };
+
+// Row-lane kernel with a workspace: how many of `tiles` 4-row tiles are handed out by claims.
+int64_t dynamic_tiles(int64_t tiles);
 
 struct QmvPlan {
     int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh); 2: row-lane kernel (qmv_rl.cuh)
@@ -78,6 +82,7 @@ struct QmvPlan {
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;
     int tc_rows;  // tensor-core kernel: rows per CTA rounded up to 16 (sizes the run sums)
+    int pre_steps = 0;  // row-lane kernel: ring slots per warp requested before the dependency wait
 };
 
 // Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.

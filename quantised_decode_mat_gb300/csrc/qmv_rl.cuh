@@ -42,10 +42,18 @@ namespace qmd {
 constexpr int RL_ROWS = 4;        // rows per tile (lane bits 3..4)
 constexpr int RL_BLOCKS = 8;      // blocks per step (lane bits 0..2)
 constexpr int RL_ACT = 272;       // shared-memory bytes per activation block: 256 codes + 16 pad
-constexpr int RL_MAX_WARPS = 16;  // warps per CTA
+constexpr int RL_MAX_WARPS = 16;  // warps that own rings, and warps that pack
+// Ring / packing warps a CTA may have for B vectors: 16 for one or two, 8 above (so that the
+// larger per-lane state of three and four vectors fits in registers), plus the warp that
+// requests the first ring fills.
+__host__ __device__ constexpr int rl_max_warps(int B) { return B <= 2 ? RL_MAX_WARPS : RL_MAX_WARPS / 2; }
+__host__ __device__ constexpr int rl_max_threads(int B) { return 32 * (rl_max_warps(B) + 1); }
 constexpr int RL_MAX_BATCH = 4;   // vectors per launch
 constexpr int RL_DEFAULT_BATCH = 2;  // the plan's default for at most this many vectors
-constexpr int RL_PRE = 1;         // steps per warp requested before the programmatic-launch wait
+constexpr int RL_POOLS = 8;          // claim pools of the scheduling workspace (CTA b draws from pool b % 8)
+constexpr int RL_WS_STRIDE = 64;     // words between the workspace's counters (256 bytes: separate L2 lines)
+static_assert(RL_WS_STRIDE * (RL_POOLS + 1) * 4 <= QMD_WORKSPACE_BYTES, "the pools' counters and the done word");
+constexpr int RL_PRE_STEPS = 1;   // default ring slots per warp requested before the dependency wait
 
 __host__ __device__ constexpr int rl_block_bytes(int f) { return f == QMD_Q6_K_SPLIT ? 208 : f == QMD_Q5_K ? 176 : 144; }
 __host__ __device__ constexpr int rl_box_bytes(int f) { return RL_ROWS * RL_BLOCKS * rl_block_bytes(f); }
@@ -55,18 +63,23 @@ __host__ __device__ constexpr int rl_tx_bytes(int f) { return rl_box_bytes(f) + 
 __host__ __device__ constexpr int rl_slot_bytes(int f) { return rl_box_bytes(f) + (f == QMD_Q6_K_SPLIT ? 128 : 0); }
 
 struct RlLayout {
-    int bar_off, act_off, dx_off, aux_off, total;
+    int bar_off, tile_off, sched_off, act_off, dx_off, aux_off, total;
 };
 
-// Shared memory: rings [W][S][slot] | mbarriers u64 [W][S] | activation codes i8 [B][nb][272] |
-// block scales f32 [B][nb] | Q4_K, Q5_K: sums i16 [B][nb][8] of each 32 codes; Q6_K: sums i16
-// [B][nb][16] of each 16 codes (for the -32 offset of the weight codes).
+// Shared memory: rings [W][S][slot] | mbarriers u64 [W][S] | the tile of each slot's step i32
+// [W][S] | activation codes i8 [B][nb][272] | block scales f32 [B][nb] | Q4_K, Q5_K: sums i16
+// [B][nb][8] of each 32 codes; Q6_K: sums i16 [B][nb][16] of each 16 codes (for the -32 offset
+// of the weight codes).
 __host__ __device__ inline RlLayout qmv_rl_layout(int f, int W, int S, int B, int nb)
 {
     RlLayout L;
     int o = W * S * rl_slot_bytes(f);
     L.bar_off = o;
-    o = align_up(o + W * S * 8, 16);
+    o += W * S * 8;
+    L.tile_off = o;
+    o += W * S * 4;
+    L.sched_off = o;  // two words: the CTA's pool is empty; warps done claiming
+    o = align_up(o + 8, 16);
     L.act_off = o;
     o += B * nb * RL_ACT;
     L.dx_off = o;
@@ -278,7 +291,7 @@ __device__ __forceinline__ void rl_block_terms(const uint8_t *bp, const int8_t *
 
 // F is QMD_Q4_K, QMD_Q5_K or QMD_Q6_K_SPLIT; B the vectors; MODE plain, recording or packing.
 template <int F, int B, int MODE>
-__global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __grid_constant__ RlParams rp)
+__global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __grid_constant__ RlParams rp)
 {
     constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
     constexpr bool PACK = MODE == QMV_PACK;
@@ -291,14 +304,23 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int W = p.WR, S = p.stages, nb = p.nb;  // W warps own rings and tiles
-    const int NW = blockDim.x >> 5;                // all the CTA's warps pack the activations
+    const int W = p.WR, S = p.stages, nb = p.nb;  // warps 0 .. W-1 own rings and tiles
+    const int NW = blockDim.x >> 5;                // warp NW-1 requests the first ring fills,
+    const int NP = NW - 1;                         // warps 0 .. NP-1 pack the activations
     const int r = lane >> 3, g = lane & 7;
     const int nsteps = (nb + RL_BLOCKS - 1) / RL_BLOCKS;
-    const int64_t ntiles = (p.rows + RL_ROWS - 1) / RL_ROWS;
-    const int64_t t0 = ntiles * blockIdx.x / gridDim.x, t1 = ntiles * (blockIdx.x + 1) / gridDim.x;
-    const int64_t ntw = (warp < W && t1 - t0 > warp) ? (t1 - t0 - warp + W - 1) / W : 0;  // this warp's tiles
-    const int64_t total = ntw * nsteps;                                     // and its steps
+    // The tiles: without a workspace, CTA b owns q or q + 1 consecutive tiles of an even split
+    // [ts0, ts1) and its warp w takes ts0 + w, ts0 + w + W, ...  With one, only the first `nstat`
+    // tiles are split so; the last p.dyn_tiles go to warps one at a time, in the order their
+    // claims reach the workspace's counters (after the dependency wait), so that CTAs which run
+    // slow do not set the end.  (Tile counts are below 2^29: 32-bit arithmetic.)
+    unsigned *const ws = p.ws;
+    const unsigned ntiles = (unsigned)((p.rows + RL_ROWS - 1) / RL_ROWS);
+    const unsigned ndyn = ws ? (unsigned)p.dyn_tiles : 0u;
+    const unsigned nstat = ntiles - ndyn;
+    const unsigned bx = blockIdx.x, G = gridDim.x;
+    const unsigned st_q = nstat / G, st_rem = nstat - st_q * G;
+    const int64_t ts0 = (int64_t)bx * st_q + min(bx, st_rem), ts1 = ts0 + st_q + (bx < st_rem ? 1 : 0);
     const RlLayout L = qmv_rl_layout(F, W, S, B, nb);
 #ifdef QMD_TRACE
     if (tid == 0 && p.trace) {
@@ -310,49 +332,150 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
 #endif
     // A launch whose geometry is not the plan's: flag it and leave without touching memory (after
     // the dependency wait, so that kernels launched after this one still see its predecessor done).
-    if ((int)blockDim.x < 32 * W || (uint32_t)L.total > dynamic_smem_bytes()) {
+    if (NW < W + 1 || (uint32_t)L.total > dynamic_smem_bytes()) {
         pdl_wait();
         if (tid == 0)
             atomicOr(p.err, ERRBIT_PLAN);
         return;
     }
 
-    const int wr = warp < W ? warp : 0;  // warps past W have no ring (and no steps)
-    uint8_t *ring = smem + (size_t)wr * S * SLOT;
-    const uint32_t bar0 = smem_addr(smem + L.bar_off) + 8u * (uint32_t)(wr * S);
     const uint64_t pol = policy_evict_first();
-    // the copies of one step (tile, s) into ring slot `slot`; lane 0 only
-    auto issue = [&](int64_t tile, int s, int slot) {
-        const uint32_t bar = bar0 + 8u * (uint32_t)slot;
+    const uint32_t bars = smem_addr(smem + L.bar_off);
+    int *const s_tiles = reinterpret_cast<int *>(smem + L.tile_off);
+    // the copies of step s of `tile` into slot `slot` of warp w's ring (one thread)
+    auto issue_w = [&](int w, int64_t tile, int s, int slot) {
+        const uint32_t bar = bars + 8u * (uint32_t)(w * S + slot);
+        s_tiles[w * S + slot] = (int)tile;
         mbar_arrive_expect_tx(bar, (uint32_t)rl_tx_bytes(F));
-        const uint32_t dst = smem_addr(ring + (size_t)slot * SLOT);
+        const uint32_t dst = smem_addr(smem + (size_t)(w * S + slot) * SLOT);
         tma_load_3d(dst, &rp.wmap, 0, RL_BLOCKS * s, (int)(RL_ROWS * tile), bar, pol);
         if (Q6)
             tma_load_2d(dst + BOX, &rp.premap, RL_BLOCKS * s, (int)(RL_ROWS * tile), bar, pol);
     };
-    // issue cursor: the next step to request (tile, step within the tile)
-    int64_t itile = t0 + warp;
-    int is = 0;
-    int64_t issued = 0;
-    // Before the wait, weights only, and only RL_PRE steps per warp: the tensor-copy unit takes
-    // about 40 ns per box, so a full ring per warp (tens of boxes per SM) would hold up the wait
-    // and the activations; the rest of each ring is requested once they are in place.
-    if (lane == 0 && warp < W) {
-        for (int i = 0; i < S; ++i)
-            mbar_init(bar0 + 8u * (uint32_t)i, 1);
+    volatile int *s_sched = reinterpret_cast<volatile int *>(smem + L.sched_off);  // [0] pool empty, [1] warps done
+    if (tid == 0) {
+        s_sched[0] = 0;
+        s_sched[1] = 0;
+    }
+    if (warp == NP && lane == 0) {
+        for (int i = 0; i < W * S; ++i)
+            mbar_init(bars + 8u * (uint32_t)i, 1);
         fence_barrier_init();
-        for (; issued < RL_PRE && issued < S && issued < total; ++issued) {
-            issue(itile, is, (int)issued);
-            if (++is == nsteps) {
-                is = 0;
-                itile += W;
+    }
+    __syncthreads();  // barriers initialised before any warp waits on them
+    pdl_launch_dependents();
+
+    // The first S steps of every ring's static tiles, requested by the one warp that does
+    // nothing else (a tensor copy takes the unit tens of nanoseconds, so a few dozen of them would
+    // hold up the packing warps), slot by slot across the warps so that every warp's first step
+    // comes first: p.pre_steps slots before the dependency wait (they read weights only; a
+    // deeper burst there measured slower where the launch's CTAs start only as the previous
+    // launch ends, since it holds up that launch's last stores and this one's activation loads),
+    // the rest as soon as the wait is over.
+    if (warp == NP) {
+        if (lane == 0) {
+            int64_t tk = 0;  // the static tile (of each warp's sequence) of step k
+            int sk = 0;      // and the step within it
+            for (int k = 0; k < S; ++k) {
+                if (k == p.pre_steps) {
+                    QMD_STAMP(p, 1);
+                    pdl_wait();
+                }
+                for (int w = 0; w < W; ++w) {
+                    const int64_t t = ts0 + w + tk * W;
+                    if (t < ts1)
+                        issue_w(w, t, sk, k);
+                }
+                if (++sk == nsteps) {
+                    sk = 0;
+                    ++tk;
+                }
             }
         }
+        return;  // the copies complete on the barriers by themselves
     }
-    if (tid == 0)
-        QMD_STAMP(p, 1);
 
-    pdl_launch_dependents();
+    const int wr = warp < W ? warp : 0;  // packing warps past W have no ring (and no steps)
+    const uint32_t bar0 = bars + 8u * (uint32_t)(wr * S);
+    auto issue = [&](int64_t tile, int s, int slot) { issue_w(wr, tile, s, slot); };
+    // Lane 0's schedule: the next static tile, then claimed ones.  The dynamic tiles are cut into
+    // RL_POOLS pools, one per group of CTAs (b % RL_POOLS), each with its own counter, so that
+    // claims spread over several addresses.  A claim is sent one tile ahead, so that its answer
+    // is back when the tile's first copy is issued; every answer is used (a tile of the pool) or
+    // marks the pool empty for the whole CTA (a shared-memory flag, so that the CTA's other warps
+    // stop asking).  The last warp of a CTA to finish claiming counts the CTA on the workspace's
+    // done word; the CTA that completes that count resets every word to 0, so the next call that
+    // uses the workspace finds it zeroed.
+    const unsigned npools = G < (unsigned)RL_POOLS ? G : (unsigned)RL_POOLS;
+    const unsigned pool = bx % npools;
+    const unsigned pq = ndyn / npools, prem = ndyn - pq * npools;
+    const int64_t pool0 = (int64_t)nstat + (int64_t)pool * pq + min(pool, prem);
+    const int64_t pool_n = pq + (pool < prem ? 1 : 0);
+    unsigned *const cnt = ws ? ws + RL_WS_STRIDE * pool : nullptr;
+    // the cursor after the steps the first warp requested: n0 of this warp's static steps
+    const int64_t nstw = (warp < W && ts1 - ts0 > warp) ? (ts1 - ts0 - warp + W - 1) / W : 0;
+    const int64_t n0 = nstw * nsteps < S ? nstw * nsteps : S;
+    int64_t issued = n0;
+    int is = (int)(n0 % nsteps);
+    int64_t itile = ts0 + warp + (n0 / nsteps) * W;  // mid-tile (is > 0): the tile being requested
+    int64_t st_next = is ? itile + W : itile;        // the next static tile to start
+    unsigned pending = 0u;
+    bool have_pending = false, claims_done = (ws == nullptr);
+    auto finish_claims = [&]() {
+        claims_done = true;
+        if (atomicAdd(const_cast<int *>(s_sched) + 1, 1) == W - 1 &&
+            atomicAdd(ws + RL_WS_STRIDE * RL_POOLS, 1u) == gridDim.x - 1u) {
+            for (int k = 0; k < RL_POOLS; ++k)
+                atomicExch(ws + RL_WS_STRIDE * k, 0u);
+            atomicExch(ws + RL_WS_STRIDE * RL_POOLS, 0u);
+        }
+    };
+    auto next_tile = [&](bool dyn_ok) -> int64_t {
+        if (st_next < ts1) {
+            const int64_t t = st_next;
+            st_next += W;
+            if (st_next >= ts1 && dyn_ok && !claims_done && !have_pending && !s_sched[0]) {
+                pending = atomicAdd(cnt, 1u);  // the first claim, sent early
+                have_pending = true;
+            }
+            return t;
+        }
+        if (!dyn_ok || claims_done)
+            return -1;
+        unsigned c;
+        if (have_pending) {
+            c = pending;
+            have_pending = false;
+        } else if (s_sched[0]) {
+            finish_claims();
+            return -1;
+        } else {
+            c = atomicAdd(cnt, 1u);
+        }
+        if ((int64_t)c >= pool_n) {
+            s_sched[0] = 1;
+            finish_claims();
+            return -1;
+        }
+        if (!s_sched[0]) {
+            pending = atomicAdd(cnt, 1u);  // the next claim, sent early
+            have_pending = true;
+        }
+        return pool0 + c;
+    };
+    auto issue_next = [&](bool dyn_ok, int slot) -> bool {  // lane 0: request the next step into `slot`
+        if (is == 0) {
+            itile = next_tile(dyn_ok);
+            if (itile < 0)
+                return false;
+        }
+        issue(itile, is, slot);
+        if (++is == nsteps)
+            is = 0;
+        ++issued;
+        return true;
+    };
+
     pdl_wait();  // activations come from earlier work in the stream
     if (tid == 0)
         QMD_STAMP(p, 2);
@@ -365,11 +488,11 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
     if (PACK) {
         // quantise the f32 activations, one warp per block, the stand-alone pack's arithmetic
         const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
-        for (int b0 = warp; b0 < NBv; b0 += 4 * NW) {
+        for (int b0 = warp; b0 < NBv; b0 += 4 * NP) {
             float4 xa[4], xb[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * NW;
+                const int b = b0 + u * NP;
                 if (b < NBv) {
                     const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
                     xa[u] = src[0];
@@ -378,7 +501,7 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * NW;  // the same for every lane of the warp
+                const int b = b0 + u * NP;  // the same for every lane of the warp
                 if (b < NBv) {
                     const float v8[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
                     const Q8Block qb = q8k_quantise_block(v8);
@@ -404,32 +527,27 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
     } else {
         // packed input: the codes 16 bytes at a time into the padded blocks; Q6_K also sums each
         // 16 codes; the scales and (Q4_K, Q5_K) the 32-code sums
-        for (int i = tid; i < NBv * 16; i += blockDim.x) {
+        for (int i = tid; i < NBv * 16; i += 32 * NP) {
             const int b = i >> 4, c = i & 15;
             const uint4 q = *reinterpret_cast<const uint4 *>(p.xqs + (int64_t)b * 256 + 16 * c);
             *reinterpret_cast<uint4 *>(acts + (size_t)b * RL_ACT + 16 * c) = q;
             if (Q6)
                 saux[b * 16 + c] = (int16_t)dp4a4(q, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u), 0);
         }
-        for (int i = tid; i < NBv; i += blockDim.x) {
+        for (int i = tid; i < NBv; i += 32 * NP) {
             sdx[i] = p.xd[i];
             if (!Q6)
                 *reinterpret_cast<int4 *>(saux + i * 8) = reinterpret_cast<const int4 *>(p.xbs)[i];
         }
     }
-    __syncthreads();
+    // the packing warps only (the requesting warp has left)
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * NP) : "memory");
     if (tid == 0)
         QMD_STAMP(p, 3);
-    // the rest of the ring
-    if (lane == 0 && warp < W) {
-        for (; issued < S && issued < total; ++issued) {
-            issue(itile, is, (int)issued);
-            if (++is == nsteps) {
-                is = 0;
-                itile += W;
-            }
+    // the rest of the ring (claims may start now)
+    if (lane == 0 && warp < W)
+        while (issued < S && issue_next(true, (int)issued)) {
         }
-    }
 
     // ---- the warp's steps --------------------------------------------------------------------
     const unsigned long long wait_ns = p.wait_ns;
@@ -437,20 +555,22 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
 #pragma unroll
     for (int v = 0; v < B; ++v)
         T[v] = R[v] = 0.0f;
-    int64_t tile = t0 + warp;
+    int64_t tile = -1;
     int s = 0, slot = 0;
     uint32_t par = 0u;
 #pragma unroll 1
-    for (int64_t i = 0; i < total; ++i) {
+    for (int64_t i = 0; warp < W; ++i) {
+        if (!__shfl_sync(0xffffffffu, (int)(issued > i), 0))  // lane 0 knows whether step i exists
+            break;
         // (the whole warp takes the same branch: a lane that gave up makes every lane leave)
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8u * (uint32_t)slot, par, wait_ns))) {
             // A copy did not land in time: flag it, wait (bounded) for this warp's copies that
-            // may still be in flight (steps i .. i + S - 1), leave.
+            // may still be in flight (steps i .. issued - 1), settle its claims, leave.
             if (lane == 0) {
                 atomicOr(p.err, ERRBIT_QMV_WAIT);
                 int sl = slot;
                 uint32_t pa = par;
-                for (int64_t j = i; j < total && j < i + S; ++j) {
+                for (int64_t j = i; j < issued; ++j) {
                     if (!mbar_wait_bounded(bar0 + 8u * (uint32_t)sl, pa, wait_ns)) {
                         atomicOr(p.err, ERRBIT_DRAIN_WAIT);
                         break;
@@ -460,13 +580,17 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
                         pa ^= 1u;
                     }
                 }
+                if (!claims_done)
+                    finish_claims();
             }
             __syncwarp();
             return;
         }
         if (i == 0 && warp == 0 && lane == 0)
             QMD_STAMP(p, 4);
-        const uint8_t *box = ring + (size_t)slot * SLOT;
+        if (s == 0)
+            tile = s_tiles[wr * S + slot];
+        const uint8_t *box = smem + (size_t)(wr * S + slot) * SLOT;
         const int blk = RL_BLOCKS * s + g;
         const int64_t row = RL_ROWS * tile + r;
         float t[B];
@@ -482,14 +606,9 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
         }
         // the slot is consumed: refill it with the step S ahead
         __syncwarp();
-        if (lane == 0 && issued < total) {
+        if (lane == 0) {
             fence_proxy_async_smem();
-            issue(itile, is, slot);
-            ++issued;
-            if (++is == nsteps) {
-                is = 0;
-                itile += W;
-            }
+            issue_next(true, slot);
         }
         // groups of four blocks: lanes g < 4 hold group 2s, lanes g >= 4 group 2s + 1
 #pragma unroll
@@ -516,7 +635,6 @@ __global__ void __launch_bounds__(RL_MAX_WARPS * 32, 1) qmv_rl_kernel(const __gr
                         p.y[(int64_t)v * p.rows + row] = T[v];
             }
             s = 0;
-            tile += W;
         } else {
             ++s;
         }

@@ -61,18 +61,19 @@ class Projection:
         return self.weight_bytes + B * self.K * 4 + B * self.rows * 4
 
 
-# Longest row (values) whose q8_K pack the default step fuses into the mat-vec.
-FUSE_MAX_K = 8192
+# Most vectors whose q8_K pack the default step fuses into the mat-vec.
+FUSE_MAX_BATCH = 2
 
 
 def fuse_pack(batch: int, K: int) -> bool:
     """Default launch form of a projection: one launch that packs inside the mat-vec
-    (qmd_qmatvec_x) for a single vector and rows of at most FUSE_MAX_K values; the stand-alone
-    pack followed by the mat-vec otherwise.  Every CTA of a fused launch packs the whole input
-    for itself after the dependency wait, which costs more than a second launch once the input
-    is long (the 14336-wide down projection: 36.9 against 38.0 us per layer) or holds several
-    vectors (measured on the 7B shapes)."""
-    return batch == 1 and K <= FUSE_MAX_K
+    (qmd_qmatvec_x) for one or two vectors (the row-lane kernel, whose CTAs pack with all their
+    warps: the fused form was as fast as or faster than pack + mat-vec on every 7B shape, the
+    14336-wide down projection included); the stand-alone pack followed by the mat-vec for more
+    vectors, where every CTA of a fused launch would pack the whole batch for itself after the
+    dependency wait (67 / 95 / 109 against 45 / 80 / 92 us per layer at 2 / 4 / 8 vectors on the
+    older kernels)."""
+    return batch <= FUSE_MAX_BATCH
 
 
 @dataclass
@@ -82,6 +83,7 @@ class DecodeStep:
     x_all: "object" = None
     y_all: "object" = None
     host_weights: dict = field(default_factory=dict)  # (layer, name) -> canonical GGUF bytes, if kept
+    ws: "object" = None    # the scheduling workspace every mat-vec of the step uses (one stream), or None
 
     @property
     def form(self) -> str:
@@ -93,10 +95,10 @@ class DecodeStep:
     def run(self, stream=None) -> None:
         for p in self.projs:
             if p.fused:
-                qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
+                qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream, workspace=self.ws)
             else:
                 q8k_pack(p.x, p.xq, stream)
-                qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+                qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream, workspace=self.ws)
 
     def run_matvecs(self, fmt: int | None = None, stream=None) -> int:
         """The step's mat-vec launches only (fused form: each packs its own activations)."""
@@ -104,9 +106,9 @@ class DecodeStep:
         for p in self.projs:
             if fmt is None or p.fmt == fmt:
                 if p.fused:
-                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream)
+                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=stream, workspace=self.ws)
                 else:
-                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream)
+                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, stream, workspace=self.ws)
                 n += 1
         return n
 
@@ -154,10 +156,10 @@ class DecodeStep:
                 cur.wait_event(x_ready[i])
             for p in span[l]:
                 if p.fused:
-                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=cur)
+                    qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, stream=cur, workspace=self.ws)
                 else:
                     q8k_pack(p.x, p.xq, cur)
-                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, cur)
+                    qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, cur, workspace=self.ws)
             for g in groups:
                 if g[-1] == l:
                     done = torch.cuda.Event()
@@ -217,16 +219,19 @@ def _gen_layer(layer: int, projections, batch: int, seed_fn):
 
 def make_step(batch: int, layers: int = synth.STEP_LAYERS, projections=synth.STEP_PROJECTIONS,
               device="cuda", seed_fn=synth.step_seed, keep_host_layers=(), threads: int = 8,
-              fused: bool | None = None) -> DecodeStep:
+              fused: bool | None = None, workspace: bool = True) -> DecodeStep:
     """Generate the seeded weights and activations of a decode step and place them on the device.
 
     keep_host_layers: layers whose canonical GGUF weight bytes stay in host memory (for the
     oracle).  Q6_K weights are bound (split) on the device.  fused: True for one launch per
     projection (qmd_qmatvec_x), False for pack + mat-vec, None for the faster of the two per
-    projection (fuse_pack)."""
+    projection (fuse_pack).  workspace: the mat-vecs share one scheduling workspace (the step
+    runs in one stream), which hands the last rows of each launch to warps as they free up."""
     import torch
+    from . import workspace as new_workspace
     dev = torch.device(device)
     step = DecodeStep(batch=batch)
+    step.ws = new_workspace(dev) if workspace else None
     x_sizes = [batch * K for (_, _, _, K) in projections] * layers
     y_sizes = [(batch * rows + 3) // 4 * 4 for (_, _, rows, _) in projections] * layers
     step.x_all = torch.empty(sum(x_sizes), dtype=torch.float32, device=dev)

@@ -16,8 +16,8 @@ def test_pack_is_fused_for_one_vector_and_short_rows_unless_asked():
     assert bench.use_fused(_args(batch=1)) is None  # the per-projection default
     assert bench.use_fused(_args(batch=4, fused=True)) is True
     assert bench.use_fused(_args(batch=1, unfused=True)) is False
-    assert fuse_pack(1, 4096) and fuse_pack(1, 8192)
-    assert not fuse_pack(1, 14336) and not fuse_pack(2, 4096) and not fuse_pack(8, 256)
+    assert fuse_pack(1, 4096) and fuse_pack(1, 14336) and fuse_pack(2, 4096) and fuse_pack(2, 14336)
+    assert not fuse_pack(3, 4096) and not fuse_pack(4, 14336) and not fuse_pack(8, 256)
 
 
 def test_workload_config_names_the_step():
@@ -27,7 +27,7 @@ def test_workload_config_names_the_step():
     assert c["projections"] == ["qkv:q4k:6144x4096", "o:q4k:4096x4096", "gate_up:q4k:28672x4096",
                                 "down:q6k:4096x14336"]
     assert bench.workload_config(_args(batch=1))["launch"] == (
-        "pack fused into the mat-vec for qkv, o, gate_up; pack+mat-vec as two kernels for the rest")
+        "pack fused into the mat-vec (one kernel per projection)")
     assert bench.workload_config(_args(batch=1, fused=True))["launch"] == (
         "pack fused into the mat-vec (one kernel per projection)")
     assert bench.workload_config(_args(batch=1, unfused=True))["launch"] == "pack+mat-vec as two kernels"

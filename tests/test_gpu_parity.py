@@ -634,3 +634,88 @@ def test_random_small_shapes(fmtname, rows, K, batch, fused, seed):
     q.get_device_error()
     assert guard_intact(buf, batch, rows)
     check_against_oracle(fmtname, Wg, x, y.cpu().numpy())
+
+
+# ---- the scheduling workspace: the last tiles handed out by claims, the same bits -------------------
+WS_SHAPES = [("q4k", 4096, 4096, 1, False), ("q4k", 28672, 4096, 1, True), ("q6k", 4096, 14336, 1, True),
+             ("q6k", 333, 14336, 2, False), ("q5k", 1000, 2048, 2, True), ("q4k", 7, 256, 1, True),
+             ("q4k", 150, 8192, 2, False), ("q6k", 9, 65536, 1, False)]
+
+
+@pytest.mark.parametrize("fmtname,rows,K,batch,fused", WS_SHAPES)
+@pytest.mark.parametrize("per_mille", [-1, 0, 500, 1000], ids=["default", "none", "half", "all"])
+@pytest.mark.parametrize("warps", [0, 1, 3], ids=["plan", "w1", "w3"])
+def test_workspace_same_bits(fmtname, rows, K, batch, fused, per_mille, warps):
+    """qmd_qmatvec_ws / qmd_qmatvec_x_ws: bit-identical to the calls without a workspace and to the
+    same-order oracle, three calls in a row on one workspace, which each call leaves zeroed.  Claims
+    are used where every warp has two tiles of its own: the 28672-row shape on the default plan,
+    and most shapes once the plan is forced to one or three warps per CTA."""
+    seed = 7 * rows + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xd = dev(x)
+    if fmtname == "q6k":
+        W, Wa = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
+    else:
+        W, Wa = dev(Wg.reshape(rows, -1)), None
+    xq = q.q8k_pack(xd)
+    ref = q.qmatvec(QFMT[fmtname], W, Wa, xq, rows=rows)
+    ws = q.workspace(DEV)
+    q.debug_set_dynamic_tiles(per_mille)
+    q.debug_set_plan(warps, 0, 2 if warps else 0, 0)
+    try:
+        for _ in range(3):
+            buf, y = poisoned_y(batch, rows)
+            if fused:
+                q.qmatvec_x(QFMT[fmtname], W, Wa, xd, y, rows=rows, workspace=ws)
+            else:
+                q.qmatvec(QFMT[fmtname], W, Wa, xq, y, rows=rows, workspace=ws)
+            q.get_device_error()
+            assert guard_intact(buf, batch, rows)
+            assert torch.equal(y.view(torch.int32), ref.view(torch.int32))
+            assert int(ws.abs().sum()) == 0, "workspace not left zeroed"
+    finally:
+        q.debug_set_dynamic_tiles(-1)
+        q.debug_set_plan()
+    check_against_oracle(fmtname, Wg, x, ref.cpu().numpy(), f64_idx=_sample_rows(rows, min(rows, 200), seed))
+
+
+def test_workspace_streams_in_parallel():
+    """Two streams, each with its own workspace, chains of launches running at the same time: the
+    same bits as one stream, and both workspaces left zeroed."""
+    rows, K = 28672, 4096
+    Wg = synth.q4k_weights(44, rows, K)
+    W = dev(Wg.reshape(rows, -1))
+    xs = [dev(synth.activations(45 + i, 1, K)) for i in range(2)]
+    refs = [q.qmatvec_x(q.Q4_K, W, None, x, rows=rows) for x in xs]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    wss = [q.workspace(DEV) for _ in range(2)]
+    ys = [[torch.empty((1, rows), dtype=torch.float32, device=DEV) for _ in range(6)] for _ in range(2)]
+    torch.cuda.synchronize()
+    for k in range(6):
+        for i in range(2):
+            q.qmatvec_x(q.Q4_K, W, None, xs[i], ys[i][k], rows=rows, stream=streams[i], workspace=wss[i])
+    torch.cuda.synchronize()
+    q.get_device_error()
+    for i in range(2):
+        assert int(wss[i].abs().sum()) == 0
+        for k in range(6):
+            assert torch.equal(ys[i][k].view(torch.int32), refs[i].view(torch.int32))
+
+
+def test_workspace_refusals_write_nothing():
+    L = q.lib()
+    rows, K = 64, 1024
+    W = dev(synth.q4k_weights(1, rows, K).reshape(rows, -1))
+    xq = q.q8k_pack(dev(synth.activations(1, 1, K)))
+    buf, y = poisoned_y(1, rows)
+    ws = q.workspace(DEV)
+    assert L.qmd_qmatvec_ws(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, K, 1, None, None) == 1
+    assert L.qmd_qmatvec_ws(q.Q4_K, W.data_ptr(), None, xq.ptrs(), y.data_ptr(), rows, K, 1,
+                            ws.data_ptr() + 4, None) == 5
+    x = dev(synth.activations(1, 1, K))
+    none = q.Q8KPtrs(None, None, None)
+    assert L.qmd_qmatvec_x_ws(q.Q4_K, W.data_ptr(), None, x.data_ptr(), none, y.data_ptr(), rows, K, 1, None,
+                              None) == 1
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all() and guard_intact(buf, 1, rows) and int(ws.abs().sum()) == 0
