@@ -210,6 +210,31 @@ qmd_status qmd_qmatvec_x_ws(qmd_fmt fmt, const void *W, const void *W_aux, const
                             float *y, int64_t rows, int64_t K, int batch, void *workspace, void *stream);
 
 /*
+ * qmd_qmatvec_x_static -- qmd_qmatvec_x_ws without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: a plug-in whose host framework owns all device memory and hands
+ * it only its inputs and outputs, or code that must not allocate on its inference path.  The
+ * pages have no counterpart; this is a convenience of this library.
+ *
+ * The same results as qmd_qmatvec_x, bit for bit, scheduled as qmd_qmatvec_x_ws schedules them.
+ * The workspace is the library's own: one QMD_WORKSPACE_BYTES array in device memory, defined at
+ * file scope, which every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no allocating library routine); it clears that array with
+ * cudaMemsetAsync on `stream` and then launches the mat-vec.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *    with that device current) and keeps it; make that first call before any stream capture.
+ *  - Every call uses the same array, which keeps what the last call left: calls that may overlap
+ *    on the GPU (other streams, concurrent graphs) race on it and give wrong results.  Issue them
+ *    in one stream, or use qmd_qmatvec_x_ws with a workspace per stream.
+ *  - Size limit: the array is one workspace, which schedules every shape the call accepts (its
+ *    counters do not grow with the problem); shapes beyond qmd_qmatvec_x's limits are refused
+ *    with the same statuses, before anything is launched.
+ * Arguments, limits and errors as qmd_qmatvec_x; in addition DEVICE if the array's address cannot
+ * be found on the current device.
+ */
+qmd_status qmd_qmatvec_x_static(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                                float *y, int64_t rows, int64_t K, int batch, void *stream);
+
+/*
  * qmd_qmatvec_rmsnorm_x -- the residual add, the RMSNorm, the q8_K pack and the mat-vec in one
  * launch: y is exactly qmd_qmatvec(fmt, W, W_aux, qmd_rmsnorm_q8k_pack(x, r, g, eps), ...),
  * with the same bits -- the same h, the same sum-of-squares order, the same codes ("Language

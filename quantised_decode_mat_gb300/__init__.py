@@ -73,6 +73,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_qmatvec_x": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_qmatvec_ws": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp], i32),
             "qmd_qmatvec_x_ws": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp], i32),
+            "qmd_qmatvec_x_static": ([i32, vp, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp], i32),
             "qmd_qmatvec_rmsnorm_x": ([i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, Q8KPtrs, vp, i64, i64, i32, vp],
                                       i32),
             "qmd_q6k_prefix_stride": ([i64], i64),
@@ -209,6 +210,21 @@ def qmatvec_x(fmt: int, W, W_aux, x, y=None, rows: int | None = None, xq_out: Q8
     else:
         _check(lib().qmd_qmatvec_x_ws(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
                                       _ptr(workspace), _stream(stream)))
+    return y
+
+
+def qmatvec_x_static(fmt: int, W, W_aux, x, y=None, rows: int | None = None, xq_out: Q8K | None = None,
+                     stream=None):
+    """qmd_qmatvec_x_static: qmatvec_x scheduled through the library's own static workspace, for
+    callers that cannot allocate; calls that overlap on the GPU race on that workspace."""
+    import torch
+    rows = W.shape[0] if rows is None else rows
+    batch, K = x.shape
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    out = xq_out.ptrs() if xq_out is not None else Q8KPtrs(None, None, None)
+    _check(lib().qmd_qmatvec_x_static(fmt, _ptr(W), _ptr(W_aux), _ptr(x), out, _ptr(y), rows, K, batch,
+                                      _stream(stream)))
     return y
 
 

@@ -23,6 +23,12 @@ namespace qmd {
 // variable: the library never allocates.
 static __device__ unsigned int g_error_word;
 
+// The scheduling workspace of qmd_qmatvec_x_static: one QMD_WORKSPACE_BYTES workspace per device,
+// a file-scope device array that every device loading the library holds until the process ends.
+// Host code must not pass its name to a kernel (on the host it stands in for the array, it is not
+// a device address): the address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned int g_static_ws[QMD_WORKSPACE_BYTES / 4];
+
 static thread_local char g_detail[320];
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 static std::atomic<int> g_force_rg{0}, g_force_rows{0}, g_force_stages{0}, g_force_cps{0};
@@ -126,6 +132,30 @@ unsigned long long *trace_reserve(int ctas)
     return p;
 }
 #endif
+
+// Device address of g_static_ws on the current device, looked up on the first call there (with
+// that device current) and kept; NULL, with the reason recorded, if the lookup fails.
+static unsigned *static_workspace()
+{
+    static std::atomic<unsigned *> addr[64];
+    static std::mutex fill;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    if (addr[dev].load(std::memory_order_acquire) == nullptr) {
+        std::lock_guard<std::mutex> lock(fill);
+        if (addr[dev].load(std::memory_order_acquire) == nullptr) {
+            void *p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
+            if (e != cudaSuccess || p == nullptr) {
+                fail(QMD_ERR_DEVICE, "cudaGetSymbolAddress(static workspace)", e);
+                return nullptr;
+            }
+            addr[dev].store(static_cast<unsigned *>(p), std::memory_order_release);
+        }
+    }
+    return addr[dev].load(std::memory_order_acquire);
+}
 
 // Rows per row group per stage: 8 at one or two vectors, 4 at three or four, 2 above (16 (row,
 // vector) slots per warp from two vectors up; measured on the 7B shapes with the CTA counts
@@ -628,6 +658,50 @@ qmd_status qmd_qmatvec_x_ws(qmd_fmt fmt, const void *W, const void *W_aux, const
     const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
     return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream,
                           NormArgs(), workspace);
+}
+
+qmd_status qmd_qmatvec_x_static(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
+                                float *y, int64_t rows, int64_t K, int batch, void *stream)
+{
+    if (!x)
+        return QMD_ERR_NULL;
+    // The static array holds one workspace, and one workspace schedules every shape the call
+    // accepts (the counters do not grow with the problem); a larger need is refused.
+    static_assert(sizeof(g_static_ws) >= QMD_WORKSPACE_BYTES, "the static workspace holds one workspace");
+    DeviceInfo dev;
+    qmd_status st = current_device(&dev);
+    if (st != QMD_OK)
+        return st;
+    unsigned *ws = static_workspace();
+    if (!ws)
+        return QMD_ERR_DEVICE;
+    // The checks qmd_qmatvec_x makes, first, so that a refused call launches nothing (not even
+    // the clearing of the workspace).
+    const qmd_q8k_const unused = {nullptr, nullptr, nullptr};
+    if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
+        return QMD_ERR_FORMAT;
+    const bool q6 = fmt == QMD_Q6_K_SPLIT;
+    const bool want_out = xq_out.qs || xq_out.d || xq_out.bsums;
+    if (!W || !y || (q6 && !W_aux) || (want_out && (!xq_out.qs || !xq_out.d || !xq_out.bsums)))
+        return QMD_ERR_NULL;
+    if ((st = check_k(K)) != QMD_OK)
+        return st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return QMD_ERR_BATCH;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return QMD_ERR_SHAPE;
+    if (!aligned(W, 16) || (q6 && !aligned(W_aux, 16)) || !aligned(y, 4) || !aligned(x, 16) ||
+        (want_out && (!aligned(xq_out.qs, 16) || !aligned(xq_out.bsums, 16) || !aligned(xq_out.d, 4))))
+        return QMD_ERR_MISALIGNED;
+    QmvPlan plan;
+    if ((st = qmv_plan(fmt, rows, (int)(K / QMD_QK), batch, dev, &plan, QMV_PACK)) != QMD_OK)
+        return st;
+    // Every call starts from a cleared workspace: the array keeps whatever the last call left.
+    const cudaError_t e = cudaMemsetAsync(ws, 0, QMD_WORKSPACE_BYTES, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(QMD_ERR_LAUNCH, "clear the static workspace", e);
+    return qmatvec_common(fmt, W, W_aux, unused, y, rows, K, batch, nullptr, nullptr, false, x, xq_out, stream,
+                          NormArgs(), ws);
 }
 
 qmd_status qmd_qmatvec_rmsnorm_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, const float *r,

@@ -60,7 +60,7 @@ def test_launch_forms_are_the_benched_ones(step):
     for p in step.projs:
         assert p.fused == fuse_pack(step.batch, p.K)
     if step.batch == 1:
-        assert [p.fused for p in step.projs[:4]] == [True, True, True, False]
+        assert [p.fused for p in step.projs[:4]] == [True, True, True, True]
 
 
 @pytest.mark.parametrize("index", range(8), ids=[f"L{i // 4}-{n}" for i, n in
