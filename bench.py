@@ -5,11 +5,11 @@
 A step is one pass of the whole hot path over one batch of synthetic input: for each of 32
 layers and each projection {q|k|v Q4_K 6144x4096, o Q4_K 4096x4096, gate|up Q4_K 28672x4096,
 down Q6_K 4096x14336}, the q8_K pack of that projection's activation and the mat-vec of its
-weight.  By default a batch of one vector runs one launch per projection of 4096-wide rows
-(qmd_qmatvec_x, which packs inside the kernel) and qmd_q8k_pack followed by qmd_qmatvec for
-the 14336-wide down projection and for larger batches (every CTA of a fused launch packs the
-whole input for itself, which costs more than the extra launch once the input is long or holds
-two or more vectors); --fused and --unfused force one form everywhere.  Each launch depends on the
+weight.  By default one or two vectors run one launch per projection (qmd_qmatvec_x_ws, which
+packs inside the kernel and hands the last rows of deep launches to warps as they free up) and
+larger batches qmd_q8k_pack followed by qmd_qmatvec_ws (every CTA of a fused launch packs the
+whole input for itself, which costs more than the extra launch once the input holds three or
+more vectors); --fused and --unfused force one form everywhere.  Each launch depends on the
 previous one in stream order, as in a real decode where a projection's input comes from the
 layer before.  The step's launches are captured once into a CUDA graph and replayed.  Weights
 (4.41 GB) exceed L2 many times over, so consecutive steps read them from HBM.
@@ -19,9 +19,10 @@ f32 outputs written, once per step (4.419 GB at batch 1).
 
 Printed (rank 0, one JSON line): the step's algorithmic bytes / time as GB/s (value), the
 same through host buffers (e2e: inputs copied in and outputs copied out every step), the
-dominant kernel's roofline, the oracle's throughput on the host cores (cpu_baseline), SM
-clocks sampled during the timed region, launch counts, and (configs) each of configs 0-3 as
-a single mat-vec on packed input, timed apart from the step.
+dominant kernel's roofline against the measured copy peak and the measured read-only ceiling,
+the oracle's throughput on the host cores (cpu_baseline), SM clocks sampled during the timed
+region, launch counts, (steps) the same step at batches 2, 4 and 8 over the same weights, and
+(configs) each of configs 0-3 as a single mat-vec on packed input, timed apart from the step.
 
 --impl reference times the CPU oracle on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs an independent replica of the step (replicas only; the
@@ -47,9 +48,10 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
-KERNEL_SOURCES = ["quantised_decode_mat_gb300/csrc/qmv.cuh", "quantised_decode_mat_gb300/csrc/qmv_q4k.cu",
-                  "quantised_decode_mat_gb300/csrc/qmv_q6k.cu", "quantised_decode_mat_gb300/csrc/ptx.cuh",
-                  "quantised_decode_mat_gb300/csrc/pack.cu", "quantised_decode_mat_gb300/csrc/q8k.cuh",]
+KERNEL_SOURCES = ["quantised_decode_mat_gb300/csrc/qmv.cuh", "quantised_decode_mat_gb300/csrc/qmv_rl.cuh",
+                  "quantised_decode_mat_gb300/csrc/qmv_q4k.cu", "quantised_decode_mat_gb300/csrc/qmv_q6k.cu",
+                  "quantised_decode_mat_gb300/csrc/ptx.cuh", "quantised_decode_mat_gb300/csrc/pack.cu",
+                  "quantised_decode_mat_gb300/csrc/q8k.cuh"]
 
 
 def kernel_source_hash() -> str:
@@ -175,13 +177,13 @@ def alu_roofline(q, step, batch: int, ms_per_launch: float, dp4a_rate: float, mm
     q4 = [p for p in step.projs if p.fmt == q.Q4_K]
     block_rows = sum(p.rows * (p.K // 256) for p in q4) / len(q4)
     info = q.launch_info(q.Q4_K, q4[0].rows, q4[0].K, batch)
-    tc = batch >= 5 and info["rows_per_stage"] == 16
+    tc = batch >= 3 and info["rows_per_stage"] == 16
     if tc:
         ops, peak, unit, op = block_rows * 4096.0, mma_rate, "TFLOP/s", "mma.sync.m16n8k16 f16->f32"
     else:
         ops, peak, unit, op = block_rows * 64.0 * batch, dp4a_rate, "Tdp4a/s", "dp4a"
     achieved = ops / (ms_per_launch * 1e-3)
-    return {"bound": "alu", "kernel": "qmv_tc_kernel" if tc else "qmv_kernel", "op": op,
+    return {"bound": "alu", "kernel": kernel_name(info, batch), "op": op,
             "achieved": achieved / 1e12, "peak": peak / 1e12, "unit": unit, "frac": achieved / peak,
             "ops_per_launch": ops, "peak_kind": "measured (qmd_measure_alu, register-only kernels)"}
 
@@ -340,7 +342,14 @@ def time_graph(torch, g, reps: int, stream) -> float:
     return e0.elapsed_time(e1) / reps
 
 
-def time_configs(torch, q, device, peak: float) -> dict:
+def kernel_name(info: dict, batch: int) -> str:
+    """The mat-vec kernel a launch plan (qmd_qmatvec_launch_info) runs."""
+    if info["rows_per_stage"] == 4:
+        return "qmv_rl_kernel"
+    return "qmv_tc_kernel" if info["rows_per_stage"] == 16 and batch >= 3 else "qmv_kernel"
+
+
+def time_configs(torch, q, device, peak: float, peak_kind: str = "measured") -> dict:
     """Configs 0-3 as single mat-vecs on packed input (the batches each config names): a
     CUDA-graph chain of launches rotating over seeded weight copies that together exceed 3 x L2,
     so every launch reads its weights from HBM.  Bytes per launch as the workload tables count
@@ -362,6 +371,7 @@ def time_configs(torch, q, device, peak: float) -> dict:
         ncopy = min(2000, max(2, -(-3 * l2 // wbytes)))
         copies = [(W.clone(), None if Wa is None else Wa.clone()) for _ in range(ncopy)]
         del g, W, Wa
+        ws = q.workspace(device)  # every launch of a chain is ordered in one stream: one workspace
         for B in c["batches"]:
             xq = q.q8k_pack(torch.from_numpy(synth.activations(c["seed"], B, K)).to(device))
             y = torch.empty((B, rows), dtype=torch.float32, device=device)
@@ -369,12 +379,12 @@ def time_configs(torch, q, device, peak: float) -> dict:
             s.wait_stream(torch.cuda.current_stream(device))
             with torch.cuda.stream(s):
                 for (Wc, Ac) in copies:  # first launches set kernel attributes outside capture
-                    q.qmatvec(f, Wc, Ac, xq, y, rows, s)
+                    q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
             torch.cuda.synchronize(device)
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=s):
                 for (Wc, Ac) in copies:
-                    q.qmatvec(f, Wc, Ac, xq, y, rows, s)
+                    q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
             for _ in range(3):
                 gr.replay()
             ms = time_graph(torch, gr, 10, torch.cuda.current_stream(device)) / ncopy  # replays go there
@@ -383,13 +393,40 @@ def time_configs(torch, q, device, peak: float) -> dict:
             info = q.launch_info(f, rows, K, B)
             out[f"config{cid}_b{B}"] = {
                 "shape": f"{fmt} {rows}x{K} batch {B}", "us_per_launch": ms * 1e3, "gbs": gbs,
-                "frac_of_peak": gbs / peak, "bytes_per_launch": alg, "weight_copies_rotated": ncopy,
-                "kernel": ("qmv_tc_kernel" if info["rows_per_stage"] == 16 and B >= 5 else "qmv_kernel"),
+                "frac_of_peak": gbs / peak, "peak_kind": peak_kind, "frac_of_nominal_8TBps": gbs / NOMINAL_HBM_GBS,
+                "bytes_per_launch": alg, "weight_copies_rotated": ncopy, "kernel": kernel_name(info, B),
                 "grid": info["grid"], "threads": info["threads"]}
             del gr
         del copies
         torch.cuda.empty_cache()
     q.get_device_error()
+    return out
+
+
+def time_step_at(torch, q, step, batch: int, steps: int, warmup: int, stream, peak: float) -> dict:
+    """The decode step over the same weights at another batch: its own graph, timed like the
+    headline step, plus its Q4_K mat-vecs as a chain (the roofline kernel at that batch)."""
+    st = step.with_batch(batch)
+    g = st.capture()
+    for _ in range(warmup):
+        g.replay()
+    ms = time_graph(torch, g, steps, stream)
+    nq4 = sum(1 for p in st.projs if p.fmt == q.Q4_K)
+    g4 = st.capture(lambda: st.run_matvecs(q.Q4_K))
+    g4.replay()
+    ms4 = time_graph(torch, g4, max(3, steps), stream) / nq4
+    per = lambda p: p.algorithmic_bytes() if p.fused else p.matvec_bytes()
+    b4 = sum(per(p) for p in st.projs if p.fmt == q.Q4_K) / nq4
+    nb = st.bytes()
+    q.get_device_error()
+    info = q.launch_info(q.Q4_K, st.projs[0].rows, st.projs[0].K, batch)
+    out = {"value": nb["algorithmic"] / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+           "frac_of_peak": nb["algorithmic"] / (ms * 1e-3) / 1e9 / peak,
+           "row_vectors_per_s": sum(p.rows for p in st.projs) * batch / (ms * 1e-3),
+           "launch": "pack fused into the mat-vec" if all(p.fused for p in st.projs) else "pack+mat-vec",
+           "q4k_kernel": kernel_name(info, batch), "q4k_us_per_launch": ms4 * 1e3,
+           "q4k_roofline_frac": b4 / (ms4 * 1e-3) / 1e9 / peak}
+    del g, g4, st
     return out
 
 
@@ -499,6 +536,12 @@ def run_ours(args):
 
     peak, peak_kind = measured_peak()
     gbs = world * nbytes["algorithmic"] / (ms_max * 1e-3) / 1e9
+    # the read-only ceiling: bulk-copy streaming of a buffer 16 x the L2, measured here
+    rbuf = torch.empty(16 * torch.cuda.get_device_properties(local_rank).L2_cache_size // 16 * 16,
+                       dtype=torch.uint8, device=stream.device)
+    read_gbs = q.measure_read_bw(rbuf) / 1e9
+    del rbuf
+    q.get_device_error()
     rows_per_step = sum(p.rows for p in step.projs)
     ach4 = b4 / (ms4 * 1e-3) / 1e9
     line = {
@@ -506,7 +549,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 dot / f32 epilogue", "data": "synthetic",
         "config": workload_config(args),
-        "pct_of_peak": {"of_" + peak_kind: gbs / world / peak, "of_nominal_8TBps": gbs / world / NOMINAL_HBM_GBS},
+        "pct_of_peak": {"of_" + peak_kind: gbs / world / peak, "of_nominal_8TBps": gbs / world / NOMINAL_HBM_GBS,
+                        "of_read_ceiling": gbs / world / read_gbs},
+        "read_ceiling": {"value": read_gbs, "unit": "GB/s",
+                         "how": "qmd_measure_read_bw: one CTA per SM streams a buffer of 16 x L2 into shared "
+                                "memory with 1-D bulk copies and discards it; 5 passes after a warm-up"},
         "rows_per_s": world * rows_per_step / (ms_max * 1e-3),
         "row_vectors_per_s": world * rows_per_step * args.batch / (ms_max * 1e-3),
         "bytes_per_step": nbytes,
@@ -515,10 +562,12 @@ def run_ours(args):
                          "matvec_only": world * nbytes["matvec"] / (ms_max * 1e-3) / 1e9,
                          "pack_inclusive": world * (nbytes["matvec"] + nbytes["pack"]) / (ms_max * 1e-3) / 1e9},
         "roofline": {"bound": "hbm",
-                     "kernel": "%s<Q4_K, batch %d, %s>" % ("qmv_tc_kernel" if args.batch >= 5 else "qmv_kernel", args.batch,
+                     "kernel": "%s<Q4_K, batch %d, %s>" % (kernel_name(q.launch_info(q.Q4_K, 4096, 4096, args.batch),
+                                                                       args.batch), args.batch,
                                                             "fused pack" if q4_fused else "packed input"),
                      "achieved": ach4, "peak": peak,
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,
+                     "frac_of_read_ceiling": ach4 / read_gbs, "frac_of_nominal_8TBps": ach4 / NOMINAL_HBM_GBS,
                      # the committed capture is of the batch-1 fused-pack launches only
                      "traffic": profiled_traffic("qmv_q4k") if args.batch == 1 and q4_fused else None,
                      "algorithmic_bytes_per_launch": b4, "ms_per_launch": ms4},
@@ -546,8 +595,12 @@ def run_ours(args):
         "gpu_launches": step.launches * args.steps,
     }
     del g, g4, g6, gp, ge, gr, gn1, gn2
+    if rank == 0 and not args.no_batches:
+        # the same step at the other batches the workload names (4) and the batched range's ends
+        line["steps"] = {f"batch{b}": time_step_at(torch, q, step, b, min(args.steps, 20), 3, stream, peak)
+                         for b in (2, 4, 8) if b != args.batch}
     if rank == 0 and not args.no_configs:
-        line["configs"] = time_configs(torch, q, torch.device(f"cuda:{local_rank}"), peak)
+        line["configs"] = time_configs(torch, q, torch.device(f"cuda:{local_rank}"), peak, peak_kind)
     if rank == 0 and args.cpu_layers > 0:
         import oracle
         oracle.build()
@@ -585,6 +638,8 @@ def main(argv=None):
                          "captures, which must stay small)")
     ap.add_argument("--no-workspace", action="store_true",
                     help="run the mat-vecs without a scheduling workspace (every row split evenly over the SMs)")
+    ap.add_argument("--no-batches", action="store_true",
+                    help="skip the step at batches 2, 4 and 8 reported beside the headline (steps)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config mat-vec timings (configs 0-3) reported beside the step")
     ap.add_argument("--cpu-layers", type=int, default=8,

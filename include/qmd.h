@@ -164,7 +164,9 @@ qmd_status qmd_rmsnorm_q8k_pack(const float *x, const float *r, const float *g, 
  * rows go to the tensor-core kernel, which takes them run by run when its per-run row sums
  * (32 x (ceil(K / 4096) - 1) bytes for each row a multiprocessor handles) fit in shared memory
  * (K = 32768: about 50,000 rows); QMD_ERR_SHAPE otherwise.
- * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, DEVICE, LAUNCH.
+ * y must not overlap the packed input (other CTAs may still read it while one writes y).
+ * Errors: NULL, FORMAT, K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, SHAPE, VALUE (overlap), DEVICE,
+ * LAUNCH.
  * Device-side bounded waits that give up, and a CTA that finds its launch geometry does not match
  * its plan (it then returns without touching memory), set a flag read by qmd_get_device_error.
  */
@@ -183,18 +185,19 @@ qmd_status qmd_qmatvec(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k_co
  *           qmd_q8k_pack writes; all three NULL writes nothing.
  * Other arguments, limits and errors as qmd_qmatvec; in addition the batch's packed codes
  * (batch x K bytes) must fit in shared memory beside the weight stages (QMD_ERR_SHAPE
- * otherwise; every K <= 16384 at batch <= 4 and K <= 32768 at batch 1 fit).
+ * otherwise; every K <= 16384 at batch <= 4 and K <= 32768 at batch 1 fit), and neither y nor
+ * xq_out may overlap x (every CTA reads x while others write): QMD_ERR_VALUE.
  */
 qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const float *x, qmd_q8k xq_out,
                          float *y, int64_t rows, int64_t K, int batch, void *stream);
 
 /*
  * qmd_qmatvec_ws, qmd_qmatvec_x_ws -- qmd_qmatvec and qmd_qmatvec_x with a scheduling workspace:
- * the same results, bit for bit.  With one or two vectors (the row-lane kernel) the first three
- * quarters of the rows are split evenly over the multiprocessors as usual, and the last quarter
- * is handed to warps four rows at a time, in the order they ask for more work, so that a
- * multiprocessor that runs slow does not set the end of the launch.  Other plans (three or more
- * vectors) ignore the workspace.  This is a scheduling choice of this implementation; the pages
+ * the same results, bit for bit.  With one vector and enough rows that every warp of the
+ * row-lane kernel has two 4-row tiles of its own (e.g. 28672 rows), the first three quarters of
+ * the rows are split evenly over the multiprocessors as usual, and the last quarter is handed to
+ * warps four rows at a time, in the order they ask for more work, so that a multiprocessor that
+ * runs slow does not set the end of the launch.  Other launches ignore the workspace.  This is a scheduling choice of this implementation; the pages
  * have no counterpart.
  *   workspace  device, QMD_WORKSPACE_BYTES bytes, 16-byte aligned, owned by the caller.  Zero it
  *              once; every call that completes leaves it zeroed again.  Calls ordered in one stream
@@ -245,7 +248,7 @@ qmd_status qmd_qmatvec_x_static(qmd_fmt fmt, const void *W, const void *W_aux, c
  *   x, r, g, eps  as qmd_rmsnorm_q8k_pack (r may be NULL)
  *   h_out   f32 [batch][K], 16-byte aligned, receives h (written by one CTA); or NULL.  Unlike
  *           qmd_rmsnorm_q8k_pack it must NOT overlap x, r or g, since every CTA still reads x
- *           and r while it is written (QMD_ERR_VALUE).
+ *           and r while it is written (QMD_ERR_VALUE); nor may y or xq_out overlap x or r.
  *   xq_out  optional, as qmd_qmatvec_x: the packed codes of the normalised vector
  * Other arguments as qmd_qmatvec.  Limits: the dp4a kernel's (every K up to 32768 at batch
  * <= 2 and 16384 above) with the packed codes in shared memory, as qmd_qmatvec_x; longer rows
@@ -360,6 +363,18 @@ qmd_status qmd_debug_qmatvec_dump(qmd_fmt fmt, const void *W, const void *W_aux,
  * on a private stream; the call waits for them.  Errors: NULL (either pointer), DEVICE, LAUNCH.
  */
 qmd_status qmd_measure_alu(double *dp4a_per_s, double *mma_flop_per_s);
+
+/*
+ * qmd_measure_read_bw -- this device's read-only streaming rate, the ceiling for a kernel that
+ * only reads its large operand: one CTA per multiprocessor streams its share of `buf` into shared
+ * memory by 1-D bulk asynchronous copies (the path the mat-vecs read weights by) and discards it,
+ * five times after a warm-up; bytes_per_s = 5 x bytes / elapsed.  `buf` is the caller's (device,
+ * 16-byte aligned, bytes a multiple of 16 and at least 12288; make it several times the L2 so
+ * that the reads come from HBM); only its contents' placement matters.  The call creates and
+ * destroys a stream and two events and waits for its kernels.  Errors: NULL, MISALIGNED, SHAPE,
+ * DEVICE, LAUNCH; a bounded wait that gives up sets the device error word.
+ */
+qmd_status qmd_measure_read_bw(const void *buf, size_t bytes, double *bytes_per_s);
 
 /*
  * qmd_debug_wait_timeout -- launches one CTA that waits, with the given limit, on a

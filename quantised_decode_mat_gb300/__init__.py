@@ -89,6 +89,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_debug_qmatvec_dump": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp, vp], i32),
             "qmd_debug_wait_timeout": ([u64, vp], i32),
             "qmd_measure_alu": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], i32),
+            "qmd_measure_read_bw": ([vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_double)], i32),
             "qmd_debug_set_plan": ([i32, i32, i32, i32], None),
             "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
             "qmd_debug_set_dynamic_tiles": ([i32], None),
@@ -317,6 +318,14 @@ def measure_alu() -> tuple[float, float]:
     d, m = ctypes.c_double(), ctypes.c_double()
     _check(lib().qmd_measure_alu(ctypes.byref(d), ctypes.byref(m)))
     return d.value, m.value
+
+
+def measure_read_bw(buf) -> float:
+    """qmd_measure_read_bw: bytes/s of read-only bulk streaming of `buf` (a CUDA tensor whose
+    byte size is a multiple of 16; make it several times the L2)."""
+    r = ctypes.c_double()
+    _check(lib().qmd_measure_read_bw(_ptr(buf), buf.numel() * buf.element_size(), ctypes.byref(r)))
+    return r.value
 
 
 def debug_wait_timeout(limit_ns: int, stream=None) -> None:

@@ -37,6 +37,55 @@ def _nvcc() -> str:
     return os.path.realpath(found)
 
 
+# The spill gate: ptxas reports, per kernel instance, the bytes it spills to local memory; a
+# spill in a product instance fails the build.  The one exemption is the test-only recording
+# variant (mode 1 of the mat-vec kernels: qmd_debug_qmatvec_dump), which stores every integer
+# dot it computes and is never on a timed path.  Template argument (0-based) that holds the mode:
+_MODE_ARG = {"qmv_kernel": 3, "qmv_tc_kernel": 1, "qmv_rl_kernel": 2}
+_RECORDING_MODE = 1
+
+
+def spills(log_text: str) -> list[tuple[str, int, int]]:
+    """(mangled kernel name, spill store bytes, spill load bytes) for every entry function of a
+    ptxas -v log that spills."""
+    import re
+    out, cur = [], None
+    for line in log_text.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            cur = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and cur and (int(m.group(1)) or int(m.group(2))):
+            out.append((cur, int(m.group(1)), int(m.group(2))))
+    return out
+
+
+def spill_exempt(mangled: str) -> bool:
+    """True for the recording variant of a mat-vec kernel, read from the mangled template
+    arguments (Itanium ABI: L<i|b><value>E in order)."""
+    import re
+    for kern, pos in _MODE_ARG.items():
+        m = re.search(r"\d+" + kern + r"I((?:L[ib]\d+E)+)E", mangled)
+        if m:
+            args = [int(v) for v in re.findall(r"L[ib](\d+)E", m.group(1))]
+            return len(args) > pos and args[pos] == _RECORDING_MODE
+    return False
+
+
+def check_spills(build_dir: str) -> None:
+    """Raise if any product kernel instance in the build's ptxas logs spills."""
+    bad = []
+    for u in UNITS:
+        path = os.path.join(build_dir, u + ".log")
+        if os.path.exists(path):
+            with open(path) as f:
+                bad += [(u,) + s for s in spills(f.read()) if not spill_exempt(s[0])]
+    if bad:
+        raise RuntimeError("register spills in product kernel instances: " +
+                           "; ".join(f"{u}: {k} ({st} B stored, {ld} B loaded)" for u, k, st, ld in bad))
+
+
 def _sources_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(HERE, "..", "include", "qmd.h"))
@@ -67,6 +116,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
         for u in failed:
             sys.stderr.write(open(os.path.join(build_dir, u + ".log")).read())
         raise RuntimeError(f"nvcc failed for {failed}")
+    check_spills(build_dir)
     tmp = lib_path + f".tmp{os.getpid()}"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
     subprocess.run([nvcc, "-shared", "--cudart", "shared", *ARCH, "-o", tmp]

@@ -498,6 +498,25 @@ inline bool overlaps(const void *a, size_t na, const void *b, size_t nb)
     return a && b && pa < pb + nb && pb < pa + na;
 }
 
+// Outputs a mat-vec writes while other CTAs may still read its inputs must not share bytes with
+// them: y (every form) and the fused forms' packed copy xq_out against x, r and the packed input.
+qmd_status outputs_apart(const float *y, int64_t rows, int batch, int64_t K, const float *x, const float *r,
+                         qmd_q8k_const xq, qmd_q8k xq_out)
+{
+    const size_t nb = (size_t)(K / QMD_QK);
+    const size_t yb = (size_t)batch * (size_t)rows * 4, vb = (size_t)batch * (size_t)K * 4;
+    const size_t qsb = (size_t)batch * (size_t)K, db = (size_t)batch * nb * 4, bsb = (size_t)batch * nb * 16;
+    const void *outs[4] = {y, xq_out.qs, xq_out.d, xq_out.bsums};
+    const size_t outb[4] = {yb, qsb, db, bsb};
+    const void *ins[5] = {x, r, xq.qs, xq.d, xq.bsums};
+    const size_t inb[5] = {vb, vb, qsb, db, bsb};
+    for (int o = 0; o < 4; ++o)
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i]))
+                return QMD_ERR_VALUE;
+    return QMD_OK;
+}
+
 // The RMSNorm form's extra arguments; g == NULL selects the other forms.
 struct NormArgs {
     const float *r = nullptr;
@@ -547,6 +566,9 @@ qmd_status qmatvec_common(qmd_fmt fmt, const void *W, const void *W_aux, qmd_q8k
             overlaps(na.h_out, vb, na.g, (size_t)K * sizeof(float)))
             return QMD_ERR_VALUE;
     }
+    if ((st = outputs_apart(y, rows, batch, K, x, na.r, xq, fused ? xq_out : qmd_q8k{nullptr, nullptr, nullptr})) !=
+        QMD_OK)
+        return st;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != QMD_OK)
         return st;
@@ -693,6 +715,8 @@ qmd_status qmd_qmatvec_x_static(qmd_fmt fmt, const void *W, const void *W_aux, c
     if (!aligned(W, 16) || (q6 && !aligned(W_aux, 16)) || !aligned(y, 4) || !aligned(x, 16) ||
         (want_out && (!aligned(xq_out.qs, 16) || !aligned(xq_out.bsums, 16) || !aligned(xq_out.d, 4))))
         return QMD_ERR_MISALIGNED;
+    if ((st = outputs_apart(y, rows, batch, K, x, nullptr, unused, xq_out)) != QMD_OK)
+        return st;
     QmvPlan plan;
     if ((st = qmv_plan(fmt, rows, (int)(K / QMD_QK), batch, dev, &plan, QMV_PACK)) != QMD_OK)
         return st;

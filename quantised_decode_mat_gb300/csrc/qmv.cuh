@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(qmv_max_threads(B, PR, MODE), 1) qmv_kernel(co
     // A launch whose plan does not fit the kernel: the RMSNorm form's sum of squares takes 256
     // threads, and the layout must lie inside the dynamic shared memory the launch was given.
     if ((NORM && NWT < 8) || (uint32_t)L.total > dynamic_smem_bytes()) {
+        pdl_wait();  // so that a kernel launched after this one still finds its predecessor done
         if (tid == 0)
             atomicOr(p.err, ERRBIT_PLAN);
         return;
@@ -905,12 +906,13 @@ inline qmd_status make_params(const QmvArgs &a, const QmvPlan &plan, QmvKParams 
     kp.eps = a.eps;
     kp.err = device_error_word();
     kp.wait_ns = wait_limit_ns();
-    // Only the row-lane kernel schedules through the workspace, and only where each warp has at
-    // least two tiles of its own: a claimed tile costs a round trip to the counter, which pays
-    // back only by evening out warps that run several tiles in sequence (measured on the 7B
-    // shapes: gate|up 13.5 -> 12.6 us; q|k|v, o and down, one tile per warp, slower).
+    // Only the row-lane kernel schedules through the workspace, only for one vector and only
+    // where each warp has at least two tiles of its own: a claimed tile costs a round trip to the
+    // counter, which pays back only by evening out warps that run several tiles in sequence
+    // (measured on the 7B shapes at one vector: gate|up 13.5 -> 12.6 us; q|k|v, o and down, one
+    // tile per warp, slower; at two vectors the 8-layer step took 41.9 against 39.4 us a layer).
     const int64_t tiles = (a.rows + 3) / 4;
-    const bool deep = plan.layout == 2 && tiles >= 2 * (int64_t)plan.WR * plan.grid;
+    const bool deep = plan.layout == 2 && a.batch == 1 && tiles >= 2 * (int64_t)plan.WR * plan.grid;
     kp.ws = deep ? a.ws : nullptr;
     kp.pre_steps = plan.pre_steps;
     kp.dyn_tiles = kp.ws ? dynamic_tiles(tiles) : 0;

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
     float *s_run = reinterpret_cast<float *>(smem + L.run_off);
     const uint64_t pol = policy_evict_first();
     if (runs > 1 && nt * TC_ROWS > p.tc_rows) {  // more rows than the run-sum buffer was sized for
+        pdl_wait();  // so that a kernel launched after this one still finds its predecessor done
         if (tid == 0)
             atomicOr(p.err, ERRBIT_PLAN);
         return;

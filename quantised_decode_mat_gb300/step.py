@@ -173,6 +173,33 @@ class DecodeStep:
         cur.wait_stream(h2d)
         cur.wait_stream(d2h)
 
+    def with_batch(self, batch: int, fused: bool | None = None, workspace: bool = True) -> "DecodeStep":
+        """The same step (the same weight tensors, shared) for `batch` activation vectors: new
+        activations from the same seeds, new outputs and packed buffers, the launch forms
+        fuse_pack picks for that batch (or `fused`), and its own scheduling workspace."""
+        import torch
+        from . import workspace as new_workspace
+        dev = self.x_all.device
+        names = [n for (n, _, _, _) in synth.STEP_PROJECTIONS]
+        st = DecodeStep(batch=batch)
+        st.ws = new_workspace(dev) if workspace else None
+        st.x_all = torch.empty(sum(batch * p.K for p in self.projs), dtype=torch.float32, device=dev)
+        st.y_all = torch.empty(sum((batch * p.rows + 3) // 4 * 4 for p in self.projs), dtype=torch.float32,
+                               device=dev)
+        xo = yo = 0
+        for p in self.projs:
+            x = st.x_all[xo: xo + batch * p.K].view(batch, p.K)
+            x.copy_(torch.from_numpy(synth.activations(synth.step_seed(p.layer), batch, p.K, p.layer,
+                                                       names.index(p.name))))
+            xo += batch * p.K
+            y = st.y_all[yo: yo + batch * p.rows].view(batch, p.rows)
+            yo += (batch * p.rows + 3) // 4 * 4
+            st.projs.append(Projection(p.name, p.layer, p.fmt, p.rows, p.K, p.W, p.W_aux, x,
+                                       Q8K.empty(batch, p.K, dev), y, p.weight_bytes,
+                                       fuse_pack(batch, p.K) if fused is None else bool(fused)))
+        torch.cuda.synchronize(dev)
+        return st
+
     def run_packs(self, stream=None) -> int:
         for p in self.projs:
             q8k_pack(p.x, p.xq, stream)

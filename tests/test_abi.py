@@ -63,13 +63,14 @@ def test_prefix_stride_and_split_bytes(L):
 
 
 A = 0x10000  # aligned fake device addresses: validation must fail before any of them is used
+YA = A + (1 << 24)  # an output buffer that overlaps none of the inputs
 
 
 def _xq(qs=A, d=A, bs=A):
     return q.Q8KPtrs(qs, d, bs)
 
 
-def st_qmatvec(L, fmt=q.Q4_K, W=A, Wa=A, xq=None, y=A, rows=16, K=512, batch=1):
+def st_qmatvec(L, fmt=q.Q4_K, W=A, Wa=A, xq=None, y=YA, rows=16, K=512, batch=1):
     return L.qmd_qmatvec(fmt, W, Wa, xq or _xq(), y, rows, K, batch, None)
 
 
@@ -93,7 +94,9 @@ def st_qmatvec(L, fmt=q.Q4_K, W=A, Wa=A, xq=None, y=A, rows=16, K=512, batch=1):
     (dict(xq=_xq(qs=A + 4)), 5),
     (dict(xq=_xq(bs=A + 2)), 5),
     (dict(xq=_xq(d=A + 2)), 5),
-    (dict(y=A + 2), 5),
+    (dict(y=YA + 2), 5),
+    # y is written while other CTAs still read the packed input: no overlap allowed
+    (dict(y=A), 10), (dict(y=A + 496), 10), (dict(y=A - 16 * 4 + 4), 10),
 ])
 def test_qmatvec_refusals(L, kw, status):
     assert st_qmatvec(L, **kw) == status
@@ -200,8 +203,22 @@ def test_fused_entry_point_reaches_the_device_check(L):
     if torch.cuda.is_available():
         pytest.skip("GPU present")
     none = q.Q8KPtrs(None, None, None)
-    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, A, 16, 512, 1, None) == 9
-    assert L.qmd_qmatvec_x(q.Q5_K, A, None, A, none, A, 16, 512, 8, None) == 9
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, YA, 16, 512, 1, None) == 9
+    assert L.qmd_qmatvec_x(q.Q5_K, A, None, A, none, YA, 16, 512, 8, None) == 9
+    assert L.qmd_qmatvec(q.Q4_K, A, None, _xq(), A + 512, 16, 512, 1, None) == 9  # adjacent, not overlapping
+
+
+def test_fused_outputs_must_not_overlap_the_input(L):
+    """Every CTA of a fused launch reads x while others write y (and CTA 0 the packed copy), so
+    an overlap is refused before anything is launched, with or without a workspace."""
+    none = q.Q8KPtrs(None, None, None)
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, A, 16, 512, 1, None) == 10
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, none, A + 2048 - 4, 16, 512, 1, None) == 10
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, q.Q8KPtrs(A + 1024, YA + 4096, YA + 8192), YA, 16, 512, 1,
+                           None) == 10
+    assert L.qmd_qmatvec_x(q.Q4_K, A, None, A, q.Q8KPtrs(YA + 4096, A, YA + 8192), YA, 16, 512, 1, None) == 10
+    assert L.qmd_qmatvec_x_ws(q.Q4_K, A, None, A, none, A, 16, 512, 1, YA + 65536, None) == 10
+    assert L.qmd_qmatvec_ws(q.Q4_K, A, None, _xq(), A, 16, 512, 1, YA + 65536, None) == 10
 
 
 def test_measure_alu_refuses_null_pointers(L):
@@ -211,7 +228,7 @@ def test_measure_alu_refuses_null_pointers(L):
     assert L.qmd_measure_alu(ctypes.byref(d), None) == 1
 
 
-def st_norm_mv(L, fmt=q.Q4_K, W=A, Wa=None, x=A, r=None, g=A, eps=1e-6, h=None, xq=None, y=A, rows=16, K=512,
+def st_norm_mv(L, fmt=q.Q4_K, W=A, Wa=None, x=A, r=None, g=A, eps=1e-6, h=None, xq=None, y=YA, rows=16, K=512,
                batch=2):
     return L.qmd_qmatvec_rmsnorm_x(fmt, W, Wa, x, r, g, ctypes.c_float(eps), h, xq or q.Q8KPtrs(None, None, None),
                                    y, rows, K, batch, None)
@@ -228,6 +245,8 @@ FAR = A + (1 << 20)  # a buffer that overlaps none of the others (2 x 512 f32 = 
     (dict(eps=-1e-3), 10), (dict(eps=float("nan")), 10), (dict(eps=float("inf")), 10),
     # h is written by one CTA while the others still read x and r: no overlap allowed
     (dict(h=A), 10), (dict(h=A + 4096 - 16), 10), (dict(r=FAR, h=FAR + 16), 10), (dict(h=A - 4096 + 16), 10),
+    # nor may y or the packed copy overlap x or r
+    (dict(y=A), 10), (dict(r=FAR, y=FAR + 64), 10), (dict(xq=q.Q8KPtrs(A, YA + 4096, YA + 8192)), 10),
 ])
 def test_rmsnorm_matvec_refusals(L, kw, status):
     assert st_norm_mv(L, **kw) == status

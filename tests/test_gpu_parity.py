@@ -648,8 +648,8 @@ WS_SHAPES = [("q4k", 4096, 4096, 1, False), ("q4k", 28672, 4096, 1, True), ("q6k
 def test_workspace_same_bits(fmtname, rows, K, batch, fused, per_mille, warps):
     """qmd_qmatvec_ws / qmd_qmatvec_x_ws: bit-identical to the calls without a workspace and to the
     same-order oracle, three calls in a row on one workspace, which each call leaves zeroed.  Claims
-    are used where every warp has two tiles of its own: the 28672-row shape on the default plan,
-    and most shapes once the plan is forced to one or three warps per CTA."""
+    are used at one vector where every warp has two tiles of its own: the 28672-row shape on the
+    default plan, and most one-vector shapes once the plan is forced to one or three warps per CTA."""
     seed = 7 * rows + K + batch
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
@@ -719,3 +719,29 @@ def test_workspace_refusals_write_nothing():
                               None) == 1
     torch.cuda.synchronize()
     assert torch.isnan(y).all() and guard_intact(buf, 1, rows) and int(ws.abs().sum()) == 0
+
+
+def test_bind_then_matvec_in_one_stream_without_a_host_sync():
+    """qmd_bind_q6k writes the split bodies and prefix with an ordinary launch; a mat-vec launched
+    right after it in the same stream, as a programmatic dependent, starts reading weights before
+    its dependency wait.  The bind kernel signals completion only by exiting, so the mat-vec must
+    still see the final weights: checked with the destination buffers filled with other bytes
+    first, the bind and the mat-vec back to back with no host synchronisation, three times."""
+    rows, K = 4096, 14336
+    nb = K // 256
+    Wg = synth.q6k_weights(91, rows, K)
+    g = dev(Wg.reshape(rows, -1))
+    x = synth.activations(92, 1, K)
+    xd = dev(x)
+    s = torch.cuda.Stream()
+    for fill in (0xA5, 0x00, 0xFF):
+        body = torch.full((rows, nb * 208), fill, dtype=torch.uint8, device=DEV)
+        prefix = torch.full((rows, q.q6k_prefix_stride(K)), -1 if fill == 0xFF else fill, dtype=torch.int16,
+                            device=DEV)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            q.bind_q6k(g, rows, K, body=body, prefix=prefix, stream=s)
+            y = q.qmatvec_x(q.Q6_K_SPLIT, body, prefix, xd, rows=rows, stream=s)
+        torch.cuda.synchronize()
+        q.get_device_error()
+        check_against_oracle("q6k", Wg, x, y.cpu().numpy(), f64_idx=_sample_rows(rows, 200, fill))
