@@ -176,14 +176,13 @@ def alu_roofline(q, step, batch: int, ms_per_launch: float, dp4a_rate: float, mm
     m16n8k16, 4096 FLOP with the batch padded to 8, per block-row) on the tensor-core kernel."""
     q4 = [p for p in step.projs if p.fmt == q.Q4_K]
     block_rows = sum(p.rows * (p.K // 256) for p in q4) / len(q4)
-    info = q.launch_info(q.Q4_K, q4[0].rows, q4[0].K, batch)
-    tc = batch >= 3 and info["rows_per_stage"] == 16
+    tc = q.launch_kernel(q.Q4_K, q4[0].rows, q4[0].K, batch) == "qmv_tc_kernel"
     if tc:
         ops, peak, unit, op = block_rows * 4096.0, mma_rate, "TFLOP/s", "mma.sync.m16n8k16 f16->f32"
     else:
         ops, peak, unit, op = block_rows * 64.0 * batch, dp4a_rate, "Tdp4a/s", "dp4a"
     achieved = ops / (ms_per_launch * 1e-3)
-    return {"bound": "alu", "kernel": kernel_name(info, batch), "op": op,
+    return {"bound": "alu", "kernel": kernel_name(q, q.Q4_K, q4[0].rows, q4[0].K, batch), "op": op,
             "achieved": achieved / 1e12, "peak": peak / 1e12, "unit": unit, "frac": achieved / peak,
             "ops_per_launch": ops, "peak_kind": "measured (qmd_measure_alu, register-only kernels)"}
 
@@ -342,11 +341,9 @@ def time_graph(torch, g, reps: int, stream) -> float:
     return e0.elapsed_time(e1) / reps
 
 
-def kernel_name(info: dict, batch: int) -> str:
-    """The mat-vec kernel a launch plan (qmd_qmatvec_launch_info) runs."""
-    if info["rows_per_stage"] == 4:
-        return "qmv_rl_kernel"
-    return "qmv_tc_kernel" if info["rows_per_stage"] == 16 and batch >= 3 else "qmv_kernel"
+def kernel_name(q, fmt: int, rows: int, K: int, batch: int) -> str:
+    """The mat-vec kernel qmd_qmatvec runs for these sizes (qmd_qmatvec_launch_kernel)."""
+    return q.launch_kernel(fmt, rows, K, batch)
 
 
 def time_configs(torch, q, device, peak: float, peak_kind: str = "measured") -> dict:
@@ -394,7 +391,7 @@ def time_configs(torch, q, device, peak: float, peak_kind: str = "measured") -> 
             out[f"config{cid}_b{B}"] = {
                 "shape": f"{fmt} {rows}x{K} batch {B}", "us_per_launch": ms * 1e3, "gbs": gbs,
                 "frac_of_peak": gbs / peak, "peak_kind": peak_kind, "frac_of_nominal_8TBps": gbs / NOMINAL_HBM_GBS,
-                "bytes_per_launch": alg, "weight_copies_rotated": ncopy, "kernel": kernel_name(info, B),
+                "bytes_per_launch": alg, "weight_copies_rotated": ncopy, "kernel": kernel_name(q, f, rows, K, B),
                 "grid": info["grid"], "threads": info["threads"]}
             del gr
         del copies
@@ -419,12 +416,12 @@ def time_step_at(torch, q, step, batch: int, steps: int, warmup: int, stream, pe
     b4 = sum(per(p) for p in st.projs if p.fmt == q.Q4_K) / nq4
     nb = st.bytes()
     q.get_device_error()
-    info = q.launch_info(q.Q4_K, st.projs[0].rows, st.projs[0].K, batch)
     out = {"value": nb["algorithmic"] / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms, "steps": steps,
            "frac_of_peak": nb["algorithmic"] / (ms * 1e-3) / 1e9 / peak,
            "row_vectors_per_s": sum(p.rows for p in st.projs) * batch / (ms * 1e-3),
            "launch": "pack fused into the mat-vec" if all(p.fused for p in st.projs) else "pack+mat-vec",
-           "q4k_kernel": kernel_name(info, batch), "q4k_us_per_launch": ms4 * 1e3,
+           "q4k_kernel": kernel_name(q, q.Q4_K, st.projs[0].rows, st.projs[0].K, batch),
+           "q4k_us_per_launch": ms4 * 1e3,
            "q4k_roofline_frac": b4 / (ms4 * 1e-3) / 1e9 / peak}
     del g, g4, st
     return out
@@ -562,8 +559,8 @@ def run_ours(args):
                          "matvec_only": world * nbytes["matvec"] / (ms_max * 1e-3) / 1e9,
                          "pack_inclusive": world * (nbytes["matvec"] + nbytes["pack"]) / (ms_max * 1e-3) / 1e9},
         "roofline": {"bound": "hbm",
-                     "kernel": "%s<Q4_K, batch %d, %s>" % (kernel_name(q.launch_info(q.Q4_K, 4096, 4096, args.batch),
-                                                                       args.batch), args.batch,
+                     "kernel": "%s<Q4_K, batch %d, %s>" % (kernel_name(q, q.Q4_K, 4096, 4096, args.batch),
+                                                            args.batch,
                                                             "fused pack" if q4_fused else "packed input"),
                      "achieved": ach4, "peak": peak,
                      "unit": "GB/s", "frac": ach4 / peak, "peak_kind": peak_kind,

@@ -194,9 +194,9 @@ qmd_status qmd_qmatvec_x(qmd_fmt fmt, const void *W, const void *W_aux, const fl
 /*
  * qmd_qmatvec_ws, qmd_qmatvec_x_ws -- qmd_qmatvec and qmd_qmatvec_x with a scheduling workspace:
  * the same results, bit for bit.  With one vector and enough rows that every warp of the
- * row-lane kernel has two 4-row tiles of its own (e.g. 28672 rows), the first three quarters of
+ * row-lane kernel has two 2-row tiles of its own (e.g. 28672 rows), the first three quarters of
  * the rows are split evenly over the multiprocessors as usual, and the last quarter is handed to
- * warps four rows at a time, in the order they ask for more work, so that a multiprocessor that
+ * warps two rows at a time, in the order they ask for more work, so that a multiprocessor that
  * runs slow does not set the end of the launch.  Other launches ignore the workspace.  This is a scheduling choice of this implementation; the pages
  * have no counterpart.
  *   workspace  device, QMD_WORKSPACE_BYTES bytes, 16-byte aligned, owned by the caller.  Zero it
@@ -339,6 +339,13 @@ void qmd_set_wait_limit_ns(uint64_t ns);
 qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int batch, int *grid,
                                    int *threads, int *smem_bytes, int *stages, int *rows_per_stage);
 
+/*
+ * qmd_qmatvec_launch_kernel -- which kernel qmd_qmatvec would run for these sizes on the current
+ * device: 0 the dp4a slice kernel, 1 the tensor-core kernel, 2 the row-lane kernel; a negative
+ * qmd_status if the call would be refused.  (Debug launch flags and forced plans apply.)
+ */
+int qmd_qmatvec_launch_kernel(qmd_fmt fmt, int64_t rows, int64_t K, int batch);
+
 /* ---- test-only entry points (same kernels, extra outputs) --------------------------------- */
 
 /*
@@ -409,7 +416,7 @@ void qmd_debug_set_launch_flags(unsigned flags);
 
 /*
  * qmd_debug_set_dynamic_tiles -- test-only: the share, per mille (0..1000), of a row-lane launch's
- * 4-row tiles that qmd_qmatvec_ws hands out by claims (the rest split evenly); any other value
+ * 2-row tiles that qmd_qmatvec_ws hands out by claims (the rest split evenly); any other value
  * restores the default.  Results do not depend on it.  Process-wide.
  */
 void qmd_debug_set_dynamic_tiles(int per_mille);

@@ -86,6 +86,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_get_device_error": ([vp], i32),
             "qmd_set_wait_limit_ns": ([u64], None),
             "qmd_qmatvec_launch_info": ([i32, i64, i64, i32, ip, ip, ip, ip, ip], i32),
+            "qmd_qmatvec_launch_kernel": ([i32, i64, i64, i32], i32),
             "qmd_debug_qmatvec_dump": ([i32, vp, vp, Q8KPtrs, vp, i64, i64, i32, vp, vp, vp], i32),
             "qmd_debug_wait_timeout": ([u64, vp], i32),
             "qmd_measure_alu": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], i32),
@@ -297,6 +298,17 @@ def launch_info(fmt: int, rows: int, K: int, batch: int) -> dict:
     vals = [ctypes.c_int() for _ in range(5)]
     _check(lib().qmd_qmatvec_launch_info(fmt, rows, K, batch, *[ctypes.byref(v) for v in vals]))
     return dict(zip(("grid", "threads", "smem_bytes", "stages", "rows_per_stage"), (v.value for v in vals)))
+
+
+KERNELS = {0: "qmv_kernel", 1: "qmv_tc_kernel", 2: "qmv_rl_kernel"}
+
+
+def launch_kernel(fmt: int, rows: int, K: int, batch: int) -> str:
+    """qmd_qmatvec_launch_kernel: the name of the kernel qmatvec runs for these sizes."""
+    k = int(lib().qmd_qmatvec_launch_kernel(fmt, rows, K, batch))
+    if k < 0:
+        _check(-k)
+    return KERNELS[k]
 
 
 def debug_qmatvec_dump(fmt: int, W, W_aux, xq: Q8K, rows: int | None = None, stream=None):

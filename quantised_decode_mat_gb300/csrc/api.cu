@@ -232,7 +232,7 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
 }
 
 // Row-lane kernel (qmv_rl.cuh): one CTA per SM (more when forced), a ring for as many warps as
-// the CTA has 4-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
+// the CTA has 2-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
 // has steps) that fits beside the activations, up to 16 warps to pack them, and one more warp
 // that requests the rings' first fills.  false if nothing fits (very long rows).
 static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
@@ -883,6 +883,26 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
     if (stages) *stages = p.stages;
     if (rows_per_stage) *rows_per_stage = p.RG * p.PR;
     return QMD_OK;
+}
+
+int qmd_qmatvec_launch_kernel(qmd_fmt fmt, int64_t rows, int64_t K, int batch)
+{
+    if (fmt != QMD_Q4_K && fmt != QMD_Q5_K && fmt != QMD_Q6_K_SPLIT)
+        return -(int)QMD_ERR_FORMAT;
+    qmd_status st = check_k(K);
+    if (st != QMD_OK)
+        return -(int)st;
+    if (batch < 1 || batch > QMD_MAX_BATCH)
+        return -(int)QMD_ERR_BATCH;
+    if (rows < 1 || rows > (int64_t)1 << 31)
+        return -(int)QMD_ERR_SHAPE;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != QMD_OK)
+        return -(int)st;
+    QmvPlan p;
+    if ((st = qmv_plan(fmt, rows, (int)(K / QMD_QK), batch, dev, &p)) != QMD_OK)
+        return -(int)st;
+    return p.layout;
 }
 
 qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)

@@ -15,32 +15,34 @@
 // runs the 64 dp4a of the block against activation codes broadcast from shared memory, and
 // evaluates the block's epilogue itself -- about 6 warp instructions per block-row.
 //
-// Work split.  Lane (r, g) = (lane / 8, lane % 8) takes row r of a 4-row tile and block 8s + g
-// of step s, so one warp step covers 4 rows x 8 blocks.  A warp owns whole rows: it walks all
-// steps of each of its tiles and sums the row's terms in registers in the declared order --
-// blocks in groups of four, (t0 + t1) + (t2 + t3) by two xor-shuffles inside each half of the
-// 8 lanes of a row; groups in runs of four, ((G0 + G1) + G2) + G3, one step giving two groups;
-// runs left to right -- so warps never wait for each other after the activations are in place.
-// CTAs (one per SM) take contiguous ranges of tiles, and warps take every W-th tile of it.
+// Work split.  Lane (r, g) = (lane / 16, lane % 16) takes row r of a 2-row tile and block 16s + g
+// of step s, so one warp step covers 2 rows x 16 blocks: one run of the declared row order.  A
+// warp owns whole rows: it walks all steps of each of its tiles and sums the row's terms in
+// registers in the declared order -- blocks in groups of four, (t0 + t1) + (t2 + t3) by two
+// xor-shuffles inside each quarter of the 16 lanes of a row; the run's four groups, ((G0 + G1) +
+// G2) + G3; runs left to right -- so warps never wait for each other after the activations are
+// in place.  CTAs (one per SM) take contiguous ranges of tiles, and warps take every W-th tile
+// of it.  (Tiles of 4 rows x 8 blocks gave the short 4096-row projections only ~7 warps per SM,
+// whose compute then set their time.)
 //
 // Staging.  Each warp streams its own steps through a private ring of S slots: lane 0 issues one
 // 3-D tensor copy (TMA) per step -- the box is (block bytes, 8 blocks, 4 rows) of the weight
-// tensor viewed as [rows][nb][block bytes] -- plus, for Q6_K, a 2-D copy of the 4 rows' 16-byte
-// chunks of the scale prefix; both complete on the slot's mbarrier.  The box lands as [4 rows]
-// [8 blocks][block bytes]: with 144, 176 or 208-byte blocks a 16-byte load by the 32 lanes hits
+// tensor viewed as [rows][nb][block bytes] -- plus, for Q6_K, a 2-D copy of the 2 rows' 32-byte
+// chunks of the scale prefix; both complete on the slot's mbarrier.  The box lands as [2 rows]
+// [16 blocks][block bytes]: with 144, 176 or 208-byte blocks a 16-byte load by the 32 lanes hits
 // each group of four banks exactly four times, the minimum for 512 bytes.  Blocks and rows past
-// the tensor's end read as zeros (their lanes skip the work and add +0).  The first S steps are
-// requested before the programmatic-launch wait (weights only).  Activation codes sit in shared
-// memory 272 bytes apart per block, so the 8 blocks a warp reads at once fall in 8 different
-// bank groups and each 16-byte load is one broadcast wavefront.
+// the tensor's end read as zeros (their lanes skip the work and add +0).  A producer warp
+// requests the first ring fills around the programmatic-launch wait (weights only).  Activation
+// codes sit in shared memory 272 bytes apart per block, so the 16 blocks a warp reads at once
+// spread evenly over the bank groups and each 16-byte load takes the minimum two wavefronts.
 #pragma once
 
 #include "qmv_tc.cuh"
 
 namespace qmd {
 
-constexpr int RL_ROWS = 4;        // rows per tile (lane bits 3..4)
-constexpr int RL_BLOCKS = 8;      // blocks per step (lane bits 0..2)
+constexpr int RL_ROWS = 2;        // rows per tile (lane bit 4)
+constexpr int RL_BLOCKS = 16;     // blocks per step, one run of the row order (lane bits 0..3)
 constexpr int RL_ACT = 272;       // shared-memory bytes per activation block: 256 codes + 16 pad
 constexpr int RL_MAX_WARPS = 16;  // warps that own rings, and warps that pack
 // Ring / packing warps a CTA may have for B vectors: 16 for one or two, 8 above (so that the
@@ -58,7 +60,7 @@ constexpr int RL_PRE_STEPS = 1;   // default ring slots per warp requested befor
 __host__ __device__ constexpr int rl_block_bytes(int f) { return f == QMD_Q6_K_SPLIT ? 208 : f == QMD_Q5_K ? 176 : 144; }
 __host__ __device__ constexpr int rl_box_bytes(int f) { return RL_ROWS * RL_BLOCKS * rl_block_bytes(f); }
 // bytes one step's copies complete on its barrier: the box, and the Q6_K prefix chunks
-__host__ __device__ constexpr int rl_tx_bytes(int f) { return rl_box_bytes(f) + (f == QMD_Q6_K_SPLIT ? RL_ROWS * 16 : 0); }
+__host__ __device__ constexpr int rl_tx_bytes(int f) { return rl_box_bytes(f) + (f == QMD_Q6_K_SPLIT ? RL_ROWS * RL_BLOCKS * 2 : 0); }
 // a ring slot, a multiple of 128 bytes: the box, then (Q6_K) the prefix chunks
 __host__ __device__ constexpr int rl_slot_bytes(int f) { return rl_box_bytes(f) + (f == QMD_Q6_K_SPLIT ? 128 : 0); }
 
@@ -92,8 +94,8 @@ __host__ __device__ inline RlLayout qmv_rl_layout(int f, int W, int S, int B, in
 
 struct RlParams {
     QmvKParams k;        // k.WR: warps with a ring (the others only pack); k.stages: ring slots per warp
-    CUtensorMap wmap;    // W as u8 [rows][nb][block bytes], box: block bytes x 8 blocks x 4 rows
-    CUtensorMap premap;  // Q6_K prefix as u16 [rows][prefix stride], box: 8 scales x 4 rows
+    CUtensorMap wmap;    // W as u8 [rows][nb][block bytes], box: block bytes x 16 blocks x 2 rows
+    CUtensorMap premap;  // Q6_K prefix as u16 [rows][prefix stride], box: 16 scales x 2 rows
 };
 
 // Byte b of w, sign-extended (a signed bit-field extract).
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
     const int W = p.WR, S = p.stages, nb = p.nb;  // warps 0 .. W-1 own rings and tiles
     const int NW = blockDim.x >> 5;                // warp NW-1 requests the first ring fills,
     const int NP = NW - 1;                         // warps 0 .. NP-1 pack the activations
-    const int r = lane >> 3, g = lane & 7;
+    const int r = lane >> 4, g = lane & 15;
     const int nsteps = (nb + RL_BLOCKS - 1) / RL_BLOCKS;
     // The tiles: without a workspace, CTA b owns q or q + 1 consecutive tiles of an even split
     // [ts0, ts1) and its warp w takes ts0 + w, ts0 + w + W, ...  With one, only the first `nstat`
@@ -551,10 +553,10 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
 
     // ---- the warp's steps --------------------------------------------------------------------
     const unsigned long long wait_ns = p.wait_ns;
-    float T[B], R[B];
+    float T[B];
 #pragma unroll
     for (int v = 0; v < B; ++v)
-        T[v] = R[v] = 0.0f;
+        T[v] = 0.0f;
     int64_t tile = -1;
     int s = 0, slot = 0;
     uint32_t par = 0u;
@@ -596,7 +598,7 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
         float t[B];
         if (blk < nb) {
             const unsigned short q6d =
-                Q6 ? *reinterpret_cast<const unsigned short *>(box + BOX + 16 * r + 2 * g) : (unsigned short)0;
+                Q6 ? *reinterpret_cast<const unsigned short *>(box + BOX + 2 * (RL_BLOCKS * r + g)) : (unsigned short)0;
             rl_block_terms<F, B, DUMP>(box + (r * RL_BLOCKS + g) * BB, acts + (size_t)blk * RL_ACT, sdx, saux, nb,
                                        blk, q6d, p, row, row < p.rows, t);
         } else {
@@ -610,22 +612,19 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
             fence_proxy_async_smem();
             issue_next(true, slot);
         }
-        // groups of four blocks: lanes g < 4 hold group 2s, lanes g >= 4 group 2s + 1
+        // The step is run s of the row: groups of four blocks, (t0 + t1) + (t2 + t3) by two
+        // xor-shuffles inside each quarter of the row's 16 lanes (absent blocks add +0); then the
+        // run, ((G0 + G1) + G2) + G3, from the four quarters (absent groups are +0 the same way);
+        // the runs left to right.  Every lane of the row ends with the same bits.
+        const int q0 = lane & 16;  // the row's first lane
 #pragma unroll
         for (int v = 0; v < B; ++v) {
             float gs = __fadd_rn(t[v], __shfl_xor_sync(0xffffffffu, t[v], 1));
             gs = __fadd_rn(gs, __shfl_xor_sync(0xffffffffu, gs, 2));
-            const float go = __shfl_xor_sync(0xffffffffu, gs, 4);
-            const float Ga = g < 4 ? gs : go, Gb = g < 4 ? go : gs;
-            if ((s & 1) == 0) {
-                R[v] = __fadd_rn(Ga, Gb);  // a run's first two groups
-                if (s == nsteps - 1)       // its last two are past the row's end
-                    R[v] = __fadd_rn(__fadd_rn(R[v], 0.0f), 0.0f);
-            } else {
-                R[v] = __fadd_rn(__fadd_rn(R[v], Ga), Gb);
-            }
-            if ((s & 1) || s == nsteps - 1)
-                T[v] = s < 2 ? R[v] : __fadd_rn(T[v], R[v]);  // runs left to right
+            const float G0 = __shfl_sync(0xffffffffu, gs, q0), G1 = __shfl_sync(0xffffffffu, gs, q0 + 4);
+            const float G2 = __shfl_sync(0xffffffffu, gs, q0 + 8), G3 = __shfl_sync(0xffffffffu, gs, q0 + 12);
+            const float Rv = __fadd_rn(__fadd_rn(__fadd_rn(G0, G1), G2), G3);
+            T[v] = s == 0 ? Rv : __fadd_rn(T[v], Rv);
         }
         if (s == nsteps - 1) {
             if (row < p.rows) {
@@ -652,9 +651,9 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
     // every step this warp requested it also consumed, so no copy is in flight here
 }
 
-// Tensor maps of one call: W as bytes [rows][nb][block bytes] in boxes of (block bytes, 8
-// blocks, 4 rows) -- blocks and rows past the end read as zeros -- and for Q6_K the prefix as
-// u16 [rows][prefix stride] in boxes of 8 entries x 4 rows.  Strides are multiples of 16 bytes
+// Tensor maps of one call: W as bytes [rows][nb][block bytes] in boxes of (block bytes, 16
+// blocks, 2 rows) -- blocks and rows past the end read as zeros -- and for Q6_K the prefix as
+// u16 [rows][prefix stride] in boxes of 16 entries x 2 rows.  Strides are multiples of 16 bytes
 // (block bytes 144, 176, 208; the prefix stride a multiple of 8 entries), bases 16-byte aligned
 // (checked by the caller).
 template <int F>
@@ -676,7 +675,7 @@ qmd_status rl_tensor_maps(const QmvKParams &kp, RlParams &rp)
     if (F == QMD_Q6_K_SPLIT) {
         const cuuint64_t pdim[2] = {(cuuint64_t)(kp.pre_bytes / 2), (cuuint64_t)kp.rows};
         const cuuint64_t pstr[1] = {(cuuint64_t)kp.pre_bytes};
-        const cuuint32_t pbox[2] = {8, (cuuint32_t)RL_ROWS};
+        const cuuint32_t pbox[2] = {(cuuint32_t)RL_BLOCKS, (cuuint32_t)RL_ROWS};
         if (enc(&rp.premap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t *>(kp.Wpre), pdim, pstr, pbox,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

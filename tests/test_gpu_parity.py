@@ -317,18 +317,17 @@ def test_long_rows_beyond_the_dp4a_limit(fmtname, rows, K, batch):
     at one or two vectors, flag 16 at three or four), or on the tensor-core kernel run by run
     (the default at three or four vectors, flag 8 below).  All bit-identical to the same-order
     oracle."""
-    assert (q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == RL_ROWS) == (batch <= 2)
+    assert (q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_rl_kernel") == (batch <= 2)
     seed = rows + K + batch
     Wg = synth.weights(fmtname, seed, rows, K)
     x = synth.activations(seed, batch, K)
     xq = gpu_pack(x)
     y = run_matvec(fmtname, Wg, xq, rows, K, batch)
     check_against_oracle(fmtname, Wg, x, y)
-    for flags, rps in ((SLICE, 16), (RL, RL_ROWS)):
+    for flags, kern in ((SLICE, "qmv_tc_kernel"), (RL, "qmv_rl_kernel")):
         q.debug_set_launch_flags(flags)
         try:
-            info = q.launch_info(QFMT[fmtname], rows, K, batch)
-            assert info["rows_per_stage"] == rps and (rps != 16 or info["threads"] == 512)
+            assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == kern
             y2 = run_matvec(fmtname, Wg, xq, rows, K, batch)
         finally:
             q.debug_set_launch_flags(0)
@@ -347,7 +346,7 @@ def test_long_rows_with_forced_ctas_per_sm(cps):
     q.debug_set_plan(0, 0, 0, cps)
     q.debug_set_launch_flags(SLICE)  # the tensor-core kernel, not the row-lane one
     try:
-        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16
+        assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_tc_kernel"
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
     finally:
         q.debug_set_plan()
@@ -428,7 +427,6 @@ DP4A_ONLY = 2  # launch flag: keep batches of 5..8 on the dp4a kernel
 TC_ALL = 4     # launch flag: every batch of 3..8 on the tensor-core kernel (long rows run by run)
 SLICE = 8      # launch flag: the dp4a slice kernel instead of the row-lane one
 RL = 16        # launch flag: the row-lane kernel for batches of 3 and 4 as well
-RL_ROWS = 4    # rows per tile of the row-lane kernel (its launch_info rows_per_stage)
 
 
 # rows of one run of at most 16 blocks, and longer rows walked run by run: 17 blocks (a run of
@@ -449,18 +447,18 @@ def test_tensor_core_path_equals_dp4a_path(fmtname, batch, rows, K):
     # the default plan: the tensor cores for Q4_K / Q5_K rows of at most 16 blocks and for rows
     # the dp4a kernel cannot take, the dp4a kernel otherwise
     default_tc = (fmtname != "q6k" and K <= 4096) or K > 16384
-    assert (q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16) == default_tc
+    assert (q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_tc_kernel") == default_tc
     q.debug_set_launch_flags(TC_ALL)
     try:
         info = q.launch_info(QFMT[fmtname], rows, K, batch)
-        assert info["threads"] == 32 * min(K // 256, 16) and info["rows_per_stage"] == 16  # the tensor-core plan
+        assert info["threads"] == 32 * min(K // 256, 16) and q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_tc_kernel"
         y_tc = run_matvec(fmtname, Wg, xq, rows, K, batch)
     finally:
         q.debug_set_launch_flags(0)
     if K <= 16384:  # the dp4a kernel's limit above two vectors
         q.debug_set_launch_flags(DP4A_ONLY)
         try:
-            assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] != 16
+            assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_kernel"
             y_dp = run_matvec(fmtname, Wg, xq, rows, K, batch)
         finally:
             q.debug_set_launch_flags(0)
@@ -495,7 +493,7 @@ def test_tensor_core_extreme_magnitudes(fmtname, K):
     x[4] = synth.activations(78, 1, K)[0]
     q.debug_set_launch_flags(TC_ALL)
     try:
-        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 16  # the tensor-core plan
+        assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_tc_kernel"
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
         if fmtname == "q6k":
             body, prefix = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)

@@ -48,10 +48,10 @@ def _rows_to_check(p, batch):
     tiles = (p.rows + 15) // 16
     for g in (G, 152, 304, 456, 608):  # the plan's grid and the grids the fused plans may take
         pick |= {(p.rows * b) // g for b in range(g)} | {(p.rows * b) // g - 1 for b in range(1, g)}
-        # the tensor-core kernel splits whole 16-row tiles, the row-lane kernel whole 4-row tiles
+        # the tensor-core kernel splits whole 16-row tiles, the row-lane kernel whole 2-row tiles
         pick |= {16 * ((tiles * b) // g) for b in range(g)} | {16 * ((tiles * b) // g) - 1 for b in range(1, g)}
-        t4 = (p.rows + 3) // 4
-        pick |= {4 * ((t4 * b) // g) for b in range(g)} | {4 * ((t4 * b) // g) - 1 for b in range(1, g)}
+        t2 = (p.rows + 1) // 2
+        pick |= {2 * ((t2 * b) // g) for b in range(g)} | {2 * ((t2 * b) // g) - 1 for b in range(1, g)}
     return np.array(sorted(r for r in pick if 0 <= r < p.rows))
 
 
