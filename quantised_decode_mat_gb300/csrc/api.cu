@@ -278,7 +278,7 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->RG = 1;
     pl->PR = RL_ROWS;
     pl->stage_bytes = rl_slot_bytes(fmt);
-    // ring slots per warp requested before the dependency wait (the rest right after it); a
+    // ring slots per warp requested before the dependency wait (the rest after the pack); a
     // forced rows-per-stage value stands for this count here
     const int pre = g_force_rows.load() > 0 ? g_force_rows.load() : RL_PRE_STEPS;
     pl->pre_steps = pre < S ? pre : S;

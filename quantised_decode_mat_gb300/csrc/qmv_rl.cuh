@@ -55,7 +55,7 @@ constexpr int RL_DEFAULT_BATCH = 2;  // the plan's default for at most this many
 constexpr int RL_POOLS = 8;          // claim pools of the scheduling workspace (CTA b draws from pool b % 8)
 constexpr int RL_WS_STRIDE = 64;     // words between the workspace's counters (256 bytes: separate L2 lines)
 static_assert(RL_WS_STRIDE * (RL_POOLS + 1) * 4 <= QMD_WORKSPACE_BYTES, "the pools' counters and the done word");
-constexpr int RL_PRE_STEPS = 1;   // default ring slots per warp requested before the dependency wait
+constexpr int RL_PRE_STEPS = 2;   // default ring slots per warp requested before the dependency wait
 
 __host__ __device__ constexpr int rl_block_bytes(int f) { return f == QMD_Q6_K_SPLIT ? 208 : f == QMD_Q5_K ? 176 : 144; }
 __host__ __device__ constexpr int rl_box_bytes(int f) { return RL_ROWS * RL_BLOCKS * rl_block_bytes(f); }
@@ -369,30 +369,40 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
 
     // The first S steps of every ring's static tiles, requested by the one warp that does
     // nothing else (a tensor copy takes the unit tens of nanoseconds, so a few dozen of them would
-    // hold up the packing warps), slot by slot across the warps so that every warp's first step
-    // comes first: p.pre_steps slots before the dependency wait (they read weights only; a
-    // deeper burst there measured slower where the launch's CTAs start only as the previous
-    // launch ends, since it holds up that launch's last stores and this one's activation loads),
-    // the rest as soon as the wait is over.
+    // hold up the packing warps), slot by slot across the warps so that every warp's first steps
+    // come first: p.pre_steps slots (2) before the dependency wait -- they read weights only --
+    // and the rest once the activations are packed, since the pack's loads from L2 share the
+    // SM's path with these copies (measured on the 8-layer step: 1, 2, 3, 4 slots before the wait
+    // with the rest after the pack 33.4, 31.4, 31.6, 31.7 us a layer; the rest right after the
+    // wait instead 31.8-32.0).
     if (warp == NP) {
-        if (lane == 0) {
-            int64_t tk = 0;  // the static tile (of each warp's sequence) of step k
-            int sk = 0;      // and the step within it
-            for (int k = 0; k < S; ++k) {
-                if (k == p.pre_steps) {
-                    QMD_STAMP(p, 1);
-                    pdl_wait();
-                }
-                for (int w = 0; w < W; ++w) {
-                    const int64_t t = ts0 + w + tk * W;
-                    if (t < ts1)
-                        issue_w(w, t, sk, k);
-                }
-                if (++sk == nsteps) {
-                    sk = 0;
-                    ++tk;
-                }
+        int64_t tk = 0;  // the static tile (of each warp's sequence) of slot k's step
+        int sk = 0;      // and the step within it
+        auto issue_slot = [&](int k) {
+            for (int w = 0; w < W; ++w) {
+                const int64_t t = ts0 + w + tk * W;
+                if (t < ts1)
+                    issue_w(w, t, sk, k);
             }
+            if (++sk == nsteps) {
+                sk = 0;
+                ++tk;
+            }
+        };
+        const int pre = p.pre_steps < S ? p.pre_steps : S;
+        if (lane == 0) {
+            for (int k = 0; k < pre; ++k)
+                issue_slot(k);
+            QMD_STAMP(p, 1);
+        }
+        if (pre < S) {
+            // the rest once the activations are packed: the pack's loads share the SM's path
+            // from L2 with these copies (the whole warp meets the packing warps' barrier)
+            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * NW) : "memory");
+            if (lane == 0)
+                for (int k = pre; k < S; ++k)
+                    issue_slot(k);
         }
         return;  // the copies complete on the barriers by themselves
     }
@@ -542,8 +552,8 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
                 *reinterpret_cast<int4 *>(saux + i * 8) = reinterpret_cast<const int4 *>(p.xbs)[i];
         }
     }
-    // the packing warps only (the requesting warp has left)
-    asm volatile("bar.sync 1, %0;" ::"r"(32 * NP) : "memory");
+    // the packing warps, and the requesting warp if it still has copies to request after the pack
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * (p.pre_steps < S ? NW : NP)) : "memory");
     if (tid == 0)
         QMD_STAMP(p, 3);
     // the rest of the ring (claims may start now)
