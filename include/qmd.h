@@ -250,9 +250,10 @@ qmd_status qmd_qmatvec_x_static(qmd_fmt fmt, const void *W, const void *W_aux, c
  *           qmd_rmsnorm_q8k_pack it must NOT overlap x, r or g, since every CTA still reads x
  *           and r while it is written (QMD_ERR_VALUE); nor may y or xq_out overlap x or r.
  *   xq_out  optional, as qmd_qmatvec_x: the packed codes of the normalised vector
- * Other arguments as qmd_qmatvec.  Limits: the dp4a kernel's (every K up to 32768 at batch
- * <= 2 and 16384 above) with the packed codes in shared memory, as qmd_qmatvec_x; longer rows
- * give QMD_ERR_SHAPE (pack with qmd_rmsnorm_q8k_pack and call qmd_qmatvec instead).
+ * Other arguments as qmd_qmatvec.  Limits: at one or two vectors, any K whose packed codes fit
+ * in shared memory beside the weight stages (about 180,000 at one vector); at three to eight,
+ * the dp4a kernel's (K up to 16384); longer rows give QMD_ERR_SHAPE (pack with
+ * qmd_rmsnorm_q8k_pack and call qmd_qmatvec instead).
  * Errors: NULL (W, x, g, y, a partial xq_out, or W_aux for Q6_K_SPLIT), FORMAT,
  * K_NOT_MULTIPLE_OF_256, BATCH, MISALIGNED, VALUE (eps, or h_out overlapping x, r or g),
  * SHAPE, DEVICE, LAUNCH.

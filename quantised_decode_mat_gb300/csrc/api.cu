@@ -235,7 +235,7 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
 // the CTA has 2-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
 // has steps) that fits beside the activations, up to 16 warps to pack them, and one more warp
 // that requests the rings' first fills.  false if nothing fits (very long rows).
-static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl)
+static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, bool norm)
 {
     const int64_t tiles = (rows + RL_ROWS - 1) / RL_ROWS;
     const int nsteps = (nb + RL_BLOCKS - 1) / RL_BLOCKS;
@@ -258,7 +258,7 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (S > steps)
         S = (int)steps;
     for (; S >= 1; --S)
-        if (qmv_rl_layout(fmt, W, S, batch, nb).total <= budget)
+        if (qmv_rl_layout(fmt, W, S, batch, nb, norm).total <= budget)
             break;
     if (S < 1)
         return false;
@@ -269,10 +269,12 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     const int want = (int)(blocks < wmax ? blocks : wmax);
     if (g_force_rg.load() <= 0 && NW < want)
         NW = want;
+    if (norm && NW < 8)  // the RMSNorm form sums the squares with 256 threads
+        NW = 8;
     pl->layout = 2;
     pl->grid = (int)grid;
     pl->threads = 32 * (NW + 1);  // plus the warp that requests the first ring fills
-    pl->smem = qmv_rl_layout(fmt, W, S, batch, nb).total;
+    pl->smem = qmv_rl_layout(fmt, W, S, batch, nb, norm).total;
     pl->stages = S;
     pl->WR = W;
     pl->RG = 1;
@@ -303,14 +305,14 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per warp) that fits
     // beside the run sums (and, fused, the packed activations).  A forced ring cap below 3
     // selects the dp4a kernel, and so does a shape that does not fit.  The RMSNorm form exists
-    // only in the dp4a kernel.
+    // in the row-lane and dp4a kernels, not in this one.
     const int fst = g_force_stages.load();
     pl->tc_rows = 0;
     // One or two vectors: the row-lane kernel, unless a test flag asks for another kernel (three
     // and four on it too when a flag asks).
     const bool rl_batch = batch <= RL_DEFAULT_BATCH || ((launch_flags() & LAUNCH_RL) && batch <= RL_MAX_BATCH);
-    if (mode != QMV_NORM && rl_batch && !(launch_flags() & (LAUNCH_SLICE | LAUNCH_TC_ALL)) &&
-        rl_plan(fmt, rows, nb, batch, dev, pl))
+    if (rl_batch && !(launch_flags() & (LAUNCH_SLICE | LAUNCH_TC_ALL)) &&
+        rl_plan(fmt, rows, nb, batch, dev, pl, mode == QMV_NORM))
         return QMD_OK;
     const bool tc_faster = batch >= TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
     const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);

@@ -65,14 +65,14 @@ __host__ __device__ constexpr int rl_tx_bytes(int f) { return rl_box_bytes(f) + 
 __host__ __device__ constexpr int rl_slot_bytes(int f) { return rl_box_bytes(f) + (f == QMD_Q6_K_SPLIT ? 128 : 0); }
 
 struct RlLayout {
-    int bar_off, tile_off, sched_off, act_off, dx_off, aux_off, total;
+    int bar_off, tile_off, sched_off, act_off, dx_off, aux_off, norm_off, total;
 };
 
 // Shared memory: rings [W][S][slot] | mbarriers u64 [W][S] | the tile of each slot's step i32
 // [W][S] | activation codes i8 [B][nb][272] | block scales f32 [B][nb] | Q4_K, Q5_K: sums i16
 // [B][nb][8] of each 32 codes; Q6_K: sums i16 [B][nb][16] of each 16 codes (for the -32 offset
-// of the weight codes).
-__host__ __device__ inline RlLayout qmv_rl_layout(int f, int W, int S, int B, int nb)
+// of the weight codes) | RMSNorm form: warp sums of squares f32 [B][8] and 1/rms f32 [B].
+__host__ __device__ inline RlLayout qmv_rl_layout(int f, int W, int S, int B, int nb, bool norm = false)
 {
     RlLayout L;
     int o = W * S * rl_slot_bytes(f);
@@ -88,6 +88,9 @@ __host__ __device__ inline RlLayout qmv_rl_layout(int f, int W, int S, int B, in
     o = align_up(o + B * nb * 4, 16);
     L.aux_off = o;
     o += B * nb * (f == QMD_Q6_K_SPLIT ? 32 : 16);
+    L.norm_off = o;
+    if (norm)
+        o += B * 9 * 4;
     L.total = align_up(o, 16);
     return L;
 }
@@ -296,7 +299,8 @@ template <int F, int B, int MODE>
 __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __grid_constant__ RlParams rp)
 {
     constexpr bool Q6 = F == QMD_Q6_K_SPLIT;
-    constexpr bool PACK = MODE == QMV_PACK;
+    constexpr bool NORM = MODE == QMV_NORM;
+    constexpr bool PACK = MODE == QMV_PACK || NORM;  // both pack f32 activations themselves
     constexpr bool DUMP = MODE == QMV_DUMP;
     constexpr int BB = rl_block_bytes(F);
     constexpr int SLOT = rl_slot_bytes(F);
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
     const unsigned bx = blockIdx.x, G = gridDim.x;
     const unsigned st_q = nstat / G, st_rem = nstat - st_q * G;
     const int64_t ts0 = (int64_t)bx * st_q + min(bx, st_rem), ts1 = ts0 + st_q + (bx < st_rem ? 1 : 0);
-    const RlLayout L = qmv_rl_layout(F, W, S, B, nb);
+    const RlLayout L = qmv_rl_layout(F, W, S, B, nb, NORM);
 #ifdef QMD_TRACE
     if (tid == 0 && p.trace) {
         p.trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS] = globaltimer_ns();
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
 #endif
     // A launch whose geometry is not the plan's: flag it and leave without touching memory (after
     // the dependency wait, so that kernels launched after this one still see its predecessor done).
-    if (NW < W + 1 || (uint32_t)L.total > dynamic_smem_bytes()) {
+    if (NW < W + 1 || (NORM && NW - 1 < 8) || (uint32_t)L.total > dynamic_smem_bytes()) {
         pdl_wait();
         if (tid == 0)
             atomicOr(p.err, ERRBIT_PLAN);
@@ -498,7 +502,60 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
     int16_t *saux = reinterpret_cast<int16_t *>(smem + L.aux_off);
     const int NBv = B * nb;  // activation blocks
     if (PACK) {
-        // quantise the f32 activations, one warp per block, the stand-alone pack's arithmetic
+        const int64_t K = (int64_t)nb * 256;
+        float *s_part = reinterpret_cast<float *>(smem + L.norm_off);  // RMSNorm form: [B][8] and 1/rms [B]
+        float *s_inv = s_part + B * 8;
+        if (NORM) {
+            // RMSNorm of h = x (+ r), each f32 operation rounded alone, the sum of squares in the
+            // order the stand-alone RMSNorm pack declares (so the codes are the same): thread t
+            // of the first 256 adds the squares of elements t, t + 256, ... left to right; each
+            // warp combines its partials by xor-shuffles 16, 8, 4, 2, 1; the eight warp totals
+            // are added left to right.  CTA 0 writes h when asked.
+            for (int v = 0; v < B; ++v) {
+                if (tid < 256) {
+                    const float *xv = p.x + v * K;
+                    const float *rv = p.r ? p.r + v * K : nullptr;
+                    float *hv = (p.h_out && blockIdx.x == 0) ? p.h_out + v * K : nullptr;
+                    float acc = 0.0f;
+                    constexpr int U = 8;  // loads in flight per thread per round
+                    for (int64_t i0 = tid; i0 < K; i0 += (int64_t)U * 256) {
+                        float xu[U], ru[U];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int64_t i = i0 + (int64_t)u * 256;
+                            xu[u] = i < K ? xv[i] : 0.0f;
+                            ru[u] = (rv && i < K) ? rv[i] : 0.0f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int64_t i = i0 + (int64_t)u * 256;
+                            if (i < K) {
+                                const float h = rv ? __fadd_rn(xu[u], ru[u]) : xu[u];
+                                if (hv)
+                                    hv[i] = h;
+                                acc = __fadd_rn(acc, __fmul_rn(h, h));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+                    if (lane == 0)
+                        s_part[v * 8 + warp] = acc;
+                }
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(32 * NP) : "memory");
+            if (tid < B) {
+                float total = s_part[tid * 8];
+                for (int w = 1; w < 8; ++w)
+                    total = __fadd_rn(total, s_part[tid * 8 + w]);
+                const float ms = __fdiv_rn(total, (float)K);
+                s_inv[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(32 * NP) : "memory");
+        }
+        // quantise the f32 activations (RMSNorm form: n = (h * (1/rms)) * g), one warp per
+        // block, the stand-alone pack's arithmetic
         const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
         for (int b0 = warp; b0 < NBv; b0 += 4 * NP) {
             float4 xa[4], xb[4];
@@ -509,6 +566,26 @@ __global__ void __launch_bounds__(rl_max_threads(B), 1) qmv_rl_kernel(const __gr
                     const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
                     xa[u] = src[0];
                     xb[u] = src[1];
+                    if (NORM) {  // n = (h * (1/rms)) * g with h = x (+ r), as the RMSNorm pack does
+                        const int v = b / nb, blk_g = b - v * nb;
+                        float4 ra = make_float4(0.f, 0.f, 0.f, 0.f), rb = ra;
+                        if (p.r) {
+                            const float4 *rsrc = reinterpret_cast<const float4 *>(p.r + (int64_t)b * 256 + 8 * lane);
+                            ra = rsrc[0];
+                            rb = rsrc[1];
+                        }
+                        const float4 *gsrc = reinterpret_cast<const float4 *>(p.g + blk_g * 256 + 8 * lane);
+                        const float4 ga = gsrc[0], gb = gsrc[1];
+                        const float inv = s_inv[v];
+                        auto nrm = [&](float x, float r, float gg) {
+                            const float h = p.r ? __fadd_rn(x, r) : x;
+                            return __fmul_rn(__fmul_rn(h, inv), gg);
+                        };
+                        xa[u] = make_float4(nrm(xa[u].x, ra.x, ga.x), nrm(xa[u].y, ra.y, ga.y), nrm(xa[u].z, ra.z, ga.z),
+                                            nrm(xa[u].w, ra.w, ga.w));
+                        xb[u] = make_float4(nrm(xb[u].x, rb.x, gb.x), nrm(xb[u].y, rb.y, gb.y), nrm(xb[u].z, rb.z, gb.z),
+                                            nrm(xb[u].w, rb.w, gb.w));
+                    }
                 }
             }
 #pragma unroll
@@ -698,6 +775,7 @@ template <int F, int B>
 qmd_status launch_rl_batch(const RlParams &rp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
     return mode == QMV_PACK   ? launch_kernel<qmv_rl_kernel<F, B, QMV_PACK>>(rp, plan, s)
+           : mode == QMV_NORM ? launch_kernel<qmv_rl_kernel<F, B, QMV_NORM>>(rp, plan, s)
            : mode == QMV_DUMP ? launch_kernel<qmv_rl_kernel<F, B, QMV_DUMP>>(rp, plan, s)
                               : launch_kernel<qmv_rl_kernel<F, B, QMV_PLAIN>>(rp, plan, s);
 }
@@ -705,8 +783,6 @@ qmd_status launch_rl_batch(const RlParams &rp, const QmvPlan &plan, int mode, cu
 template <int F>
 qmd_status launch_qmv_rl(const QmvKParams &kp, const QmvPlan &plan, int mode, int batch, cudaStream_t s)
 {
-    if (mode == QMV_NORM)  // the RMSNorm form exists only in the dp4a slice kernel
-        return QMD_ERR_SHAPE;
     RlParams rp;
     rp.k = kp;
     const qmd_status st = rl_tensor_maps<F>(kp, rp);

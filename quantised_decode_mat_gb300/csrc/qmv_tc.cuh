@@ -766,7 +766,7 @@ template <int F>
 qmd_status launch_qmv_tc(const QmvKParams &kp, const QmvPlan &plan, int mode, cudaStream_t s)
 {
     const bool multi = kp.nb > TC_RUN;
-    if (mode == QMV_NORM)  // the RMSNorm form exists only in the dp4a kernel
+    if (mode == QMV_NORM)  // the RMSNorm form is not built in this kernel
         return QMD_ERR_SHAPE;
     TcParams tp;
     tp.k = kp;

@@ -101,10 +101,13 @@ def test_rmsnorm_matvec_equals_two_launches_and_the_oracle(fmtname, rows, K, bat
     assert O.rel_err(yg, O.qmatvec_f64(OFMT[fmtname], Wo, oqs, od)).max() <= 2e-3
 
 
+@pytest.mark.parametrize("flags", [0, 8], ids=["rowlane", "slice"])
 @pytest.mark.parametrize("rg,cps", [(1, 1), (2, 3), (4, 2), (8, 1)])
-def test_rmsnorm_matvec_under_forced_plans(rg, cps):
-    """Forced row groups and CTAs per SM (every CTA recomputes the norm; one row group of 4 warps
-    is widened to 256 threads): the same bits."""
+def test_rmsnorm_matvec_under_forced_plans(rg, cps, flags):
+    """Forced row groups (row-lane kernel: ring warps) and CTAs per SM (every CTA recomputes the
+    norm; a CTA with fewer than 8 warps is widened to the 256 threads the sum of squares takes):
+    the same bits, on the row-lane kernel (default at one vector) and the dp4a slice kernel."""
+    q.debug_set_launch_flags(flags)
     rows, K, batch = 3000, 4096, 1
     Wg, W, Wa = weights("q4k", 5, rows, K)
     x, r, g = synth.activations(5, batch, K), synth.residual(5, batch, K), synth.norm_gain(5, K)
@@ -116,6 +119,7 @@ def test_rmsnorm_matvec_under_forced_plans(rg, cps):
         q.get_device_error()
     finally:
         q.debug_set_plan()
+        q.debug_set_launch_flags(0)
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
 
 
@@ -129,10 +133,10 @@ def test_rmsnorm_matvec_refusals_write_nothing():
         q.qmatvec_rmsnorm_x(q.Q4_K, W, None, x, None, g, 1e-6, h_out=x, y=y, rows=rows)
     with pytest.raises(q.QmdError, match="QMD_ERR_VALUE"):
         q.qmatvec_rmsnorm_x(q.Q4_K, W, None, x, None, g, -1.0, y=y, rows=rows)
-    with pytest.raises(q.QmdError, match="QMD_ERR_SHAPE"):  # beyond the dp4a kernel's row length
-        Wl = torch.zeros(rows * 256 * 144, dtype=torch.uint8, device=DEV)
-        xl = torch.ones((1, 65536), dtype=torch.float32, device=DEV)
-        gl = torch.ones(65536, dtype=torch.float32, device=DEV)
+    with pytest.raises(q.QmdError, match="QMD_ERR_SHAPE"):  # a row too long for every kernel's form
+        Wl = torch.zeros(rows * 1024 * 144, dtype=torch.uint8, device=DEV)
+        xl = torch.ones((1, 262144), dtype=torch.float32, device=DEV)
+        gl = torch.ones(262144, dtype=torch.float32, device=DEV)
         q.qmatvec_rmsnorm_x(q.Q4_K, Wl, None, xl, None, gl, 1e-6, y=y[:1], rows=rows)
     torch.cuda.synchronize()
     assert torch.isnan(y).all() and intact(ybuf, batch, rows)
