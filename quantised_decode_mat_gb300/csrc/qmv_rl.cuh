@@ -48,7 +48,7 @@ constexpr int RL_MAX_WARPS = 16;  // warps that own rings, and warps that pack
 // Ring / packing warps a CTA may have for B vectors: 16 for one or two, 8 above (so that the
 // larger per-lane state of three and four vectors fits in registers), plus the warp that
 // requests the first ring fills.
-__host__ __device__ constexpr int rl_max_warps(int B) { return B <= 2 ? RL_MAX_WARPS : RL_MAX_WARPS / 2; }
+__host__ __device__ constexpr int rl_max_warps(int B) { return B <= 2 ? RL_MAX_WARPS : 12; }
 __host__ __device__ constexpr int rl_max_threads(int B) { return 32 * (rl_max_warps(B) + 1); }
 constexpr int RL_MAX_BATCH = 4;   // vectors per launch
 constexpr int RL_DEFAULT_BATCH = 2;  // the plan's default for at most this many vectors

@@ -11,8 +11,8 @@
 // cross-lane sum over those 16 values happens inside the instruction.
 //
 // Exactness.  Every operand is a small integer held exactly in f16: a weight code n (0..15, 0..31
-// with Q5_K's fifth bit, 0..63 for Q6_K) enters as 1024 + n (the byte, under a 0x64 exponent
-// byte), an activation code as itself (|q| <= 127).  The accumulator starts at -1024 x (the sum
+// with Q5_K's fifth bit, 0..63 for Q6_K) enters as 1024 + n (the code's bits in the mantissa of
+// 1024; a Q4_K / Q5_K high-nibble code as 1024 + 16 n), an activation code as itself (|q| <= 127).  The accumulator starts at -1024 x (the sum
 // of the activation codes the step covers) -- for Q6_K at -1056 x that sum, which also takes the
 // codes' -32 offset -- so the step leaves the exact integer dot: every partial sum is an integer
 // below 2^24 in magnitude, whatever order the unit adds in.  The dots leave as exact integers
@@ -21,8 +21,11 @@
 // Value order inside a step.  The MMA's k index can be any permutation of the step's 16 values,
 // as long as both operands use the same one.  Q4_K / Q5_K (32-value sub-blocks, two steps
 // each): lane (g, t) = (lane / 4, lane % 4) takes, of each 32-byte code chunk, the eight bytes
-// 8t .. 8t+7 (one 8-byte shared load per row), so step u in {0, 1} covers bytes 8t + 4u ..
-// 8t + 4u + 3 as the MMA's k = 2t, 2t+1, 2t+8, 2t+9.  Q6_K (16-value sub-blocks, one step
+// 8t .. 8t+7 (one 8-byte shared load per row), so step u in {0, 1} covers bytes 8t + 4u + i,
+// i = 0, 2 as the MMA's k = 2t, 2t+1 and i = 1, 3 as k = 2t+8, 2t+9.  That order lets one
+// masked OR turn two codes of a word into an f16 pair (bytes 0 and 2 of the word, then of the
+// word shifted by a byte); a high nibble enters in place, as 16 n, and its sub-block's scale
+// carries the 1/16.  Q6_K (16-value sub-blocks, one step
 // each): lane t takes values 4t .. 4t+3 of the sub-block, whose low nibbles and high bit pairs
 // sit in one 4-byte word of ql and one of qh.
 //
@@ -74,7 +77,8 @@ struct TcLayout {
 
 // Shared memory: warp rings [RW][stages][slot] | ring barriers u64 [RW][stages] | block terms f32
 // [TC_RED][RW][16 rows][8 vectors]
-// | accumulator starts f32 [RW][steps][8 vectors] | arrival counters u32 [TC_RED] | finished
+// | accumulator starts f32 [RW][steps][4 lane columns t][b(2t), b(2t+1), b(2t), b(2t+1)] (each
+// lane's C operand as one 16-byte load) | arrival counters u32 [TC_RED] | finished
 // tile i32 [TC_RED] | finished runs per row tile i32 [rows_pad / 16] | earlier runs' sums f32
 // [runs - 1][rows_pad][8] | fused form only: codes i8 [B][K], d f32 [B][nb], sums i16
 // [B][nb][8].  RW = min(nb, 16) warps; rows_pad = the CTA's rows rounded up to 16.
@@ -89,7 +93,7 @@ __host__ __device__ inline TcLayout qmv_tc_layout(int stages, int fmt, int nb, i
     L.red_off = o;
     o += TC_RED * RW * TC_ROWS * 8 * 4;
     L.bias_off = o;
-    o += RW * tc_steps(fmt) * 8 * 4;
+    o += RW * tc_steps(fmt) * 16 * 4;
     L.cnt_off = o;
     o += TC_RED * 4;
     L.fin_off = o;
@@ -135,6 +139,31 @@ __device__ __forceinline__ void mma_16816_c(float (&d)[4], const uint32_t (&a)[4
 __device__ __forceinline__ float byte_as_float(uint32_t w, uint32_t b)
 {
     return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b)), 8388608.0f);
+}
+
+// Byte b (0..3) of w over 16 as an exact float: the byte under the exponent of 2^19, whose
+// mantissa unit is 1/16, minus 2^19.
+__device__ __forceinline__ float byte16th_as_float(uint32_t w, uint32_t b)
+{
+    return __fsub_rn(__uint_as_float(__byte_perm(w, 0x49000000u, 0x7440u | b)), 524288.0f);
+}
+
+// The bits of w under mask M in bytes 0 and 2 (M = 0x000F000F: low nibbles n; 0x00F000F0: high
+// nibbles, 16 n) as the f16 pair 1024 + those bits: they sit in the mantissa of 0x6400 (1024,
+// unit 1).  One three-input logic operation, (w & M) | k, with k = 0x64006400 held in a register
+// (k6400()): written out, the compiler splits it in two.
+template <uint32_t M>
+__device__ __forceinline__ uint32_t nib_f16x2(uint32_t w, uint32_t k)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(M), "r"(k));
+    return r;
+}
+__device__ __forceinline__ uint32_t k6400()
+{
+    uint32_t k;
+    asm("mov.b32 %0, 0x64006400;" : "=r"(k));
+    return k;
 }
 
 // Signed byte b (0..3) of w as an exact float: (byte ^ 0x80) is byte + 128 in 0..255 under the
@@ -315,7 +344,7 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
     uint32_t bfr[32];
     float dxv[2];
     int4 bsv[2];
-    float *bias = reinterpret_cast<float *>(smem + L.bias_off) + warp * NSTEP * 8;
+    float *bias = reinterpret_cast<float *>(smem + L.bias_off) + warp * NSTEP * 16;
     auto load_run = [&](int blk) {
         const bool have = g < B;
         if (Q6) {
@@ -330,20 +359,23 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
                 int ps = __dp4a((int)w, 0x01010101, 0);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 1);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-                if (t == 0)
-                    bias[s * 8 + g] = -1056.0f * (float)ps;
+                if (t == 0) {  // vector g's start, in lane column g / 2 of step s
+                    float *bq = bias + (s * 4 + (g >> 1)) * 4 + (g & 1);
+                    bq[0] = bq[2] = -1056.0f * (float)ps;
+                }
             }
         } else {
-            // k-step (j, u): the lane's four values of sub-block j are 32j + 8t + 4u .. +3 (the
-            // MMA's k = 2t, 2t+1, 2t+8, 2t+9), matching the A fragments built below
+            // k-step (j, u): the lane's four values of sub-block j are 32j + 8t + 4u + i, i = 0, 2
+            // as the MMA's k = 2t, 2t+1 and i = 1, 3 as k = 2t+8, 2t+9, matching the A fragments
+            // built below (codes of bytes 0, 2 of a word, then of its bytes 1, 3)
             const int8_t *xv = a_src + (int64_t)g * K + 256 * blk + 8 * t;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const uint32_t w = have ? *reinterpret_cast<const uint32_t *>(xv + 32 * j + 4 * u) : 0u;
-                    bfr[4 * j + 2 * u] = s8x2_to_f16x2(w, 0x4140u);      // values 8t + 4u, +1
-                    bfr[4 * j + 2 * u + 1] = s8x2_to_f16x2(w, 0x4342u);  // values +2, +3
+                    bfr[4 * j + 2 * u] = s8x2_to_f16x2(w, 0x4240u);      // values 8t + 4u, +2
+                    bfr[4 * j + 2 * u + 1] = s8x2_to_f16x2(w, 0x4341u);  // values +1, +3
                 }
         }
 #pragma unroll
@@ -362,8 +394,10 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
                                    (int)(int16_t)(bsv[e].w & 0xffff), bsv[e].w >> 16};
                 if (g == 0) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        bias[j * 8 + v] = -1024.0f * (float)s8[j];
+                    for (int j = 0; j < 8; ++j) {
+                        float *bq = bias + (j * 4 + t) * 4 + e;
+                        bq[0] = bq[2] = -1024.0f * (float)s8[j];
+                    }
                 }
             }
         }
@@ -429,9 +463,9 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
                     const uint32_t wB = ((qlB[qi] >> nsh) & 0x0F0F0F0Fu) | (((qhB[half] >> hsh) & 0x03030303u) << 4);
                     const uint32_t a[4] = {__byte_perm(wA, 0x64u, 0x4140u), __byte_perm(wB, 0x64u, 0x4140u),
                                            __byte_perm(wA, 0x64u, 0x4342u), __byte_perm(wB, 0x64u, 0x4342u)};
-                    const float2 bb = *reinterpret_cast<const float2 *>(bias + s * 8 + 2 * t);
+                    const float4 bb = *reinterpret_cast<const float4 *>(bias + (s * 4 + t) * 4);
                     float d[4];
-                    mma_16816_c(d, a, bfr[2 * s], bfr[2 * s + 1], bb.x, bb.y, bb.x, bb.y);
+                    mma_16816_c(d, a, bfr[2 * s], bfr[2 * s + 1], bb.x, bb.y, bb.z, bb.w);
                     // d holds the exact dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
                     const uint32_t wsA = s < 4 ? scA.x : s < 8 ? scA.y : s < 12 ? scA.z : scA.w;
                     const uint32_t wsB = s < 4 ? scB.x : s < 8 ? scB.y : s < 12 ? scB.z : scB.w;
@@ -488,73 +522,79 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
             }
             // Q4_K: sum_j sc_j * dot_j in f32 over each half block (sub-blocks 0..3, 4..7): every
             // product and partial sum is an integer of magnitude at most 4 * 63 * 15 * 127 * 32
-            // < 2^24, so the f32 fused multiply-adds are exact
-            float Sf[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half block: [row g v0, v1, g+8 v0, v1]
+            // < 2^24, so the f32 fused multiply-adds are exact, and the f32 sum of the two halves
+            // is S rounded to f32 once -- the value the epilogue converts S to.  Q5_K (codes up to
+            // 31) sums in int32.
+            float Sf[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};  // [half][g v0, v1, g+8 v0, v1]
+            const uint32_t k64 = k6400();
 #pragma unroll
             for (int cq = 0; cq < 4; ++cq) {  // 32-byte code chunk cq: sub-blocks 2cq (low), 2cq+1 (high)
                 float dlo[4], dhi[4];
-                const float2 blo = *reinterpret_cast<const float2 *>(bias + (2 * cq) * 8 + 2 * t);
-                const float2 bhi = *reinterpret_cast<const float2 *>(bias + (2 * cq + 1) * 8 + 2 * t);
+                const float4 blo = *reinterpret_cast<const float4 *>(bias + ((2 * cq) * 4 + t) * 4);
+                const float4 bhi = *reinterpret_cast<const float4 *>(bias + ((2 * cq + 1) * 4 + t) * 4);
                 const uint2 cA = *reinterpret_cast<const uint2 *>(rowA + QS_OFF + 32 * cq + 8 * t);
                 const uint2 cB = *reinterpret_cast<const uint2 *>(rowB + QS_OFF + 32 * cq + 8 * t);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
+                    // bytes 8t + 4u + i: values +0, +2 from the word itself, +1, +3 from it shifted
+                    // by a byte; low nibbles as 1024 + n, high nibbles as 1024 + 16 n (their dots
+                    // come out 16-fold, which the high scale's 1/16 takes back)
                     const uint32_t wA = u ? cA.y : cA.x, wB = u ? cB.y : cB.x;
-                    uint32_t loA = wA & 0x0F0F0F0Fu, loB = wB & 0x0F0F0F0Fu;
-                    uint32_t hiA = (wA >> 4) & 0x0F0F0F0Fu, hiB = (wB >> 4) & 0x0F0F0F0Fu;
+                    const uint32_t sA = wA >> 8, sB = wB >> 8;
+                    uint32_t alo[4] = {nib_f16x2<0x000F000Fu>(wA, k64), nib_f16x2<0x000F000Fu>(wB, k64),
+                                       nib_f16x2<0x000F000Fu>(sA, k64), nib_f16x2<0x000F000Fu>(sB, k64)};
+                    uint32_t ahi[4] = {nib_f16x2<0x00F000F0u>(wA, k64), nib_f16x2<0x00F000F0u>(wB, k64),
+                                       nib_f16x2<0x00F000F0u>(sA, k64), nib_f16x2<0x00F000F0u>(sB, k64)};
                     if (Q5) {
+                        // bit 4 of byte i of the rotated fifth-bit words is value +i's fifth bit:
+                        // 16 in a low code (f16 bit 4), 256 in a 16-fold high code (f16 bit 8)
                         const uint32_t qA = u ? qhA.y : qhA.x, qB = u ? qhB.y : qhB.x;
                         const int rl = (2 * cq - 4) & 31, rh = (2 * cq - 3) & 31;
-                        loA |= __funnelshift_r(qA, qA, rl) & 0x10101010u;
-                        loB |= __funnelshift_r(qB, qB, rl) & 0x10101010u;
-                        hiA |= __funnelshift_r(qA, qA, rh) & 0x10101010u;
-                        hiB |= __funnelshift_r(qB, qB, rh) & 0x10101010u;
+                        const uint32_t lA = __funnelshift_r(qA, qA, rl), lB = __funnelshift_r(qB, qB, rl);
+                        const uint32_t xA = __funnelshift_r(qA, qA, rh), xB = __funnelshift_r(qB, qB, rh);
+                        alo[0] |= lA & 0x00100010u;
+                        alo[1] |= lB & 0x00100010u;
+                        alo[2] |= (lA >> 8) & 0x00100010u;
+                        alo[3] |= (lB >> 8) & 0x00100010u;
+                        ahi[0] |= (xA << 4) & 0x01000100u;
+                        ahi[1] |= (xB << 4) & 0x01000100u;
+                        ahi[2] |= (xA >> 4) & 0x01000100u;
+                        ahi[3] |= (xB >> 4) & 0x01000100u;
                     }
-                    // codes as f16 1024 + n: rows g (A) and g+8 (B), bytes 0, 1 then 2, 3
-                    const uint32_t alo[4] = {__byte_perm(loA, 0x64u, 0x4140u), __byte_perm(loB, 0x64u, 0x4140u),
-                                             __byte_perm(loA, 0x64u, 0x4342u), __byte_perm(loB, 0x64u, 0x4342u)};
-                    const uint32_t ahi[4] = {__byte_perm(hiA, 0x64u, 0x4140u), __byte_perm(hiB, 0x64u, 0x4140u),
-                                             __byte_perm(hiA, 0x64u, 0x4342u), __byte_perm(hiB, 0x64u, 0x4342u)};
                     if (u == 0) {
-                        mma_16816_c(dlo, alo, bfr[8 * cq], bfr[8 * cq + 1], blo.x, blo.y, blo.x, blo.y);
-                        mma_16816_c(dhi, ahi, bfr[8 * cq + 4], bfr[8 * cq + 5], bhi.x, bhi.y, bhi.x, bhi.y);
+                        mma_16816_c(dlo, alo, bfr[8 * cq], bfr[8 * cq + 1], blo.x, blo.y, blo.z, blo.w);
+                        mma_16816_c(dhi, ahi, bfr[8 * cq + 4], bfr[8 * cq + 5], bhi.x, bhi.y, bhi.z, bhi.w);
                     } else {
                         mma_16816(dlo, alo, bfr[8 * cq + 2], bfr[8 * cq + 3]);
                         mma_16816(dhi, ahi, bfr[8 * cq + 6], bfr[8 * cq + 7]);
                     }
                 }
-                // dlo, dhi hold the exact integer dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
+                // dlo holds the exact dots, dhi 16 x the exact dots [row g: v 2t, 2t+1 | row g+8: v 2t, 2t+1]
                 const uint32_t wsA = cq < 2 ? scA0 : scA1, wsB = cq < 2 ? scB0 : scB1;
                 const uint32_t bl = 2 * (cq & 1), bh = bl + 1;
                 if (!Q5) {
-                    const float fAl = byte_as_float(wsA, bl), fAh = byte_as_float(wsA, bh);
-                    const float fBl = byte_as_float(wsB, bl), fBh = byte_as_float(wsB, bh);
-                    Sf[0] = __fmaf_rn(fAh, dhi[0], __fmaf_rn(fAl, dlo[0], Sf[0]));
-                    Sf[1] = __fmaf_rn(fAh, dhi[1], __fmaf_rn(fAl, dlo[1], Sf[1]));
-                    Sf[2] = __fmaf_rn(fBh, dhi[2], __fmaf_rn(fBl, dlo[2], Sf[2]));
-                    Sf[3] = __fmaf_rn(fBh, dhi[3], __fmaf_rn(fBl, dlo[3], Sf[3]));
-                    if (cq & 1) {  // a half block is complete: bank it as int32 (exact, below 2^24)
-                        S[0][0] += __float2int_rn(Sf[0]);
-                        S[0][1] += __float2int_rn(Sf[1]);
-                        S[1][0] += __float2int_rn(Sf[2]);
-                        S[1][1] += __float2int_rn(Sf[3]);
-                        Sf[0] = Sf[1] = Sf[2] = Sf[3] = 0.0f;
-                    }
+                    const float fAl = byte_as_float(wsA, bl), fAh = byte16th_as_float(wsA, bh);
+                    const float fBl = byte_as_float(wsB, bl), fBh = byte16th_as_float(wsB, bh);
+                    float *Sh = Sf[cq >> 1];
+                    Sh[0] = __fmaf_rn(fAh, dhi[0], __fmaf_rn(fAl, dlo[0], Sh[0]));
+                    Sh[1] = __fmaf_rn(fAh, dhi[1], __fmaf_rn(fAl, dlo[1], Sh[1]));
+                    Sh[2] = __fmaf_rn(fBh, dhi[2], __fmaf_rn(fBl, dlo[2], Sh[2]));
+                    Sh[3] = __fmaf_rn(fBh, dhi[3], __fmaf_rn(fBl, dlo[3], Sh[3]));
                 } else {
                     const uint32_t sl = 0x4440u | bl, sh = 0x4440u | bh;
                     const int sAl = (int)__byte_perm(wsA, 0u, sl), sAh = (int)__byte_perm(wsA, 0u, sh);
                     const int sBl = (int)__byte_perm(wsB, 0u, sl), sBh = (int)__byte_perm(wsB, 0u, sh);
-                    S[0][0] += sAl * exact_small_int(dlo[0]) + sAh * exact_small_int(dhi[0]);
-                    S[0][1] += sAl * exact_small_int(dlo[1]) + sAh * exact_small_int(dhi[1]);
-                    S[1][0] += sBl * exact_small_int(dlo[2]) + sBh * exact_small_int(dhi[2]);
-                    S[1][1] += sBl * exact_small_int(dlo[3]) + sBh * exact_small_int(dhi[3]);
+                    S[0][0] += sAl * exact_small_int(dlo[0]) + sAh * (exact_small_int(dhi[0]) >> 4);
+                    S[0][1] += sAl * exact_small_int(dlo[1]) + sAh * (exact_small_int(dhi[1]) >> 4);
+                    S[1][0] += sBl * exact_small_int(dlo[2]) + sBh * (exact_small_int(dhi[2]) >> 4);
+                    S[1][1] += sBl * exact_small_int(dlo[3]) + sBh * (exact_small_int(dhi[3]) >> 4);
                 }
                 if (DUMP) {
                     int il[4], ih[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         il[i] = exact_small_int(dlo[i]);
-                        ih[i] = exact_small_int(dhi[i]);
+                        ih[i] = exact_small_int(dhi[i]) >> 4;
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -583,11 +623,11 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
                     M = __dp2a_hi(bsv[e].y, (int)m0, M);
                     M = __dp2a_lo(bsv[e].z, (int)m1, M);
                     M = __dp2a_hi(bsv[e].w, (int)m1, M);
-                    term[rr][e] = __fmul_rn(dxv[e], __fsub_rn(__fmul_rn(d, __int2float_rn(S[rr][e])),
-                                                              __fmul_rn(dmin, __int2float_rn(M))));
+                    const float fS = Q5 ? __int2float_rn(S[rr][e]) : __fadd_rn(Sf[0][2 * rr + e], Sf[1][2 * rr + e]);
+                    term[rr][e] = __fmul_rn(dxv[e], __fsub_rn(__fmul_rn(d, fS), __fmul_rn(dmin, __int2float_rn(M))));
                     if (DUMP && row < nr && 2 * t + e < B) {
                         int32_t *sm = p.dbg_sm + (((2 * t + e) * p.rows + rs + row) * nb + blk) * 2;
-                        sm[0] = S[rr][e];
+                        sm[0] = Q5 ? S[rr][e] : __float2int_rn(Sf[0][2 * rr + e]) + __float2int_rn(Sf[1][2 * rr + e]);
                         sm[1] = M;
                     }
                 }
