@@ -301,11 +301,13 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // blocks at 5..8 vectors (below 5 the dp4a kernel is faster; Q6_K's 14336-wide down
     // projection takes 26.9 us against 26.2 on dp4a at 8 vectors) -- and for rows the dp4a
     // kernel cannot take (more than 128 blocks at one or two vectors, 64 above), which it walks
-    // run by run.  One warp per block of a run of 16 blocks, each with its own ring of 16-row
-    // tiles; about 16 warps per SM, with the deepest ring (3 or 4 tiles per warp) that fits
-    // beside the run sums (and, fused, the packed activations).  A forced ring cap below 3
-    // selects the dp4a kernel, and so does a shape that does not fit.  The RMSNorm form exists
-    // in the row-lane and dp4a kernels, not in this one.
+    // run by run.  One warp per block of a run of 16 blocks, each with its own ring of tiles;
+    // about 16 warps per SM.  Tiles of 32 rows (rings of 2) where that gives no CTA more rows
+    // than tiles of 16 do and the rings fit (not Q6_K), else tiles of 16 rows with the deepest
+    // ring (3 or 4 tiles per warp) that fits beside the run sums (and, fused, the packed
+    // activations).  A forced ring cap of 2 asks for 32-row tiles, of 3 or more caps the 16-row
+    // ring, of 1 selects the dp4a kernel, and so does a shape that does not fit.  The RMSNorm
+    // form exists in the row-lane and dp4a kernels, not in this one.
     const int fst = g_force_stages.load();
     pl->tc_rows = 0;
     // One or two vectors: the row-lane kernel, unless a test flag asks for another kernel (three
@@ -318,32 +320,45 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);
     const bool tc_forced = (launch_flags() & LAUNCH_TC_ALL) && batch >= 3;
     if (!norm && (tc_faster || dp4a_cannot || tc_forced) && !(launch_flags() & LAUNCH_DP4A_ONLY) &&
-        (fst <= 0 || fst >= 3)) {
+        (fst <= 0 || fst >= 2)) {
         const int RW = nb < TC_RUN ? nb : TC_RUN;
-        const int64_t ntiles = (rows + TC_ROWS - 1) / TC_ROWS;
         int cps = g_force_cps.load() > 0 ? g_force_cps.load() : (16 / RW > 0 ? 16 / RW : 1);
         if (cps > 8)
             cps = 8;
         int st = 0;
         int64_t grid = 0, rows_pad = 0;
         for (; cps >= 1; --cps) {
-            grid = (int64_t)dev.sm_count * cps;
-            if (grid > ntiles)
-                grid = ntiles;
-            rows_pad = ((rows + grid - 1) / grid + TC_ROWS - 1) / TC_ROWS * TC_ROWS;
             int budget = dev.smem_per_sm / cps - 1024;
             if (budget > dev.smem_optin)
                 budget = dev.smem_optin;
+            // CTAs and rows per CTA for tiles of th rows: every CTA takes whole tiles
+            auto split = [&](int th, int64_t *g, int64_t *rp) {
+                const int64_t nt = (rows + th - 1) / th;
+                *g = (int64_t)dev.sm_count * cps < nt ? (int64_t)dev.sm_count * cps : nt;
+                *rp = (rows + th * *g - 1) / (th * *g) * th;
+            };
+            int64_t g16, rp16, g32, rp32;
+            split(TC_ROWS, &g16, &rp16);
+            split(2 * TC_ROWS, &g32, &rp32);
             st = 0;
-            if (rows_pad <= (1 << 16))
-                for (st = 4; st >= 3; --st)
-                    if ((fst <= 0 || st <= fst) &&
-                        qmv_tc_layout(st, fmt, nb, batch, fused, (int)rows_pad).total <= budget)
-                        break;
-            if (st >= 3)
+            const bool try32 = fmt != QMD_Q6_K_SPLIT && (fst == 2 || (fst <= 0 && rp32 <= rp16));
+            if (try32 && rp32 <= (1 << 16) && qmv_tc_layout(2, fmt, nb, batch, fused, (int)rp32).total <= budget) {
+                st = 2;
+                grid = g32;
+                rows_pad = rp32;
                 break;
+            }
+            if (fst != 2 && rp16 <= (1 << 16))
+                for (st = 4; st >= 3; --st)
+                    if ((fst <= 0 || st <= fst) && qmv_tc_layout(st, fmt, nb, batch, fused, (int)rp16).total <= budget)
+                        break;
+            if (st >= 3) {
+                grid = g16;
+                rows_pad = rp16;
+                break;
+            }
         }
-        if (cps >= 1 && st >= 3) {  // otherwise the dp4a kernel below takes the call
+        if (cps >= 1 && st >= 2) {  // otherwise the dp4a kernel below takes the call
             pl->layout = 1;
             pl->grid = (int)grid;
             pl->stages = st;
@@ -351,8 +366,8 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
             pl->smem = qmv_tc_layout(st, fmt, nb, batch, fused, (int)rows_pad).total;
             pl->WR = RW;
             pl->RG = 1;
-            pl->PR = TC_ROWS;
-            pl->stage_bytes = tc_slot_bytes(fmt);
+            pl->PR = tc_tile_rows(st);
+            pl->stage_bytes = tc_slot_bytes(fmt, tc_tile_rows(st));
             pl->tc_rows = (int)rows_pad;
             return QMD_OK;
         }

@@ -81,7 +81,7 @@ struct QmvPlan {
     int grid, threads, smem, stages;
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;
-    int tc_rows;  // tensor-core kernel: rows per CTA rounded up to 16 (sizes the run sums)
+    int tc_rows;  // tensor-core kernel: rows per CTA rounded up to its tile rows (sizes the run sums)
     int pre_steps = 0;  // row-lane kernel: ring slots per warp requested before the dependency wait
 };
 

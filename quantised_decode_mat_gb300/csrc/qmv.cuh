@@ -55,7 +55,7 @@ struct QmvKParams {
     int64_t rows;
     int nb, WR, RG, stages, row_bytes, pre_bytes, stage_bytes, row_stride;
     int batch;
-    int tc_rows;          // tensor-core kernel: rows per CTA rounded up to 16
+    int tc_rows;          // tensor-core kernel: rows per CTA rounded up to its tile rows
     int32_t *dbg_dots;
     int32_t *dbg_sm;
     const float *x;       // fused form: f32 activations [B][K], packed inside the kernel

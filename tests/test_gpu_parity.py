@@ -225,12 +225,13 @@ def test_sweep_shapes(fmtname, rows, K, batch):
                                                   ("q6k", 600, 3584, 1), ("q6k", 150, 7168, 2),
                                                   ("q6k", 90, 14336, 1), ("q5k", 1500, 4096, 1),
                                                   ("q5k", 300, 3072, 4), ("q4k", 900, 4096, 6)])
-@pytest.mark.parametrize("flags", [0, 8, 16], ids=["default", "slice", "rowlane"])
+@pytest.mark.parametrize("flags", [0, 8, 16, 4], ids=["default", "slice", "rowlane", "tensor"])
 def test_pipeline_plans(plan, fmtname, rows, K, batch, flags):
     """Force small stage rings (many wrap-arounds per CTA) and other CTA shapes: same bits.  For
     the row-lane kernel (batches 1 and 2 by default, 3 and 4 with flag 16) the plan's row groups
     are its warps per CTA and its stages the slots of each warp's ring; flag 8 runs the dp4a
-    slice kernel instead."""
+    slice kernel instead; flag 4 the tensor-core kernel from three vectors up (a ring cap of 2:
+    its 32-row tiles, 3 or more: 16-row tiles in rings of at most that many)."""
     q.debug_set_plan(*plan)
     q.debug_set_launch_flags(flags)
     try:
@@ -467,12 +468,16 @@ def test_tensor_core_path_equals_dp4a_path(fmtname, batch, rows, K):
     check_against_oracle(fmtname, Wg, x, y_tc, rows_idx=idx)
 
 
+@pytest.mark.parametrize("tile32", [False, True], ids=["tile16", "tile32"])
 @pytest.mark.parametrize("fmtname,K", [("q4k", 4096), ("q5k", 4096), ("q4k", 8192), ("q6k", 4096),
                                        ("q6k", 14336)])
-def test_tensor_core_extreme_magnitudes(fmtname, K):
+def test_tensor_core_extreme_magnitudes(fmtname, K, tile32):
     """The largest codes and scales against activations of +-127: the accumulator's partial
     sums reach their bound, and the integer dots must still be exact (Q6_K: scales -128 and
-    127, codes 63 and 0, so a two-sub-block sum of scaled dots reaches 2 x 128 x 16 x 32 x 127)."""
+    127, codes 63 and 0, so a two-sub-block sum of scaled dots reaches 2 x 128 x 16 x 32 x 127).
+    tile32: Q4_K / Q5_K in 32-row tiles (a ring cap of 2), rows 0-31 in one tile."""
+    if tile32 and fmtname == "q6k":
+        pytest.skip("Q6_K takes 16-row tiles only")
     rows, batch = 48, 8
     Wg = synth.weights(fmtname, 77, rows, K).copy()
     if fmtname == "q6k":
@@ -492,8 +497,11 @@ def test_tensor_core_extreme_magnitudes(fmtname, K):
     x[2, ::3] = -1.0                       # mixed signs
     x[4] = synth.activations(78, 1, K)[0]
     q.debug_set_launch_flags(TC_ALL)
+    if tile32:
+        q.debug_set_plan(0, 0, 2, 0)
     try:
         assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_tc_kernel"
+        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == (32 if tile32 else 16)
         y = run_matvec(fmtname, Wg, gpu_pack(x), rows, K, batch)
         if fmtname == "q6k":
             body, prefix = q.bind_q6k(dev(Wg.reshape(rows, -1)), rows, K)
@@ -503,6 +511,7 @@ def test_tensor_core_extreme_magnitudes(fmtname, K):
         q.get_device_error()
     finally:
         q.debug_set_launch_flags(0)
+        q.debug_set_plan()
     check_against_oracle(fmtname, Wg, x, y)
     oqs, _, _ = O.q8k_pack(x)
     dots = dots.cpu().numpy()
