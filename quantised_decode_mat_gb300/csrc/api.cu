@@ -298,10 +298,10 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->pre_bytes = pre_bytes;
     pl->row_stride = row_bytes;
     // Tensor-core kernel.  Chosen where it was measured faster -- Q4_K / Q5_K rows of at most 16
-    // blocks at 5..8 vectors (below 5 the dp4a kernel is faster; Q6_K's 14336-wide down
-    // projection takes 26.9 us against 26.2 on dp4a at 8 vectors) -- and for rows the dp4a
-    // kernel cannot take (more than 128 blocks at one or two vectors, 64 above), which it walks
-    // run by run.  One warp per block of a run of 16 blocks, each with its own ring of tiles;
+    // blocks at 5..8 vectors, and at 3..4 where its 32-row tiles give every CTA many rows (Q6_K's
+    // 14336-wide down projection: 24.4 us against 24.9 on dp4a at 8 vectors, kept on dp4a) --
+    // and for rows the dp4a kernel cannot take (more than 128 blocks at one or two vectors, 64
+    // above), which it walks run by run.  One warp per block of a run of 16 blocks, each with its own ring of tiles;
     // about 16 warps per SM.  Tiles of 32 rows (rings of 2) where that gives no CTA more rows
     // than tiles of 16 do and the rings fit (not Q6_K), else tiles of 16 rows with the deepest
     // ring (3 or 4 tiles per warp) that fits beside the run sums (and, fused, the packed
@@ -316,7 +316,19 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (rl_batch && !(launch_flags() & (LAUNCH_SLICE | LAUNCH_TC_ALL)) &&
         rl_plan(fmt, rows, nb, batch, dev, pl, mode == QMV_NORM))
         return QMD_OK;
-    const bool tc_faster = batch >= TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
+    // Three and four vectors: the tensor cores only where 32-row tiles give every CTA many rows
+    // (measured on the 7B shapes: gate|up 18.5 against 20.3 us on dp4a at four vectors; q|k|v
+    // 7.7 against 6.8 and o 5.3 against 5.3, whose CTAs have 27-40 rows)
+    bool tall = false;
+    if (batch >= TC_MIN_BATCH_TALL && batch < TC_MIN_BATCH && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT) {
+        const int rw = nb < TC_RUN ? nb : TC_RUN;
+        const int64_t cta = (int64_t)dev.sm_count * (16 / rw > 0 ? 16 / rw : 1);
+        const int64_t t16 = (rows + TC_ROWS - 1) / TC_ROWS, t32 = (rows + 2 * TC_ROWS - 1) / (2 * TC_ROWS);
+        const int64_t g16 = cta < t16 ? cta : t16, g32 = cta < t32 ? cta : t32;
+        const int64_t rp16 = (t16 + g16 - 1) / g16 * TC_ROWS, rp32 = (t32 + g32 - 1) / g32 * 2 * TC_ROWS;
+        tall = rp32 <= rp16 && rp32 >= TC_TALL_ROWS;
+    }
+    const bool tc_faster = (batch >= TC_MIN_BATCH || tall) && nb <= TC_RUN && fmt != QMD_Q6_K_SPLIT;
     const bool dp4a_cannot = nb > (batch <= 2 ? 128 : 64);
     const bool tc_forced = (launch_flags() & LAUNCH_TC_ALL) && batch >= 3;
     if (!norm && (tc_faster || dp4a_cannot || tc_forced) && !(launch_flags() & LAUNCH_DP4A_ONLY) &&

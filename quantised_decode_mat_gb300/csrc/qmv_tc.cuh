@@ -57,9 +57,11 @@
 namespace qmd {
 
 constexpr int TC_ROWS = 16;      // rows per MMA sub-tile (the MMA's M)
-constexpr int TC_RED = 2;        // tiles whose block terms can be pending at once
+constexpr int TC_RED = 3;        // tiles whose block terms can be pending at once
 constexpr int TC_RUN = 16;       // blocks per run (warps per CTA at most)
-constexpr int TC_MIN_BATCH = 5;  // smallest batch the plan gives to this kernel for rows the dp4a kernel can take
+constexpr int TC_MIN_BATCH = 5;  // smallest batch the plan gives to this kernel for rows the dp4a kernel can take,
+constexpr int TC_MIN_BATCH_TALL = 3;  // and for many rows a CTA in 32-row tiles (at least TC_TALL_ROWS)
+constexpr int TC_TALL_ROWS = 64;
 
 __host__ __device__ constexpr int tc_block_bytes(int fmt)
 {

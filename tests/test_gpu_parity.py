@@ -468,16 +468,47 @@ def test_tensor_core_path_equals_dp4a_path(fmtname, batch, rows, K):
     check_against_oracle(fmtname, Wg, x, y_tc, rows_idx=idx)
 
 
+@pytest.mark.parametrize("batch", [3, 4])
+@pytest.mark.parametrize("fmtname,rows,K", [("q4k", 9728, 4096), ("q4k", 28672, 4096), ("q5k", 19456, 2048),
+                                            ("q4k", 10000, 4096), ("q4k", 6144, 4096)])
+def test_tensor_cores_for_tall_tiles_at_three_and_four(fmtname, rows, K, batch):
+    """Three and four vectors go to the tensor cores where 32-row tiles give every CTA at least
+    64 rows and no more rows than 16-row tiles would (gate|up-like shapes), else to the dp4a
+    kernel (q|k|v-like): the same bits either way."""
+    seed = rows + K + batch
+    Wg = synth.weights(fmtname, seed, rows, K)
+    x = synth.activations(seed, batch, K)
+    xq = gpu_pack(x)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ctas = sms * max(16 // min(K // 256, 16), 1)
+    per_cta = lambda th: -(-(-(-rows // th)) // min(ctas, -(-rows // th))) * th  # whole tiles per CTA
+    tall = per_cta(32) <= per_cta(16) and per_cta(32) >= 64
+    kern = q.launch_kernel(QFMT[fmtname], rows, K, batch)
+    assert kern == ("qmv_tc_kernel" if tall else "qmv_kernel")
+    if tall and fmtname == "q4k":  # (Q5_K's two-slot rings of 32-row tiles do not fit: 16-row tiles)
+        assert q.launch_info(QFMT[fmtname], rows, K, batch)["rows_per_stage"] == 32
+    y = run_matvec(fmtname, Wg, xq, rows, K, batch)
+    q.debug_set_launch_flags(DP4A_ONLY)
+    try:
+        assert q.launch_kernel(QFMT[fmtname], rows, K, batch) == "qmv_kernel"
+        y_dp = run_matvec(fmtname, Wg, xq, rows, K, batch)
+    finally:
+        q.debug_set_launch_flags(0)
+    assert np.array_equal(y.view(np.uint32), y_dp.view(np.uint32))
+    check_against_oracle(fmtname, Wg, x, y, rows_idx=_sample_rows(rows, 64, seed))
+
+
 @pytest.mark.parametrize("tile32", [False, True], ids=["tile16", "tile32"])
-@pytest.mark.parametrize("fmtname,K", [("q4k", 4096), ("q5k", 4096), ("q4k", 8192), ("q6k", 4096),
-                                       ("q6k", 14336)])
+@pytest.mark.parametrize("fmtname,K", [("q4k", 4096), ("q5k", 4096), ("q5k", 2048), ("q4k", 8192),
+                                       ("q6k", 4096), ("q6k", 14336)])
 def test_tensor_core_extreme_magnitudes(fmtname, K, tile32):
     """The largest codes and scales against activations of +-127: the accumulator's partial
     sums reach their bound, and the integer dots must still be exact (Q6_K: scales -128 and
     127, codes 63 and 0, so a two-sub-block sum of scaled dots reaches 2 x 128 x 16 x 32 x 127).
-    tile32: Q4_K / Q5_K in 32-row tiles (a ring cap of 2), rows 0-31 in one tile."""
-    if tile32 and fmtname == "q6k":
-        pytest.skip("Q6_K takes 16-row tiles only")
+    tile32: Q4_K / Q5_K in 32-row tiles (a ring cap of 2), rows 0-31 in one tile (Q5_K's rings
+    of 16 such tiles do not fit beside 16 warps' term slots: 8 blocks there)."""
+    if tile32 and (fmtname == "q6k" or (fmtname == "q5k" and K > 2048)):
+        pytest.skip("16-row tiles only for this format and width")
     rows, batch = 48, 8
     Wg = synth.weights(fmtname, 77, rows, K).copy()
     if fmtname == "q6k":
