@@ -410,8 +410,9 @@ void qmd_debug_set_plan(int row_groups, int rows_per_stage, int max_stages, int 
  * kernel would be chosen; bit 2 computes every batch of 3..8 vectors with the tensor-core
  * kernel where it fits (rows of more than 16 blocks run by run); bit 3 keeps one and two vectors
  * off the row-lane kernel (the dp4a slice kernel, or the tensor-core kernel for rows the slice
- * kernel cannot take); bit 4 puts three and four vectors on the row-lane kernel as well.  Results
- * are the same either way.  Process-wide.
+ * kernel cannot take); bit 4 puts three and four vectors on the row-lane kernel as well; bit 5
+ * gives the row-lane kernel rings up to 4 deep for one vector and rows of at most 16 blocks too
+ * (its plan keeps them at 2 there).  Results are the same either way.  Process-wide.
  */
 void qmd_debug_set_launch_flags(unsigned flags);
 

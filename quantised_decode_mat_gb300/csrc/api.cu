@@ -232,9 +232,10 @@ static bool fit_stages(const DeviceInfo &dev, int64_t rows, int TR, int stage_by
 }
 
 // Row-lane kernel (qmv_rl.cuh): one CTA per SM (more when forced), a ring for as many warps as
-// the CTA has 2-row tiles up to 16, the deepest ring (up to 4 steps per warp, no more than a warp
-// has steps) that fits beside the activations, up to 16 warps to pack them, and one more warp
-// that requests the rings' first fills.  false if nothing fits (very long rows).
+// the CTA has 2-row tiles up to 16, the deepest ring (up to 4 steps per warp -- 2 for one vector
+// and rows of one step -- no more than a warp has steps) that fits beside the activations, up to
+// 16 warps to pack them, and one more warp that requests the rings' first fills.  false if
+// nothing fits (very long rows).
 static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, bool norm)
 {
     const int64_t tiles = (rows + RL_ROWS - 1) / RL_ROWS;
@@ -245,6 +246,12 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
         grid = tiles;
     const int64_t per_cta = (tiles + grid - 1) / grid;
     const int wmax = rl_max_warps(batch);
+    // One vector and rows of one step (at most 16 blocks): rings of 2.  Measured on the 32-layer
+    // step (gate|up is the projection it changes; q|k|v and o have 1-2 steps a warp): 4357 ->
+    // 4553 GB/s; rings of 1 4331.  (An 8-warp CTA for q|k|v and o with every slot requested
+    // before the wait, faster in chains of one projection, lost in the step: 4430-4542.)
+    const bool forced = g_force_rg.load() > 0 || g_force_stages.load() > 0 || g_force_rows.load() > 0;
+    const bool ring2 = batch == 1 && nsteps == 1 && !norm && !forced && !(launch_flags() & LAUNCH_RL_DEEP);
     int W = g_force_rg.load() > 0 ? g_force_rg.load() : (int)(per_cta < wmax ? per_cta : wmax);
     if (W > wmax)
         W = wmax;
@@ -254,7 +261,7 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     if (budget > dev.smem_optin)
         budget = dev.smem_optin;
     const int64_t steps = (per_cta + W - 1) / W * nsteps;  // most steps a warp has
-    int S = g_force_stages.load() > 0 ? g_force_stages.load() : 4;
+    int S = g_force_stages.load() > 0 ? g_force_stages.load() : ring2 ? 2 : 4;
     if (S > steps)
         S = (int)steps;
     for (; S >= 1; --S)

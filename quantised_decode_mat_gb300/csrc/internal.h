@@ -37,7 +37,14 @@ uint64_t wait_limit_ns();
 // the tensor-core kernel for every batch of 3..8; bit 3: the dp4a slice kernel instead of the
 // row-lane kernel; bit 4: the row-lane kernel for batches of 3 and 4 as well).
 unsigned launch_flags();
-enum : unsigned { LAUNCH_NO_PDL = 1u, LAUNCH_DP4A_ONLY = 2u, LAUNCH_TC_ALL = 4u, LAUNCH_SLICE = 8u, LAUNCH_RL = 16u };
+enum : unsigned {
+    LAUNCH_NO_PDL = 1u,
+    LAUNCH_DP4A_ONLY = 2u,
+    LAUNCH_TC_ALL = 4u,
+    LAUNCH_SLICE = 8u,
+    LAUNCH_RL = 16u,
+    LAUNCH_RL_DEEP = 32u,  // row-lane plan: rings up to 4 deep for one vector and one-step rows too
+};
 
 #ifdef QMD_TRACE
 // Traced build: the stamp records for the next launch of `ctas` CTAs (QMD_TRACE_FIELDS each), or
