@@ -56,6 +56,7 @@ constexpr int RL_POOLS = 8;          // claim pools of the scheduling workspace 
 constexpr int RL_WS_STRIDE = 64;     // words between the workspace's counters (256 bytes: separate L2 lines)
 static_assert(RL_WS_STRIDE * (RL_POOLS + 1) * 4 <= QMD_WORKSPACE_BYTES, "the pools' counters and the done word");
 constexpr int RL_PRE_STEPS = 2;   // default ring slots per warp requested before the dependency wait
+constexpr int RL_FEW_TILES = 32;  // a one-vector launch with at most this many tiles per CTA requests one
 
 __host__ __device__ constexpr int rl_block_bytes(int f) { return f == QMD_Q6_K_SPLIT ? 208 : f == QMD_Q5_K ? 176 : 144; }
 __host__ __device__ constexpr int rl_box_bytes(int f) { return RL_ROWS * RL_BLOCKS * rl_block_bytes(f); }

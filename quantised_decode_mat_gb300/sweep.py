@@ -3,6 +3,7 @@
     python -m quantised_decode_mat_gb300.sweep [--projection down] [--batch 1] [--layers 8]
         [--warps 8,12,16] [--stages 1,2,3,4] [--pre 1,2,3] [--reps 20]
     python -m quantised_decode_mat_gb300.sweep --step-flags 0,32 [--batch 1] [--layers 32]
+    python -m quantised_decode_mat_gb300.sweep --in-step --projection down [--layers 32] [grid as above]
 
 Makes the decode step of `--layers` layers as bench.py does and, for the default plan and then
 every forced plan of the grid (qmd_debug_set_plan: ring warps per CTA, ring slots per warp, and
@@ -15,7 +16,10 @@ Every forced plan's outputs are compared with the default plan's, bit for bit.
 
 With --step-flags, the whole step (every projection, in the step's launch forms) is captured
 once per value of qmd_debug_set_launch_flags and the graphs are timed in turn, three rounds
-interleaved, 200 replays each; printed as GB/s over the step's algorithmic bytes.
+interleaved, 200 replays each; printed as GB/s over the step's algorithmic bytes.  With
+--in-step, the grid of plans is applied to the chosen projection's launches only, inside the
+whole step (a plan is fixed when a launch is captured, so the other projections keep their
+default plans), each plan's step timed the same way.
 """
 from __future__ import annotations
 
@@ -38,6 +42,7 @@ def main(argv=None) -> int:
     ap.add_argument("--pre", default="1,2,3")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--step-flags", default=None, help="time the whole step under each of these launch-flag values")
+    ap.add_argument("--in-step", action="store_true", help="force the plans on one projection inside the whole step")
     args = ap.parse_args(argv)
 
     import torch
@@ -78,6 +83,8 @@ def main(argv=None) -> int:
         for fl, v in res.items():
             print(f"| {fl} | " + ", ".join(f"{x:.0f}" for x in v) + " |")
         return 0
+    if args.in_step:
+        return _in_step(args, st, torch)
     ps = [p for p in st.projs if p.name == args.projection]
     alg = sum(p.algorithmic_bytes() for p in ps) / len(ps)
 
@@ -134,6 +141,70 @@ def main(argv=None) -> int:
     if rows:
         best = min(rows)
         print(f"\nfastest forced plan: {best[1]} warps, {best[2]} slots, {best[3]} before the wait: {best[0]:.2f} µs")
+    return 0
+
+
+def _launch(p, ws):
+    from . import q8k_pack, qmatvec, qmatvec_x
+    if p.fused:
+        qmatvec_x(p.fmt, p.W, p.W_aux, p.x, p.y, p.rows, workspace=ws)
+    else:
+        q8k_pack(p.x, p.xq)
+        qmatvec(p.fmt, p.W, p.W_aux, p.xq, p.y, p.rows, workspace=ws)
+
+
+def _in_step(args, st, torch) -> int:
+    """The whole step with the grid's plans forced on one projection's launches only."""
+    from . import debug_set_plan, get_device_error, launch_info
+    nbytes = st.bytes()["algorithmic"]
+    p0 = [p for p in st.projs if p.name == args.projection][0]
+    plans = [None] + [(w, pre, s) for w, s, pre in itertools.product(_ints(args.warps), _ints(args.stages),
+                                                                      _ints(args.pre)) if pre <= s]
+
+    def capture(plan):
+        def run():
+            try:
+                for p in st.projs:
+                    if plan is not None and p.name == args.projection:
+                        debug_set_plan(plan[0], plan[1], plan[2], 0)
+                    else:
+                        debug_set_plan()
+                    _launch(p, st.ws)
+            finally:
+                debug_set_plan()
+        return st.capture(run)
+
+    graphs, used = {}, {}
+    for plan in plans:
+        if plan is not None:
+            debug_set_plan(plan[0], plan[1], plan[2], 0)
+        info = launch_info(p0.fmt, p0.rows, p0.K, args.batch)
+        debug_set_plan()
+        used[plan] = f"{info['grid']} x {info['threads']}, {info['stages']}"
+        graphs[plan] = capture(plan)
+    res = {plan: [] for plan in plans}
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        for plan, g in graphs.items():
+            for _ in range(5):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(100):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[plan].append(nbytes / (e0.elapsed_time(e1) / 100 * 1e-3) / 1e9)
+    get_device_error()
+    print(f"{args.layers}-layer step, batch {args.batch}, plans forced on {args.projection} only "
+          f"({p0.rows} x {p0.K}), {nbytes / 1e9:.3f} GB a step")
+    print()
+    print("| plan on it (warps, slots, before wait) | used: grid x threads, slots | step GB/s, three rounds |")
+    print("|---|---|---|")
+    for plan in plans:
+        name = "default" if plan is None else f"{plan[0]}, {plan[2]}, {plan[1]}"
+        print(f"| {name} | {used[plan]} | " + ", ".join(f"{x:.0f}" for x in res[plan]) + " |")
     return 0
 
 
