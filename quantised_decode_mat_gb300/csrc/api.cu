@@ -394,6 +394,11 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
             pl->PR = tc_tile_rows(st);
             pl->stage_bytes = tc_slot_bytes(fmt, tc_tile_rows(st));
             pl->tc_rows = (int)rows_pad;
+            // one ring slot per warp requested before the dependency wait, the rest once the
+            // warp's activation fragments are loaded (the fragments' loads otherwise arrive behind
+            // every SM's pre-wait copies): 32-layer step at 8 / 4 vectors 2137 / 2774 GB/s with
+            // the whole ring before the wait, 2159 / 2851 with one slot, 2018 / 2705 with none
+            pl->pre_steps = 1;
             return QMD_OK;
         }
     }

@@ -89,7 +89,7 @@ struct QmvPlan {
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;
     int tc_rows;  // tensor-core kernel: rows per CTA rounded up to its tile rows (sizes the run sums)
-    int pre_steps = 0;  // row-lane kernel: ring slots per warp requested before the dependency wait
+    int pre_steps = 0;  // row-lane, tensor-core kernels: ring slots per warp requested before the dependency wait
 };
 
 // Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.

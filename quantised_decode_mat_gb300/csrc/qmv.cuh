@@ -70,7 +70,7 @@ struct QmvKParams {
     unsigned long long wait_ns;
     unsigned *ws;         // row-lane kernel: the scheduling workspace (two counters), or NULL
     int64_t dyn_tiles;    // row-lane kernel with a workspace: the last tiles, handed out by claims
-    int pre_steps;        // row-lane kernel: ring slots per warp requested before the dependency wait
+    int pre_steps;        // row-lane, tensor-core kernels: ring slots per warp requested before the dependency wait
 #ifdef QMD_TRACE
     unsigned long long *trace;  // traced build: QMD_TRACE_FIELDS time stamps per CTA, or NULL
 #endif

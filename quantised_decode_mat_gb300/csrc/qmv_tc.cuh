@@ -37,7 +37,8 @@
 // constants, and per 16-row MMA sub-tile computes the block term of rows g and g+8 for vectors
 // 2t and 2t+1.  Each warp streams its own column (the tile's rows x one block, plus the rows'
 // f16 scales for Q6_K) through a private ring of STAGES slots: one tensor copy (TMA) per tile
-// and operand, issued by lane 0 and completing on the slot's mbarrier.  The rows land dense
+// and operand, issued by lane 0 and completing on the slot's mbarrier (p.pre_steps slots before
+// the dependency wait, the rest once the warp's activation fragments are loaded).  The rows land dense
 // (144, 176 or 208 bytes apart), which keeps every fragment load at its minimum number of
 // shared-memory wavefronts: the eight rows g of a load start 4, 12 or 20 banks apart.  CTAs take
 // whole tiles.
@@ -260,6 +261,14 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
     volatile int *s_done = reinterpret_cast<volatile int *>(smem + L.done_off);
     float *s_run = reinterpret_cast<float *>(smem + L.run_off);
     const uint64_t pol = policy_evict_first();
+#ifdef QMD_TRACE
+    if (tid == 0 && p.trace) {
+        p.trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS] = globaltimer_ns();
+        p.trace[(size_t)blockIdx.x * QMD_TRACE_FIELDS + 7] =
+            (unsigned long long)smid() | ((unsigned long long)blockIdx.x << 16) |
+            ((unsigned long long)gridDim.x << 32) | ((unsigned long long)(PACK ? 1 : 2) << 48);
+    }
+#endif
     if (runs > 1 && nt * TH > p.tc_rows) {  // more rows than the run-sum buffer was sized for
         pdl_wait();  // so that a kernel launched after this one still finds its predecessor done
         if (tid == 0)
@@ -309,12 +318,17 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
         fence_barrier_init();
 #pragma unroll
         for (int T = 0; T < STAGES; ++T)
-            issue(T);
+            if (T < p.pre_steps)
+                issue(T);
     }
     __syncthreads();
 
     pdl_launch_dependents();
+    if (tid == 0)
+        QMD_STAMP(p, 1);
     pdl_wait();  // activations come from earlier work in the stream
+    if (tid == 0)
+        QMD_STAMP(p, 2);
 
     const int64_t K = (int64_t)nb * 256;
     const int8_t *a_src = p.xqs;
@@ -382,11 +396,15 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
             // as the MMA's k = 2t, 2t+1 and i = 1, 3 as k = 2t+8, 2t+9, matching the A fragments
             // built below (codes of bytes 0, 2 of a word, then of its bytes 1, 3)
             const int8_t *xv = a_src + (int64_t)g * K + 256 * blk + 8 * t;
+            uint2 xw[8];  // the lane's eight bytes of each 32-value sub-block, all loads first
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                xw[j] = have ? *reinterpret_cast<const uint2 *>(xv + 32 * j) : make_uint2(0u, 0u);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint32_t w = have ? *reinterpret_cast<const uint32_t *>(xv + 32 * j + 4 * u) : 0u;
+                    const uint32_t w = u ? xw[j].y : xw[j].x;
                     bfr[4 * j + 2 * u] = s8x2_to_f16x2(w, 0x4240u);      // values 8t + 4u, +2
                     bfr[4 * j + 2 * u + 1] = s8x2_to_f16x2(w, 0x4341u);  // values +1, +3
                 }
@@ -420,6 +438,11 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
     int run_nb = MULTI ? 0 : nb, blk = warp;
     if (!MULTI)
         load_run(warp);
+    if (lane == 0)  // the rest of the ring, after the activations are in registers
+        for (int T = p.pre_steps; T < STAGES; ++T)
+            issue(T);
+    if (tid == 0)
+        QMD_STAMP(p, 3);
 #pragma unroll 1
     for (int T = 0; T < ntot; ++T) {
         const int r = MULTI ? T / nt : 0, c = MULTI ? T - r * nt : T;
@@ -439,6 +462,8 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
             return;
         }
         const int64_t rs0 = r0 + (int64_t)c * TH;  // the tile's first row
+        if (T == 0 && tid == 0)
+            QMD_STAMP(p, 4);
 
         // the tile's term slot must have been summed for tile T - TC_RED (bounded wait; the clock
         // is read every 16th poll)
@@ -757,9 +782,17 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
                 if (MULTI && !final_run)  // finishers of one row tile's runs may overlap
                     atomicAdd(const_cast<int *>(&s_done[c]), 1);
                 s_fin[rslot] = T;
+#ifdef QMD_TRACE
+                if (final_run && p.trace)
+                    atomicMax(p.trace + (size_t)blockIdx.x * QMD_TRACE_FIELDS + 5, globaltimer_ns());
+#endif
             }
         }
     }
+#ifdef QMD_TRACE
+    if (lane == 0 && p.trace)
+        atomicMax(p.trace + (size_t)blockIdx.x * QMD_TRACE_FIELDS + 6, globaltimer_ns());
+#endif
     // every tile a warp copies it also consumes, so no copy is in flight here
 }
 
