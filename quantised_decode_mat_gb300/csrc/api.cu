@@ -316,7 +316,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     // and for rows the dp4a kernel cannot take (more than 128 blocks at one or two vectors, 64
     // above), which it walks run by run.  One warp per block of a run of 16 blocks, each with its own ring of tiles;
     // about 16 warps per SM.  Tiles of 32 rows (rings of 2) where that gives no CTA more rows
-    // than tiles of 16 do and the rings fit (not Q6_K), else tiles of 16 rows with the deepest
+    // than tiles of 16 do and the rings fit (rows of one run, not Q6_K), else tiles of 16 rows with the deepest
     // ring (3 or 4 tiles per warp) that fits beside the run sums (and, fused, the packed
     // activations).  A forced ring cap of 2 asks for 32-row tiles, of 3 or more caps the 16-row
     // ring, of 1 selects the dp4a kernel, and so does a shape that does not fit.  The RMSNorm
@@ -366,7 +366,7 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
             split(TC_ROWS, &g16, &rp16);
             split(2 * TC_ROWS, &g32, &rp32);
             st = 0;
-            const bool try32 = fmt != QMD_Q6_K_SPLIT && (fst == 2 || (fst <= 0 && rp32 <= rp16));
+            const bool try32 = fmt != QMD_Q6_K_SPLIT && nb <= TC_RUN && (fst == 2 || (fst <= 0 && rp32 <= rp16));
             if (try32 && rp32 <= (1 << 16) && qmv_tc_layout(2, fmt, nb, batch, fused, (int)rp32).total <= budget) {
                 st = 2;
                 grid = g32;

@@ -869,9 +869,10 @@ qmd_status launch_qmv_tc(const QmvKParams &kp, const QmvPlan &plan, int mode, cu
     if (st != QMD_OK)
         return st;
     switch (plan.stages) {
-    case 2:  // 32-row tiles (Q6_K's two-slot rings of them do not fit beside 16 warps)
+    case 2:  // 32-row tiles, rows of one run (Q6_K's two-slot rings of them do not fit beside 16 warps)
         if constexpr (F != QMD_Q6_K_SPLIT)
-            return multi ? launch_tc_stages<F, 2, true>(tp, plan, mode, s) : launch_tc_stages<F, 2, false>(tp, plan, mode, s);
+            if (!multi)
+                return launch_tc_stages<F, 2, false>(tp, plan, mode, s);
         break;
     case 3:
         return multi ? launch_tc_stages<F, 3, true>(tp, plan, mode, s) : launch_tc_stages<F, 3, false>(tp, plan, mode, s);
