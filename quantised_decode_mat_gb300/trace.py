@@ -92,6 +92,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true")
     ap.add_argument("--unfused", action="store_true")
     ap.add_argument("--json", action="store_true", help="print the per-launch records as JSON too")
+    ap.add_argument("--flags", type=int, default=0,
+                    help="qmd_debug_set_launch_flags value for the captured step (e.g. 4: batches of 3..8 "
+                         "on the tensor-core kernel wherever it fits)")
     ap.add_argument("--detail", default=None,
                     help="a projection name: print one of its launches CTA by CTA (SM id, times from the "
                          "previous launch's last exit)")
@@ -115,13 +118,17 @@ def main(argv=None):
     # warm (kernel attributes are set outside the capture), then capture with recording on
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        step.run()
-    torch.cuda.synchronize()
-    q._check(L.qmd_debug_trace(buf.data_ptr(), n_rec))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        step.run()
+    q.debug_set_launch_flags(args.flags)
+    try:
+        with torch.cuda.stream(s):
+            step.run()
+        torch.cuda.synchronize()
+        q._check(L.qmd_debug_trace(buf.data_ptr(), n_rec))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step.run()
+    finally:
+        q.debug_set_launch_flags(0)
     n = L.qmd_debug_trace_launches(None, None, 0)
     first = (ctypes.c_int64 * n)()
     ctas = (ctypes.c_int32 * n)()
@@ -145,7 +152,7 @@ def main(argv=None):
     per = per[len(names) // args.layers:]  # drop the first layer (its first launch has no predecessor in the graph)
     summ = summarise(per)
     periods = [d["period"] for d in per if "period" in d]
-    print(json.dumps({"workload": f"decode step, {args.layers} layers, batch {args.batch}, form {step.form}",
+    print(json.dumps({"workload": f"decode step, {args.layers} layers, batch {args.batch}, form {step.form}, launch flags {args.flags}",
                       "reps": args.reps, "per_projection_us": summ,
                       "layer_us": round(sum(periods) / (args.layers - 1), 3)}, indent=1))
     if args.json:
