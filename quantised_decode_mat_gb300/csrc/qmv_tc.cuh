@@ -341,22 +341,39 @@ __global__ void __launch_bounds__(512, 1) qmv_tc_kernel(const __grid_constant__ 
         float *dx = reinterpret_cast<float *>(smem + L.dx_off);
         int16_t *bs = reinterpret_cast<int16_t *>(smem + L.bs_off);
         const bool out = blockIdx.x == 0 && p.xq_qs_out != nullptr;
-        for (int b = warp; b < B * nb; b += RW) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
-            const float4 xa = src[0], xb = src[1];
-            const float v8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-            const Q8Block q = q8k_quantise_block(v8);
-            *reinterpret_cast<uint2 *>(acts + b * 256 + 8 * lane) = q.codes;
-            if (!Q6 && (lane & 3) == 0)
-                bs[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
-            if (lane == 0)
-                dx[b] = q.d;
-            if (out) {
-                *reinterpret_cast<uint2 *>(p.xq_qs_out + (int64_t)b * 256 + 8 * lane) = q.codes;
-                if ((lane & 3) == 0)
-                    p.xq_bs_out[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
-                if (lane == 0)
-                    p.xq_d_out[b] = q.d;
+        // four blocks' loads in flight per warp, then their four quantisations (a warp packs
+        // B x nb / RW blocks: one round trip to L2 per four instead of per block)
+        constexpr int PK = 4;
+        for (int b0 = warp; b0 < B * nb; b0 += PK * RW) {
+            float4 xa[PK], xb[PK];
+#pragma unroll
+            for (int u = 0; u < PK; ++u) {
+                const int b = b0 + u * RW;
+                if (b < B * nb) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.x + (int64_t)b * 256 + 8 * lane);
+                    xa[u] = src[0];
+                    xb[u] = src[1];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < PK; ++u) {
+                const int b = b0 + u * RW;  // the same for every lane of the warp
+                if (b < B * nb) {
+                    const float v8[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                    const Q8Block q = q8k_quantise_block(v8);
+                    *reinterpret_cast<uint2 *>(acts + b * 256 + 8 * lane) = q.codes;
+                    if (!Q6 && (lane & 3) == 0)
+                        bs[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
+                    if (lane == 0)
+                        dx[b] = q.d;
+                    if (out) {
+                        *reinterpret_cast<uint2 *>(p.xq_qs_out + (int64_t)b * 256 + 8 * lane) = q.codes;
+                        if ((lane & 3) == 0)
+                            p.xq_bs_out[b * 8 + (lane >> 2)] = (int16_t)q.sum4;
+                        if (lane == 0)
+                            p.xq_d_out[b] = q.d;
+                    }
+                }
             }
         }
         __syncthreads();
