@@ -372,28 +372,37 @@ def time_configs(torch, q, device, peak: float, peak_kind: str = "measured") -> 
         for B in c["batches"]:
             xq = q.q8k_pack(torch.from_numpy(synth.activations(c["seed"], B, K)).to(device))
             y = torch.empty((B, rows), dtype=torch.float32, device=device)
-            s = torch.cuda.Stream(device)
-            s.wait_stream(torch.cuda.current_stream(device))
-            with torch.cuda.stream(s):
-                for (Wc, Ac) in copies:  # first launches set kernel attributes outside capture
-                    q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
-            torch.cuda.synchronize(device)
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=s):
-                for (Wc, Ac) in copies:
-                    q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
-            for _ in range(3):
-                gr.replay()
-            ms = time_graph(torch, gr, 10, torch.cuda.current_stream(device)) / ncopy  # replays go there
-            alg = wbytes + B * nb * 276 + B * rows * 4
-            gbs = alg / (ms * 1e-3) / 1e9
-            info = q.launch_info(f, rows, K, B)
-            out[f"config{cid}_b{B}"] = {
-                "shape": f"{fmt} {rows}x{K} batch {B}", "us_per_launch": ms * 1e3, "gbs": gbs,
-                "frac_of_peak": gbs / peak, "peak_kind": peak_kind, "frac_of_nominal_8TBps": gbs / NOMINAL_HBM_GBS,
-                "bytes_per_launch": alg, "weight_copies_rotated": ncopy, "kernel": kernel_name(q, f, rows, K, B),
-                "grid": info["grid"], "threads": info["threads"]}
-            del gr
+            # the default plan; for the short one-vector configs also the split-K form at each
+            # split count the rows allow (qmd_debug_set_split_k), so its cost is on record beside it
+            splits = [0] + ([ks for ks in (2, 3, 4) if ks <= nb // 4] if cid in (0, 1) and B == 1 else [])
+            for ks in splits:
+                q.debug_set_split_k(ks)
+                try:
+                    s = torch.cuda.Stream(device)
+                    s.wait_stream(torch.cuda.current_stream(device))
+                    with torch.cuda.stream(s):
+                        for (Wc, Ac) in copies:  # first launches set kernel attributes outside capture
+                            q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
+                    torch.cuda.synchronize(device)
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=s):
+                        for (Wc, Ac) in copies:
+                            q.qmatvec(f, Wc, Ac, xq, y, rows, s, workspace=ws)
+                    info = q.launch_info(f, rows, K, B)
+                    kname = kernel_name(q, f, rows, K, B)
+                finally:
+                    q.debug_set_split_k(0)
+                for _ in range(3):
+                    gr.replay()
+                ms = time_graph(torch, gr, 10, torch.cuda.current_stream(device)) / ncopy  # replays go there
+                alg = wbytes + B * nb * 276 + B * rows * 4
+                gbs = alg / (ms * 1e-3) / 1e9
+                out[f"config{cid}_b{B}" + (f"_splitk{ks}" if ks else "")] = {
+                    "shape": f"{fmt} {rows}x{K} batch {B}", "us_per_launch": ms * 1e3, "gbs": gbs,
+                    "frac_of_peak": gbs / peak, "peak_kind": peak_kind, "frac_of_nominal_8TBps": gbs / NOMINAL_HBM_GBS,
+                    "bytes_per_launch": alg, "weight_copies_rotated": ncopy, "kernel": kname,
+                    "grid": info["grid"], "threads": info["threads"]}
+                del gr
         del copies
         torch.cuda.empty_cache()
     q.get_device_error()

@@ -342,7 +342,8 @@ qmd_status qmd_qmatvec_launch_info(qmd_fmt fmt, int64_t rows, int64_t K, int bat
 
 /*
  * qmd_qmatvec_launch_kernel -- which kernel qmd_qmatvec would run for these sizes on the current
- * device: 0 the dp4a slice kernel, 1 the tensor-core kernel, 2 the row-lane kernel; a negative
+ * device: 0 the dp4a slice kernel, 1 the tensor-core kernel, 2 the row-lane kernel, 3 the split-K
+ * kernel; a negative
  * qmd_status if the call would be refused.  (Debug launch flags and forced plans apply.)
  */
 int qmd_qmatvec_launch_kernel(qmd_fmt fmt, int64_t rows, int64_t K, int batch);
@@ -422,6 +423,17 @@ void qmd_debug_set_launch_flags(unsigned flags);
  * restores the default.  Results do not depend on it.  Process-wide.
  */
 void qmd_debug_set_dynamic_tiles(int per_mille);
+
+/*
+ * qmd_debug_set_split_k -- split-K for later launches of one or two vectors (plain and fused
+ * forms; "Language models on the device: the cajeta-llm kernels", §2.3: partial sums along K
+ * and a fixup that adds them): each row's groups of four blocks are split over `ctas` CTAs
+ * (2..8) of a thread-block cluster, each packing and multiplying only its slice, and the cluster
+ * adds the slices' group sums in the declared row order through distributed shared memory.
+ * Applies where a row has at least `ctas` groups; any other value restores the default plan.
+ * Results are the same bits either way.  Process-wide.
+ */
+void qmd_debug_set_split_k(int ctas);
 
 /* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
 int qmd_version(void);

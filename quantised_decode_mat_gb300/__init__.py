@@ -94,6 +94,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             "qmd_debug_set_plan": ([i32, i32, i32, i32], None),
             "qmd_debug_set_launch_flags": ([ctypes.c_uint], None),
             "qmd_debug_set_dynamic_tiles": ([i32], None),
+            "qmd_debug_set_split_k": ([i32], None),
             "qmd_version": ([], i32),
         }
         if hasattr(L, "qmd_debug_trace"):  # the traced build (include/qmd_trace.h)
@@ -300,7 +301,7 @@ def launch_info(fmt: int, rows: int, K: int, batch: int) -> dict:
     return dict(zip(("grid", "threads", "smem_bytes", "stages", "rows_per_stage"), (v.value for v in vals)))
 
 
-KERNELS = {0: "qmv_kernel", 1: "qmv_tc_kernel", 2: "qmv_rl_kernel"}
+KERNELS = {0: "qmv_kernel", 1: "qmv_tc_kernel", 2: "qmv_rl_kernel", 3: "qmv_sk_kernel"}
 
 
 def launch_kernel(fmt: int, rows: int, K: int, batch: int) -> str:
@@ -354,6 +355,11 @@ def debug_set_launch_flags(flags: int = 0) -> None:
 
 def debug_set_dynamic_tiles(per_mille: int = -1) -> None:
     lib().qmd_debug_set_dynamic_tiles(int(per_mille))
+
+
+def debug_set_split_k(ctas: int = 0) -> None:
+    """qmd_debug_set_split_k: split each row's blocks over `ctas` CTAs of a cluster (2..8); 0 restores the default."""
+    lib().qmd_debug_set_split_k(int(ctas))
 
 
 def version() -> int:

@@ -15,7 +15,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
-#include "qmv_rl.cuh"
+#include "qmv_splitk.cuh"
 
 namespace qmd {
 
@@ -32,6 +32,7 @@ static __device__ __align__(256) unsigned int g_static_ws[QMD_WORKSPACE_BYTES / 
 static thread_local char g_detail[320];
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 static std::atomic<int> g_force_rg{0}, g_force_rows{0}, g_force_stages{0}, g_force_cps{0};
+static std::atomic<int> g_force_split{0};  // split-K: CTAs per cluster (0: the default plan)
 // Per mille of a row-lane launch's tiles handed out by claims when a workspace is given
 // (measured on the 7B shapes; qmd_debug_set_dynamic_tiles overrides it).
 static constexpr int DYN_PERMILLE = 250;
@@ -300,6 +301,63 @@ static bool rl_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     return true;
 }
 
+// Split-K kernel (qmv_splitk.cuh): clusters of KS CTAs, one CTA per SM, each cluster a range of
+// 8-row tiles and each CTA one of KS slices of every row's groups of four blocks; a ring for as
+// many warps as the range has tiles up to 16 (or the forced row-group count), the deepest ring up to 4 steps (no more than a warp
+// has) that fits beside the activations and the group sums, and up to 16 warps to pack the
+// slice's activations.  false where it does not apply: more than two vectors, fewer groups than
+// slices, or nothing fits.
+static bool sk_plan(int fmt, int64_t rows, int nb, int batch, int KS, const DeviceInfo &dev, QmvPlan *pl)
+{
+    const int gq = (nb + SK_BLOCKS - 1) / SK_BLOCKS;
+    if (batch > SK_MAX_BATCH || KS < 2 || KS > SK_MAX_SPLIT || KS > gq)
+        return false;
+    const int64_t ntiles = (rows + SK_ROWS - 1) / SK_ROWS;
+    int64_t nc = dev.sm_count / KS;
+    if (nc > ntiles)
+        nc = ntiles;
+    if (nc < 1)
+        return false;
+    const int64_t tiles_c = (ntiles + nc - 1) / nc;
+    if (tiles_c > (1 << 20))
+        return false;
+    int W = (int)(tiles_c < SK_MAX_WARPS ? tiles_c : SK_MAX_WARPS);
+    if (g_force_rg.load() > 0)
+        W = g_force_rg.load() < SK_MAX_WARPS ? g_force_rg.load() : SK_MAX_WARPS;
+    const int gs = (gq + KS - 1) / KS;  // the most groups a slice has
+    const int nbs = SK_BLOCKS * gs;
+    int budget = dev.smem_per_sm - 1024;
+    if (budget > dev.smem_optin)
+        budget = dev.smem_optin;
+    const int64_t steps = (tiles_c + W - 1) / W * gs;  // most steps a warp has
+    int S = g_force_stages.load() > 0 ? g_force_stages.load() : 4;
+    if (S > steps)
+        S = (int)steps;
+    for (; S >= 1; --S)
+        if (qmv_sk_layout(fmt, W, S, batch, nbs, (int)(SK_ROWS * tiles_c), gq).total <= budget)
+            break;
+    if (S < 1)
+        return false;
+    const int want = batch * nbs < SK_MAX_WARPS ? batch * nbs : SK_MAX_WARPS;
+    const int NW = W > want ? W : want;
+    pl->layout = 3;
+    pl->grid = (int)(nc * KS);
+    pl->threads = 32 * NW;
+    pl->smem = qmv_sk_layout(fmt, W, S, batch, nbs, (int)(SK_ROWS * tiles_c), gq).total;
+    pl->stages = S;
+    pl->WR = W;
+    pl->RG = 1;
+    pl->PR = SK_ROWS;
+    pl->stage_bytes = sk_slot_bytes(fmt);
+    pl->ksplit = KS;
+    pl->tiles_c = (int)tiles_c;
+    // ring slots per warp requested before the dependency wait (a forced rows-per-stage value
+    // stands for this count here)
+    const int pre = g_force_rows.load() > 0 ? g_force_rows.load() : RL_PRE_STEPS;
+    pl->pre_steps = pre < S ? pre : S;
+    return true;
+}
+
 qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &dev, QmvPlan *pl, int mode)
 {
     const bool q6 = fmt == QMD_Q6_K_SPLIT;
@@ -325,6 +383,13 @@ qmd_status qmv_plan(int fmt, int64_t rows, int nb, int batch, const DeviceInfo &
     pl->tc_rows = 0;
     // One or two vectors: the row-lane kernel, unless a test flag asks for another kernel (three
     // and four on it too when a flag asks).
+    // Split-K where asked (plain and fused forms, one or two vectors, rows of at least as many
+    // groups of four blocks as slices).
+    pl->ksplit = 0;
+    pl->tiles_c = 0;
+    if ((mode == QMV_PLAIN || mode == QMV_PACK) && g_force_split.load() >= 2 &&
+        sk_plan(fmt, rows, nb, batch, g_force_split.load(), dev, pl))
+        return QMD_OK;
     const bool rl_batch = batch <= RL_DEFAULT_BATCH || ((launch_flags() & LAUNCH_RL) && batch <= RL_MAX_BATCH);
     if (rl_batch && !(launch_flags() & (LAUNCH_SLICE | LAUNCH_TC_ALL)) &&
         rl_plan(fmt, rows, nb, batch, dev, pl, mode == QMV_NORM))
@@ -969,6 +1034,8 @@ qmd_status qmd_debug_wait_timeout(uint64_t limit_ns, void *stream)
 }
 
 void qmd_debug_set_launch_flags(unsigned flags) { g_launch_flags.store(flags); }
+
+void qmd_debug_set_split_k(int ctas) { g_force_split.store(ctas >= 2 && ctas <= SK_MAX_SPLIT ? ctas : 0); }
 
 void qmd_debug_set_dynamic_tiles(int per_mille)
 {

@@ -84,12 +84,15 @@ struct QmvArgs {
 int64_t dynamic_tiles(int64_t tiles);
 
 struct QmvPlan {
-    int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh); 2: row-lane kernel (qmv_rl.cuh)
+    int layout;  // 0: dp4a slice kernel (qmv.cuh); 1: tensor-core kernel (qmv_tc.cuh); 2: row-lane kernel (qmv_rl.cuh);
+                 // 3: split-K kernel (qmv_splitk.cuh)
     int grid, threads, smem, stages;
     int WR, RG, PR;  // warps per row group, row groups per CTA, rows per group per stage
     int row_bytes, pre_bytes, stage_bytes, row_stride;
     int tc_rows;  // tensor-core kernel: rows per CTA rounded up to its tile rows (sizes the run sums)
-    int pre_steps = 0;  // row-lane, tensor-core kernels: ring slots per warp requested before the dependency wait
+    int pre_steps = 0;  // row-lane, tensor-core, split-K kernels: ring slots per warp requested before the dependency wait
+    int ksplit = 0;     // split-K kernel: CTAs per cluster, each with a slice of every row's blocks
+    int tiles_c = 0;    // split-K kernel: the most 8-row tiles a cluster's range has
 };
 
 // Launch shape for these sizes on this device; QMD_ERR_SHAPE if K is above the batch's limit.

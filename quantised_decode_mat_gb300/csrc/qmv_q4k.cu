@@ -1,5 +1,5 @@
 // qmv_q4k.cu -- Q4_K instances of the decode mat-vec (batch 1..8, plus the recording variant).
-#include "qmv_rl.cuh"
+#include "qmv_splitk.cuh"
 
 namespace qmd {
 
@@ -14,6 +14,8 @@ qmd_status launch_qmv_q4k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
         return launch_qmv_tc<QMD_Q4_K>(kp, plan, mode, s);
     if (plan.layout == 2)
         return launch_qmv_rl<QMD_Q4_K>(kp, plan, mode, a.batch, s);
+    if (plan.layout == 3)
+        return launch_qmv_sk<QMD_Q4_K>(kp, plan, mode, a.batch, s);
     return launch_qmv_slice<QMD_Q4_K>(kp, plan, a.batch, mode, s);
 }
 

@@ -1,6 +1,6 @@
 // qmv_q6k.cu -- Q6_K (split layout) instances of the decode mat-vec (batch 1..8, plus the
 // recording variant).
-#include "qmv_rl.cuh"
+#include "qmv_splitk.cuh"
 
 namespace qmd {
 
@@ -15,6 +15,8 @@ qmd_status launch_qmv_q6k(const QmvArgs &a, const QmvPlan &plan, cudaStream_t s)
         return launch_qmv_tc<QMD_Q6_K_SPLIT>(kp, plan, mode, s);
     if (plan.layout == 2)
         return launch_qmv_rl<QMD_Q6_K_SPLIT>(kp, plan, mode, a.batch, s);
+    if (plan.layout == 3)
+        return launch_qmv_sk<QMD_Q6_K_SPLIT>(kp, plan, mode, a.batch, s);
     return launch_qmv_slice<QMD_Q6_K_SPLIT>(kp, plan, a.batch, mode, s);
 }
 

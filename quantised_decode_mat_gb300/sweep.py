@@ -4,6 +4,7 @@
         [--warps 8,12,16] [--stages 1,2,3,4] [--pre 1,2,3] [--reps 20]
     python -m quantised_decode_mat_gb300.sweep --step-flags 0,32 [--batch 1] [--layers 32]
     python -m quantised_decode_mat_gb300.sweep --in-step --projection down [--layers 32] [grid as above]
+    python -m quantised_decode_mat_gb300.sweep --projection o --split-k 2,3,4 --warps "" [--in-step]
 
 Makes the decode step of `--layers` layers as bench.py does and, for the default plan and then
 every forced plan of the grid (qmd_debug_set_plan: ring warps per CTA, ring slots per warp, and
@@ -19,7 +20,9 @@ once per value of qmd_debug_set_launch_flags and the graphs are timed in turn, t
 interleaved, 200 replays each; printed as GB/s over the step's algorithmic bytes.  With
 --in-step, the grid of plans is applied to the chosen projection's launches only, inside the
 whole step (a plan is fixed when a launch is captured, so the other projections keep their
-default plans), each plan's step timed the same way.
+default plans), each plan's step timed the same way.  --split-k adds the split-K form at each
+of the given cluster sizes (qmd_debug_set_split_k), with each --pre value as its slots requested
+before the dependency wait, to either mode.
 """
 from __future__ import annotations
 
@@ -43,11 +46,12 @@ def main(argv=None) -> int:
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--step-flags", default=None, help="time the whole step under each of these launch-flag values")
     ap.add_argument("--in-step", action="store_true", help="force the plans on one projection inside the whole step")
+    ap.add_argument("--split-k", default="", help="also the split-K form at these CTAs per cluster")
     args = ap.parse_args(argv)
 
     import torch
-    from . import (debug_set_launch_flags, debug_set_plan, get_device_error, launch_info, lib, q8k_pack, qmatvec,
-                   qmatvec_x)
+    from . import (debug_set_launch_flags, debug_set_plan, debug_set_split_k, get_device_error, launch_info, lib,
+                   q8k_pack, qmatvec, qmatvec_x)
     from .step import make_step
 
     lib()
@@ -123,21 +127,25 @@ def main(argv=None) -> int:
     print("|---|---|---:|---:|")
     print(f"| default | {info['grid']} x {info['threads']}, {info['stages']} | {us:.2f} | {alg / us / 1e3:.0f} |")
     rows = []
+    grid = [(0, w, s, pre) for w, s, pre in itertools.product(_ints(args.warps), _ints(args.stages), _ints(args.pre))
+            if pre <= s]
+    grid += [(ks, 0, 0, pre) for ks, pre in itertools.product(_ints(args.split_k), _ints(args.pre))]
     try:
-        for w, s, pre in itertools.product(_ints(args.warps), _ints(args.stages), _ints(args.pre)):
-            if pre > s:
-                continue
+        for ks, w, s, pre in grid:
+            debug_set_split_k(ks)
             debug_set_plan(w, pre, s, 0)
             info = launch_info(p0.fmt, p0.rows, p0.K, args.batch)
             us = time_plan()
             same = torch.equal(torch.cat([p.y.reshape(-1) for p in ps]).view(torch.int32), ref.view(torch.int32))
             rows.append((us, w, s, pre))
-            print(f"| {w}, {s}, {pre} | {info['grid']} x {info['threads']}, {info['stages']} | {us:.2f} | "
+            name = f"split-K {ks}, {info['stages']}, {pre}" if ks else f"{w}, {s}, {pre}"
+            print(f"| {name} | {info['grid']} x {info['threads']}, {info['stages']} | {us:.2f} | "
                   f"{alg / us / 1e3:.0f} |" + ("" if same else " OUTPUTS DIFFER"), flush=True)
             if not same:
                 return 1
     finally:
         debug_set_plan()
+        debug_set_split_k(0)
     if rows:
         best = min(rows)
         print(f"\nfastest forced plan: {best[1]} warps, {best[2]} slots, {best[3]} before the wait: {best[0]:.2f} µs")
@@ -155,31 +163,37 @@ def _launch(p, ws):
 
 def _in_step(args, st, torch) -> int:
     """The whole step with the grid's plans forced on one projection's launches only."""
-    from . import debug_set_plan, get_device_error, launch_info
+    from . import debug_set_plan, debug_set_split_k, get_device_error, launch_info
     nbytes = st.bytes()["algorithmic"]
     p0 = [p for p in st.projs if p.name == args.projection][0]
-    plans = [None] + [(w, pre, s) for w, s, pre in itertools.product(_ints(args.warps), _ints(args.stages),
-                                                                      _ints(args.pre)) if pre <= s]
+    # (ring warps, slots before the wait, ring slots, split-K CTAs per cluster)
+    plans = [None] + [(w, pre, s, 0) for w, s, pre in itertools.product(_ints(args.warps), _ints(args.stages),
+                                                                         _ints(args.pre)) if pre <= s]
+    plans += [(0, pre, 0, ks) for ks, pre in itertools.product(_ints(args.split_k), _ints(args.pre))]
+
+    def force(plan):
+        if plan is None:
+            debug_set_plan()
+            debug_set_split_k(0)
+        else:
+            debug_set_plan(plan[0], plan[1], plan[2], 0)
+            debug_set_split_k(plan[3])
 
     def capture(plan):
         def run():
             try:
                 for p in st.projs:
-                    if plan is not None and p.name == args.projection:
-                        debug_set_plan(plan[0], plan[1], plan[2], 0)
-                    else:
-                        debug_set_plan()
+                    force(plan if p.name == args.projection else None)
                     _launch(p, st.ws)
             finally:
-                debug_set_plan()
+                force(None)
         return st.capture(run)
 
     graphs, used = {}, {}
     for plan in plans:
-        if plan is not None:
-            debug_set_plan(plan[0], plan[1], plan[2], 0)
+        force(plan)
         info = launch_info(p0.fmt, p0.rows, p0.K, args.batch)
-        debug_set_plan()
+        force(None)
         used[plan] = f"{info['grid']} x {info['threads']}, {info['stages']}"
         graphs[plan] = capture(plan)
     res = {plan: [] for plan in plans}
@@ -203,7 +217,8 @@ def _in_step(args, st, torch) -> int:
     print("| plan on it (warps, slots, before wait) | used: grid x threads, slots | step GB/s, three rounds |")
     print("|---|---|---|")
     for plan in plans:
-        name = "default" if plan is None else f"{plan[0]}, {plan[2]}, {plan[1]}"
+        name = ("default" if plan is None else f"split-K {plan[3]}, -, {plan[1]}" if plan[3]
+                else f"{plan[0]}, {plan[2]}, {plan[1]}")
         print(f"| {name} | {used[plan]} | " + ", ".join(f"{x:.0f}" for x in res[plan]) + " |")
     return 0
 

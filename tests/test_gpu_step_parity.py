@@ -23,19 +23,29 @@ TOL_F64 = 2e-3
 OFMT = {q.Q4_K: O.FMT_Q4_K, q.Q6_K_SPLIT: O.FMT_Q6_K}
 
 
-@pytest.fixture(scope="module", params=[1, 4, 8], ids=["b1", "b4", "b8"])
+@pytest.fixture(scope="module", params=[(1, 0), (4, 0), (8, 0), (1, 2), (1, 4)],
+                ids=["b1", "b4", "b8", "b1-splitk2", "b1-splitk4"])
 def step(request):
+    """The 2-layer step at one batch; the split-K cases run every projection of it split over
+    clusters of 2 or 4 CTAs (qmd_debug_set_split_k)."""
     from quantised_decode_mat_gb300 import build as qbuild
     from quantised_decode_mat_gb300 import step as qstep
     qbuild.build()
     q.lib()
     q.debug_set_plan()
     q.debug_set_launch_flags(0)
-    s = qstep.make_step(request.param, layers=2, device="cuda", keep_host_layers=(0, 1))
-    s.y_all.fill_(float("nan"))
-    s.run()
-    torch.cuda.synchronize()
-    q.get_device_error()
+    batch, ks = request.param
+    q.debug_set_split_k(ks)
+    try:
+        s = qstep.make_step(batch, layers=2, device="cuda", keep_host_layers=(0, 1))
+        if ks:
+            assert all(q.launch_kernel(p.fmt, p.rows, p.K, batch) == "qmv_sk_kernel" for p in s.projs)
+        s.y_all.fill_(float("nan"))
+        s.run()
+        torch.cuda.synchronize()
+        q.get_device_error()
+    finally:
+        q.debug_set_split_k(0)
     return s
 
 
