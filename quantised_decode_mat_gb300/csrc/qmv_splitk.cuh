@@ -54,6 +54,14 @@ __host__ __device__ constexpr int sk_slot_bytes(int f) { return sk_box_bytes(f) 
 __host__ __device__ constexpr int sk_g0(int k, int gq, int KS) { return (k * gq) / KS; }
 // the rank whose slice holds group g: the largest k with sk_g0(k) <= g
 __host__ __device__ constexpr int sk_owner(int g, int gq, int KS) { return ((g + 1) * KS - 1) / gq; }
+// the 8-row tiles [c0, c1) of cluster cid of NC: an even split of ntiles, the first
+// ntiles % NC clusters one tile more
+__host__ __device__ inline void sk_cluster_tiles(int64_t cid, int64_t NC, int64_t ntiles, int64_t *c0, int64_t *c1)
+{
+    const int64_t tq = ntiles / NC, trem = ntiles - tq * NC;
+    *c0 = cid * tq + (cid < trem ? cid : trem);
+    *c1 = *c0 + tq + (cid < trem ? 1 : 0);
+}
 
 struct SkLayout {
     int bar_off, act_off, dx_off, aux_off, part_off, total;
@@ -158,8 +166,8 @@ __global__ void __launch_bounds__(32 * SK_MAX_WARPS, 1) qmv_sk_kernel(const __gr
     const int nbl = min(nb, SK_BLOCKS * g1) - blk0;      // and its block count
     // the cluster's tiles: an even split of the 8-row tiles over the clusters
     const int64_t ntiles = (p.rows + SK_ROWS - 1) / SK_ROWS;
-    const int64_t tq = ntiles / NC, trem = ntiles - tq * NC;
-    const int64_t c0 = (int64_t)cid * tq + min((int64_t)cid, trem), c1 = c0 + tq + ((int64_t)cid < trem ? 1 : 0);
+    int64_t c0, c1;
+    sk_cluster_tiles(cid, NC, ntiles, &c0, &c1);
     const int rows_c = SK_ROWS * sp.tiles_c;
     const SkLayout L = qmv_sk_layout(F, W, S, B, nbs, rows_c, gq);
     // A launch whose geometry is not the plan's: flag it and leave without touching memory.  Every
